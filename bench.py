@@ -1,0 +1,378 @@
+"""Throughput of the fused trellis-MoE layer on synthetic inputs.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                [--workload decode|prefill|odd|large-decode|large-prefill] [--tokens T]
+
+One step is one pass of the whole hot path over one token batch: router on the
+logits, route map, fused rotate+quantize, FC1 with its activation epilogue,
+FC2 with the unrotation epilogue, and the top-k combine -- all in the
+library's CUDA kernels, replayed from CUDA graphs captured per batch.
+
+The default workload is the decode layer (H=1024, I=512, E=128, top-k 8,
+W4A8, K=4 trellis) at T=8 tokens per step. Its touched weights (~41 MB per
+step) would sit in the 129 MB L2, so the step cycles through several copies of
+the layer living at different addresses (touched bytes between two uses of one
+copy exceed 2x L2) and through as many token batches.
+
+Output: one JSON line on rank 0. ``roofline`` is for the dominant kernel
+(FC1): algorithmic bytes (or FLOPs) per launch divided by its CUDA-event
+duration, timed inside the captured graphs of the timed region.
+``cpu_baseline`` times the float64 CPU oracle on a bounded sample.
+``--impl reference`` runs only that oracle (the CPU reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from trellis_quantized_moe_route_gb300 import synth  # noqa: E402
+
+METRIC = "fused trellis-MoE layer tokens/s (decode T=1-8, prefill T=2048); % of roofline"
+L2_BYTES = 129e6
+
+WORKLOADS = {
+    # name: (config, T, mode)
+    "decode": ("decode", 8, "w4a8"),
+    "prefill": ("prefill", 2048, "w4a16"),
+    "odd": ("odd", 512, "w4a16"),
+    "large-decode": ("large", 1, "w4a8"),
+    "large-prefill": ("large", 4096, "w4a16"),
+}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.samples = []
+        self._stop = threading.Event()
+        self._t = None
+
+    def _query(self):
+        try:
+            r = subprocess.run(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=5)
+            if r.returncode == 0 and r.stdout.strip():
+                self.samples.append([v.strip() for v in r.stdout.strip().split(",")])
+        except Exception:
+            pass
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._query()
+            self._stop.wait(self.period / 1000.0)
+
+    def start(self):
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+
+    def stop(self):
+        self._stop.set()
+        if self._t:
+            self._t.join()
+        self._query()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        sm = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for s in self.samples:
+            for n, v in zip(names, s[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------- ours ---
+def touched_bytes_fc1(cfg, ids, T):
+    """Algorithmic DRAM bytes of one FC1 launch: trellis payload, per-channel
+    scales and rotation rows of every touched expert, the quantised input rows
+    read, and the FC1 epilogue's output rows written."""
+    E, H, I = cfg.E, cfg.H, cfg.I
+    K = max(cfg.bits)
+    d = len(np.unique(ids))
+    R = ids.size
+    act_b = 1 if WORK_MODE[0] == "w4a8" else 2
+    weights = d * (2 * I * H * K // 8 + 2 * I * 2 + 3 * I * 2)
+    acts = T * H * act_b + (T * H // 32 if act_b == 1 else 0)
+    outs = R * I * act_b + (R * I // 32 if act_b == 1 else 0)
+    return weights + acts + outs, d
+
+
+WORK_MODE = ["w4a8"]
+
+
+def run_ours(args, rank, world):
+    import torch
+    from trellis_quantized_moe_route_gb300 import binding, build
+
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    build.build()
+    binding.load_library()
+    cfg_name, T_default, mode = WORKLOADS[args.workload]
+    WORK_MODE[0] = mode
+    cfg = synth.CONFIGS[cfg_name]
+    T = args.tokens or T_default
+    K = max(cfg.bits)
+    R = T * cfg.topk
+
+    # layer copies at distinct addresses so that the bytes touched between two
+    # uses of one copy exceed twice the L2
+    layer = synth.make_layer(cfg)
+    per_expert = 3 * cfg.H * cfg.I * K // 8
+    touched_est = min(cfg.E, R) * per_expert
+    copies = int(min(16, max(1, np.ceil(2 * L2_BYTES / max(touched_est, 1)) + 1)))
+    moes = [binding.TrellisMoE(layer, max_tokens=T) for _ in range(copies)]
+    batches = []
+    for b in range(copies):
+        x_bits, logits = synth.make_tokens(cfg, T=T, seed=1000 + 17 * rank + b)
+        x = torch.from_numpy(np.ascontiguousarray(x_bits.view(np.int16))).cuda()
+        lg = torch.from_numpy(np.ascontiguousarray(logits)).cuda()
+        out = torch.empty((T, cfg.H), dtype=torch.float32, device="cuda")
+        batches.append((x, lg, out, x_bits, logits))
+    stream = torch.cuda.Stream()
+
+    # warm-up (eager; also fixes kernel attributes before capture)
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 1)):
+            b = i % copies
+            moes[b].forward_logits(batches[b][0], batches[b][1], mode=mode, out=batches[b][2])
+    torch.cuda.synchronize()
+
+    # one graph per (copy, batch), each with its own stage events
+    graphs, evsets = [], []
+    for b in range(copies):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+        for ev in evs:
+            ev.record(stream)
+        torch.cuda.synchronize()
+        moes[b].set_stage_events(evs)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            moes[b].forward_logits(batches[b][0], batches[b][1], mode=mode, out=batches[b][2])
+        moes[b].set_stage_events(None)
+        graphs.append(g)
+        evsets.append(evs)
+    for i in range(max(args.warmup, 3)):
+        graphs[i % copies].replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            graphs[i % copies].replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([total_ms], dtype=torch.float64)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+
+    # stage times of the most recent replay of every graph (inside the timed region)
+    stage = {k: [] for k in ("router", "route_map", "rotate", "fc1", "fc2", "combine", "step")}
+    for evs in evsets:
+        e = [evs[i] for i in range(7)]
+        stage["router"].append(e[0].elapsed_time(e[1]) * 1e3)
+        stage["route_map"].append(e[1].elapsed_time(e[2]) * 1e3)
+        stage["rotate"].append(e[2].elapsed_time(e[3]) * 1e3)
+        stage["fc1"].append(e[3].elapsed_time(e[4]) * 1e3)
+        stage["fc2"].append(e[4].elapsed_time(e[5]) * 1e3)
+        stage["combine"].append(e[5].elapsed_time(e[6]) * 1e3)
+        stage["step"].append(e[0].elapsed_time(e[6]) * 1e3)
+    stages_us = {k: round(statistics.mean(v), 3) for k, v in stage.items()}
+
+    # algorithmic work per FC1 launch, from each batch's routes
+    fc1_bytes, distinct = [], []
+    for b in range(copies):
+        ids, _ = binding.route(batches[b][1], cfg.topk)
+        nb, d = touched_bytes_fc1(cfg, ids.cpu().numpy(), T)
+        fc1_bytes.append(nb)
+        distinct.append(d)
+    pk = peaks()
+    if mode == "w4a8" and T <= 64:
+        achieved = statistics.mean(fc1_bytes) / (stages_us["fc1"] * 1e-6) / 1e9
+        roof = {"bound": "hbm", "kernel": "k_fc<W4A8,FC1>", "achieved": round(achieved, 1),
+                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                "traffic": None, "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst)",
+                "bytes_per_launch": int(statistics.mean(fc1_bytes))}
+    else:
+        flops = 2 * R * 2 * cfg.I * cfg.H
+        achieved = flops / (stages_us["fc1"] * 1e-6) / 1e12
+        roof = {"bound": "tensor", "kernel": "k_fc<W4A16,FC1>", "achieved": round(achieved, 2),
+                "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4),
+                "traffic": None, "peak_source": pk["source"] + " (bf16 dense burst; fp16 runs at the bf16 rate)",
+                "flops_per_launch": flops}
+
+    # end to end through the host-buffer C-ABI call
+    e2e_steps = min(args.steps, 200)
+    xh = [torch.from_numpy(np.ascontiguousarray(b[3].view(np.int16))).pin_memory() for b in batches]
+    lh = [torch.from_numpy(np.ascontiguousarray(b[4])).pin_memory() for b in batches]
+    oh = [torch.empty((T, cfg.H), dtype=torch.float32).pin_memory() for _ in batches]
+    with torch.cuda.stream(stream):
+        for i in range(min(3, copies)):
+            moes[i].forward_host(xh[i], lh[i], oh[i], mode=mode)
+    torch.cuda.synchronize()
+    h0 = torch.cuda.Event(enable_timing=True)
+    h1 = torch.cuda.Event(enable_timing=True)
+    h0.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(e2e_steps):
+            b = i % copies
+            moes[b].forward_host(xh[b], lh[b], oh[b], mode=mode)
+    h1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = h0.elapsed_time(h1)
+    e2e = {"value": round(e2e_steps * T * world / (e2e_ms / 1e3), 2), "unit": "tokens/s",
+           "h2d_bytes_per_step": T * cfg.H * 2 + T * cfg.E * 4, "d2h_bytes_per_step": T * cfg.H * 4,
+           "steps": e2e_steps, "api": "trellis_moe_forward_host"}
+
+    launches_per_step = 6 + (2 if R > 1024 else 0)
+    res = {
+        "metric": METRIC, "value": round(args.steps * T * world / (total_ms / 1e3), 2), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3" if mode == "w4a8" else "f16", "data": "synthetic",
+        "config": {"workload": "%s: H=%d I=%d E=%d top-k=%d K=%d %s T=%d" % (
+            args.workload, cfg.H, cfg.I, cfg.E, cfg.topk, K, mode.upper(), T),
+            "tokens_per_step": T, "layer_copies": copies,
+            "l2": "inputs larger than L2: %d layer copies and token batches cycled" % copies,
+            "distinct_experts_per_step": round(statistics.mean(distinct), 2),
+            "graphs": "one CUDA graph per (layer copy, batch), replayed"},
+        "roofline": roof, "stages_us": stages_us,
+        "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": sampler.summary(),
+    }
+    return res, (cfg, T, mode, batches)
+
+
+# -------------------------------------------------------------- reference ---
+def oracle_sample(cfg, T, mode, budget_s, seed=1000):
+    """Time the float64 CPU oracle on whole batches of the workload (or on a
+    prefix of one batch) for about ``budget_s`` seconds. Returns (tokens/s,
+    description)."""
+    from oracle import layer as olayer, route as oroute
+    L = synth.make_layer(cfg)
+    x_bits, logits = synth.make_tokens(cfg, T=T, seed=seed)
+    done, t_start = 0, time.perf_counter()
+    n = min(T, 8)
+    while True:
+        toks = np.arange(done % T, done % T + n) % T
+        ids, w = oroute.route_topk_softmax(logits[toks], cfg.topk)
+        olayer.layer_forward(L, x_bits[toks], ids, w, mode=mode)
+        done += n
+        el = time.perf_counter() - t_start
+        if el > budget_s:
+            break
+    return done / el, "%d tokens of the %s workload in %.1f s (oracle: router, per-expert decode, float64 GEMMs)" % (
+        done, cfg.name, el)
+
+
+def cpu_baseline(cfg, T, mode, budget_s=12.0):
+    v, desc = oracle_sample(cfg, T, mode, budget_s)
+    return {"value": round(v, 3), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle", "sample": desc}
+
+
+def run_reference(args, rank, world):
+    cfg_name, T_default, mode = WORKLOADS[args.workload]
+    cfg = synth.CONFIGS[cfg_name]
+    T = args.tokens or T_default
+    budget = max(1.0, min(8.0, 150.0 / max(args.steps + args.warmup, 1)))
+    for _ in range(min(args.warmup, 2)):
+        oracle_sample(cfg, T, mode, 0.0)
+    vals = []
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        v, desc = oracle_sample(cfg, T, mode, budget, seed=2000 + i)
+        vals.append(v)
+        if time.perf_counter() - t0 > 170.0:
+            break
+    value = statistics.mean(vals)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * min(T, 8) / value, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "%s: H=%d I=%d E=%d top-k=%d %s T=%d" % (args.workload, cfg.H, cfg.I, cfg.E,
+                                                                      cfg.topk, mode.upper(), T)},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": "%d steps of about %.1f s each, up to 8 tokens per oracle call (%s)" % (
+                             len(vals), budget, desc)},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--tokens", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("gloo")
+    res, (cfg, T, mode, _) = run_ours(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(cfg, T, mode)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

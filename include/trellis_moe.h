@@ -1,0 +1,197 @@
+/*
+ * trellis_moe.h -- C ABI of a fused mixture-of-experts layer whose expert
+ * weights are bitshift-trellis codes, for NVIDIA GB300 (sm_103a).
+ *
+ * What the layer computes (sources are four pull-request pages, cited by title
+ * and section):
+ *   1. route:    top-k expert ids and weights from router logits (optional);
+ *   2. route map: per-expert counts, padded exclusive scan, stable route order
+ *                (sparkinfer PR #90 "moe: integrate EXL3 Trellis into the fused
+ *                W4A16 API", review of route_pack.py; b12x PR #433 "Share
+ *                trellis preparation across native and EXL3 containers",
+ *                review of route_pack.py);
+ *   3. x~ = H_b(suh * x), one kernel that also quantises it: fp16 for W4A16,
+ *      MXFP8 (E4M3 + one E8M0 exponent per 32) for W4A8 (b12x PR #129
+ *      "feat(moe): serve canonical Fruit QSRT atoms", Hot path);
+ *   4. FC1 gate/up grouped GEMM over route-major rows, expanding 256-weight
+ *      trellis tiles (16*K int16 words, 16-bit tail-biting state, MCG codebook
+ *      0xCBAC1FED / 0x8fff8fff / 0x3b603b60, per-output-channel fp16 scales)
+ *      straight into MMA operands -- dense weights are never written to
+ *      memory (same page, Hot path; sparkinfer PR #90, review of
+ *      intrinsics.py and prepare.py);
+ *   5. fused epilogue: H -> svh -> SiLU(gate)*up -> suh_down -> H (sparkinfer
+ *      PR #90, review of kernel.py: _run_activation);
+ *   6. FC2 route-major grouped GEMM with the same decode, then the output
+ *      rotation is undone (H, down_svh);
+ *   7. top-k weighted combine into an FP32 output, in fixed slot order
+ *      (deterministic) or by FP32 atomics (opt-in, not bitwise reproducible:
+ *      b12x PR #433, conversation: "does not guarantee bitwise summation
+ *      order").
+ *
+ * Conventions for every entry point:
+ *   - Pointers named *_host are host memory; all others are device memory of
+ *     the current CUDA device, owned by the caller, never freed by the library.
+ *   - "fp16" / "bf16" arrays are passed as uint16_t bit patterns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - Every argument is validated on the host before any launch; a call that
+ *     returns an error has launched nothing and written nothing.
+ *   - Errors: a negative tm_status; trellis_moe_last_error() gives a message
+ *     for the calling thread.
+ *   - No entry point other than trellis_moe_prepare allocates device memory.
+ *     trellis_moe_forward* use only the caller's workspace, launch only on
+ *     `stream`, and can be captured in a CUDA graph (the workspace pointer must
+ *     then stay the same for every replay).
+ */
+#ifndef TRELLIS_MOE_H_
+#define TRELLIS_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct tm_layer tm_layer; /* opaque; created by prepare, freed by destroy */
+
+typedef enum {
+  TM_OK = 0,
+  TM_EINVAL = -1,        /* bad argument (null pointer, shape, range, alignment) */
+  TM_EUNSUPPORTED = -2,  /* well-formed but outside what this build implements */
+  TM_EWORKSPACE = -3,    /* workspace missing, too small or misaligned */
+  TM_ECUDA = -4,         /* a CUDA runtime call failed */
+  TM_EDEVICE = -5        /* a kernel reported bad device data (see poll_error) */
+} tm_status;
+
+typedef enum {
+  TM_MODE_AUTO = 0,   /* W4A8 when T <= decode_max_rows, else W4A16 */
+  TM_MODE_W4A16 = 1,  /* fp16 activations x fp16 codebook weights, fp32 accumulate */
+  TM_MODE_W4A8 = 2    /* MXFP8 activations x E4M3-rounded codebook weights */
+} tm_mode;
+
+/* Layer description. Device arrays must stay valid until trellis_moe_destroy. */
+typedef struct {
+  int32_t E;              /* experts, 1..256 */
+  int32_t H;              /* hidden size, multiple of 128 */
+  int32_t I;              /* intermediate size per half, multiple of 64 */
+  int32_t topk;           /* experts per token, 1..min(E, 32) */
+  int32_t rot_block_h;    /* Hadamard block on H: 1 (identity), 64 or 128 */
+  int32_t rot_block_i;    /* Hadamard block on I: 1, 64 or 128 (must divide I) */
+  const uint8_t* bits_per_expert; /* HOST [E], trellis bits K_e in 2..6 */
+  /* Payload words, experts concatenated in order. Expert e's FC1 block is
+   * [2I/16][H/16][16*K_e] int16 (tile rows = output channels: rows 0..I-1 gate,
+   * I..2I-1 up); its FC2 block is [H/16][I/16][16*K_e]. Base 16-byte aligned. */
+  const int16_t* fc1_payload;
+  const int16_t* fc2_payload;
+  const uint16_t* fc1_scale;  /* fp16 [E, 2I] per-output-channel scale */
+  const uint16_t* fc2_scale;  /* fp16 [E, H] */
+  const uint16_t* in_suh;     /* fp16 [H] input signs (shared by gate and up) */
+  const uint16_t* rot_tab;    /* fp16 [E, 3I] = gate svh | up svh | down suh */
+  const uint16_t* out_svh;    /* fp16 [E, H] output (down) svh */
+  int32_t max_tokens;         /* largest T any forward call will pass, >= 1 */
+  int32_t decode_max_rows;    /* AUTO picks W4A8 iff T <= this (default 8) */
+  int32_t deterministic;      /* 1: fixed-order FP32 combine; 0: FP32 atomics */
+} tm_layer_desc;
+
+/* Validate `desc`, upload the per-expert offset tables and return a handle and
+ * the workspace size (bytes) a forward call of up to desc->max_tokens tokens
+ * needs. Allocates only the small descriptor tables; call before any stream
+ * capture. Errors: TM_EINVAL / TM_EUNSUPPORTED / TM_ECUDA; *out is then NULL. */
+tm_status trellis_moe_prepare(const tm_layer_desc* desc, tm_layer** out, size_t* workspace_bytes);
+
+/* Workspace bytes for forward calls of up to `max_tokens` tokens (<= the
+ * prepared max_tokens). */
+size_t trellis_moe_workspace_size(const tm_layer* layer, int32_t max_tokens);
+
+/* Full layer from given routes.
+ *   x        bf16 [T, H] activations
+ *   topk_ids int32 [T, topk] expert ids; out-of-range ids are dropped from the
+ *            sum and flagged in the device error word (trellis_moe_poll_error)
+ *   topk_w   fp32 [T, topk] route weights
+ *   mode     tm_mode
+ *   out      fp32 [T, H] result (overwritten)
+ *   workspace >= trellis_moe_workspace_size(layer, T) bytes, 256-byte aligned;
+ *            contents on entry are ignored (any bytes give the same result).
+ * T = 0 is a no-op. Errors: TM_EINVAL, TM_EWORKSPACE, TM_ECUDA. */
+tm_status trellis_moe_forward(tm_layer* layer, const uint16_t* x, const int32_t* topk_ids,
+                              const float* topk_w, int32_t T, int32_t mode, float* out,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* Router + full layer: logits fp32 [T, E] are routed on the device (top-k,
+ * softmax over the selected logits) into the workspace, then as forward. */
+tm_status trellis_moe_forward_logits(tm_layer* layer, const uint16_t* x, const float* logits,
+                                     int32_t T, int32_t mode, float* out,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* As forward_logits, but x_host, logits_host and out_host are HOST buffers
+ * (pinned memory recommended). Copies the inputs into the workspace, runs the
+ * layer and copies the result back, all on `stream`, then synchronises the
+ * stream. Workspace: trellis_moe_workspace_size(layer, T) bytes. */
+tm_status trellis_moe_forward_host(tm_layer* layer, const uint16_t* x_host,
+                                   const float* logits_host, int32_t T, int32_t mode,
+                                   float* out_host, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
+/* Top-k softmax router. logits fp32 [T, E] -> ids int32 [T, k] (descending
+ * logit, ties to the lower id) and w fp32 [T, k] = softmax over the k selected
+ * logits. E <= 256, 1 <= k <= min(E, 32). No workspace. */
+tm_status trellis_moe_route(const float* logits, int32_t T, int32_t E, int32_t k,
+                            int32_t* ids, float* w, void* stream);
+
+/* Route map of topk_ids int32 [T, topk] with expert segments padded to `block`
+ * (1..256): counts int32 [E], offsets int32 [E+1] (padded exclusive scan),
+ * route_of_slot int32 [offsets[E]] (route r = t*topk + j, -1 for padding;
+ * within an expert in ascending r), slot_of_route int32 [T*topk] (-1 for a
+ * dropped id). The caller sizes route_of_slot for the worst case
+ * T*topk + E*(block-1). Uses the workspace for scratch. */
+tm_status trellis_moe_route_map(tm_layer* layer, const int32_t* topk_ids, int32_t T, int32_t block,
+                                int32_t* counts, int32_t* offsets, int32_t* route_of_slot,
+                                int32_t* slot_of_route, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/* Step 3 alone: x bf16 [T, H] -> W4A16: fp16 [T, H] into xq; W4A8: E4M3 bytes
+ * [T, H] into xq and E8M0 bytes [T, H/32] into xs (xs unused for W4A16). */
+tm_status trellis_moe_rotate_quant(tm_layer* layer, const uint16_t* x, int32_t T, int32_t mode,
+                                   void* xq, uint8_t* xs, void* stream);
+
+/* Decode `ntiles` tiles of expert `expert`'s projection `proj` (1 = FC1,
+ * 2 = FC2) starting at tile index `tile0` (row-tile major order) into dst:
+ * W4A16 -> fp16 bits [ntiles][256], W4A8 -> E4M3 bytes [ntiles][256], in
+ * in-tile weight order j (row j/16, column j%16). For parity tests. */
+tm_status trellis_moe_decode_tiles(tm_layer* layer, int32_t proj, int32_t expert, int32_t tile0,
+                                   int32_t ntiles, int32_t mode, void* dst, void* stream);
+
+/* Where a forward call of `T` tokens keeps its intermediates inside the
+ * workspace (for tests): which = 0 x~ (fp16 or E4M3), 1 x~ E8M0 exponents,
+ * 2 FC1 epilogue output z~ (fp16 or E4M3), 3 z~ E8M0 exponents, 4 per-slot
+ * FC2 output (fp32 [slots, H]), 5 slot_of_route (int32 [T*topk]),
+ * 6 device error word (uint32). Returns TM_EINVAL for an unknown `which`. */
+tm_status trellis_moe_workspace_region(const tm_layer* layer, int32_t T, int32_t which,
+                                       size_t* offset, size_t* bytes);
+
+/* Stage timing for benchmarks and profilers. With `events` non-NULL (n = 7
+ * cudaEvent_t handles created by the caller, NULL entries skipped), every later
+ * forward call on this handle records events[i] on its stream, with
+ * cudaEventRecordExternal so that the records also become nodes of a captured
+ * CUDA graph, at these boundaries: 0 start, 1 after the router (forward_logits
+ * and forward_host only), 2 after the route map, 3 after rotate+quantize,
+ * 4 after FC1, 5 after FC2, 6 after the combine. events = NULL or n = 0 turns
+ * recording off. The handles are copied; the caller keeps ownership. */
+tm_status trellis_moe_set_stage_events(tm_layer* layer, void* const* events, int32_t n);
+
+/* Read and clear the device error word of `workspace` (synchronises `stream`).
+ * *flags: bit 0 = an expert id was out of range. Returns TM_EDEVICE if any flag
+ * was set, else TM_OK. */
+tm_status trellis_moe_poll_error(tm_layer* layer, void* workspace, uint32_t* flags, void* stream);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* trellis_moe_last_error(void);
+
+/* Free the handle and its descriptor tables (not the caller's arrays). */
+void trellis_moe_destroy(tm_layer* layer);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TRELLIS_MOE_H_ */

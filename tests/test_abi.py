@@ -1,0 +1,66 @@
+"""The C ABI library builds, loads and exports every entry point the public
+header declares; host-side argument validation runs without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "trellis_moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from trellis_quantized_moe_route_gb300 import binding, build
+    build.build()
+    return binding.load_library()
+
+
+def declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(trellis_moe_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared()
+    for must in ("trellis_moe_prepare", "trellis_moe_forward", "trellis_moe_route", "trellis_moe_destroy"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from trellis_quantized_moe_route_gb300 import binding
+    for name in declared():
+        assert hasattr(lib, name), name
+    assert sorted(binding.EXPORTED) == declared()
+
+
+def test_host_validation_without_gpu(lib):
+    from trellis_quantized_moe_route_gb300 import binding
+    P = ctypes.c_void_p
+    # router: k outside 1..min(E, 32) is rejected before any CUDA call
+    assert lib.trellis_moe_route(P(8), 4, 8, 0, P(8), P(8), None) == -1
+    assert b"k=0" in lib.trellis_moe_last_error()
+    assert lib.trellis_moe_route(P(8), 4, 300, 2, P(8), P(8), None) == -2
+    # prepare without a descriptor
+    h = ctypes.c_void_p()
+    assert lib.trellis_moe_prepare(None, ctypes.byref(h), None) == -1
+    # prepare with unsupported shapes fails before touching the device
+    d = binding.LayerDesc()
+    d.E, d.H, d.I, d.topk, d.rot_block_h, d.rot_block_i = 8, 100, 64, 2, 128, 64
+    assert lib.trellis_moe_prepare(ctypes.byref(d), ctypes.byref(h), None) == -2
+    assert b"H=100" in lib.trellis_moe_last_error()
+    d.H = 256
+    d.rot_block_i = 32
+    assert lib.trellis_moe_prepare(ctypes.byref(d), ctypes.byref(h), None) == -2
+    d.rot_block_i, d.topk = 64, 9
+    assert lib.trellis_moe_prepare(ctypes.byref(d), ctypes.byref(h), None) == -1
+    d.topk, d.max_tokens = 2, 4
+    bits = (ctypes.c_uint8 * 8)(*([4] * 8))
+    d.bits_per_expert = ctypes.cast(bits, ctypes.c_void_p)
+    assert lib.trellis_moe_prepare(ctypes.byref(d), ctypes.byref(h), None) == -1   # NULL payload
+    assert b"fc1_payload" in lib.trellis_moe_last_error()
+    # forward on a NULL handle
+    assert lib.trellis_moe_forward(None, P(8), P(8), P(8), 1, 0, P(8), P(256), 1 << 20, None) == -1
+    assert lib.trellis_moe_set_stage_events(None, None, 0) == -1
+    lib.trellis_moe_destroy(None)

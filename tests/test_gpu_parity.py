@@ -1,0 +1,330 @@
+"""CUDA path vs. oracle, through the C ABI (needs a GB300)."""
+import numpy as np
+import pytest
+
+from oracle import hadamard, layer as olayer, mxfp8, route as oroute, trellis
+from tests.gpu_util import TOL, oracle_routes, rel_row_err, run_and_compare, small_cfg, upload_tokens
+from trellis_quantized_moe_route_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from trellis_quantized_moe_route_gb300 import binding, build
+    build.build()
+    binding.load_library()
+
+
+def _moe(L, max_tokens, **kw):
+    from trellis_quantized_moe_route_gb300.binding import TrellisMoE
+    return TrellisMoE(L, max_tokens=max_tokens, **kw)
+
+
+# ---------------------------------------------------------------- decode ---
+@pytest.mark.parametrize("K", [2, 3, 4, 5, 6])
+@pytest.mark.parametrize("mode", ["w4a16", "w4a8"])
+def test_decode_tiles_bit_exact(K, mode):
+    cfg = small_cfg(E=3, H=128, I=64, topk=2, rot_block_i=64, bits=(K,), seed=40 + K)
+    L = synth.make_layer(cfg)
+    moe = _moe(L, 4)
+    for proj, rows, cols in ((1, 2 * cfg.I, cfg.H), (2, cfg.H, cfg.I)):
+        ntiles = (rows // 16) * (cols // 16)
+        got = moe.decode_tiles(proj, 1, 0, ntiles, mode).cpu().numpy()
+        payload = L.fc1_payload if proj == 1 else L.fc2_payload
+        tiles = trellis.expert_payload(payload, rows, cols, L.bits, 1).reshape(ntiles, 16 * K)
+        ref = trellis.decode_tiles_fp16(tiles, K)
+        if mode == "w4a16":
+            assert np.array_equal(got.view(np.uint16), ref.view(np.uint16))
+        else:
+            assert np.array_equal(got, mxfp8.e4m3_encode(ref.astype(np.float64)))
+
+
+def test_decode_tiles_mixed_bits_offsets():
+    cfg = synth.CONFIGS["odd"]
+    small = small_cfg(E=6, H=256, I=64, rot_block_i=64, bits=(2, 3, 4), seed=3)
+    L = synth.make_layer(small)
+    moe = _moe(L, 4)
+    for e in range(small.E):
+        K = int(L.bits[e])
+        ntiles = (small.H // 16) * (small.I // 16)
+        got = moe.decode_tiles(2, e, 3, 5, "w4a16").cpu().numpy()
+        tiles = trellis.expert_payload(L.fc2_payload, small.H, small.I, L.bits, e).reshape(ntiles, 16 * K)
+        assert np.array_equal(got.view(np.uint16), trellis.decode_tiles_fp16(tiles[3:8], K).view(np.uint16))
+    assert cfg.bits == (2, 3, 4)
+
+
+# ---------------------------------------------------------------- routing ---
+@pytest.mark.parametrize("name,T", [("decode", 64), ("prefill", 300), ("tiny", 4), ("large", 37)])
+def test_router_matches_oracle(name, T):
+    from trellis_quantized_moe_route_gb300 import binding
+    cfg = synth.CONFIGS[name]
+    _, logits = synth.make_tokens(cfg, T=T)
+    ids_ref, w_ref = oroute.route_topk_softmax(logits, cfg.topk)
+    ids, w = binding.route(torch.from_numpy(logits).cuda(), cfg.topk)
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    assert np.allclose(w.cpu().numpy(), w_ref, rtol=2e-6, atol=1e-7)
+
+
+def test_router_ties_go_to_lower_id():
+    from trellis_quantized_moe_route_gb300 import binding
+    lg = np.round(synth.Stream(9, 9).normal(50 * 40).reshape(50, 40)).astype(np.float32)
+    ids_ref, _ = oroute.route_topk_softmax(lg, 6)
+    ids, _ = binding.route(torch.from_numpy(lg).cuda(), 6)
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+
+
+@pytest.mark.parametrize("T,E,k,block", [(4, 8, 2, 8), (8, 128, 8, 8), (2048, 128, 8, 64), (512, 64, 10, 64),
+                                         (1, 160, 8, 8), (129, 16, 8, 64), (3000, 256, 3, 16)])
+def test_route_map_bit_exact(T, E, k, block):
+    cfg = small_cfg(E=E, topk=k, H=128, I=64, rot_block_i=64)
+    L = synth.make_layer(cfg, bits=[4] * E)
+    moe = _moe(L, T)
+    ids = synth.random_ids(100 + T, T, E, k)
+    got = moe.route_map(torch.from_numpy(ids).cuda(), block)
+    ref = oroute.route_map(ids, E, block)
+    n = int(ref["offsets"][-1])
+    assert np.array_equal(got["counts"].cpu().numpy(), ref["counts"])
+    assert np.array_equal(got["offsets"].cpu().numpy(), ref["offsets"])
+    assert np.array_equal(got["route_of_slot"].cpu().numpy()[:n], ref["route_of_slot"])
+    assert np.array_equal(got["slot_of_route"].cpu().numpy(), ref["slot_of_route"])
+
+
+def test_route_map_skewed_single_expert():
+    T, E, k = 3000, 32, 1
+    cfg = small_cfg(E=E, topk=k, H=128, I=64, rot_block_i=64)
+    moe = _moe(synth.make_layer(cfg, bits=[4] * E), T)
+    ids = np.full((T, k), 5, dtype=np.int32)
+    got = moe.route_map(torch.from_numpy(ids).cuda(), 64)
+    ref = oroute.route_map(ids, E, 64)
+    n = int(ref["offsets"][-1])
+    assert np.array_equal(got["route_of_slot"].cpu().numpy()[:n], ref["route_of_slot"])
+    assert np.array_equal(got["offsets"].cpu().numpy(), ref["offsets"])
+
+
+def test_out_of_range_ids_are_dropped_and_flagged():
+    cfg = small_cfg(E=8, topk=2, H=128, I=64, rot_block_i=64, T=4)
+    L = synth.make_layer(cfg)
+    moe = _moe(L, 4)
+    x_bits, logits = synth.make_tokens(cfg)
+    ids, w = oracle_routes(logits, 2)
+    bad = ids.copy()
+    bad[1, 1] = 8
+    bad[3, 0] = -1
+    x, _ = upload_tokens(x_bits, logits)
+    out = moe.forward(x, torch.from_numpy(bad).cuda(), torch.from_numpy(w.astype(np.float32)).cuda(), mode="w4a16")
+    assert moe.poll_error() == 1
+    assert moe.poll_error() == 0
+    w2 = w.copy()
+    w2[1, 1] = 0.0
+    w2[3, 0] = 0.0
+    ref = olayer.layer_forward(L, x_bits, np.where(bad < 0, 0, np.minimum(bad, 7)), w2, mode="w4a16")
+    assert rel_row_err(out.cpu().numpy(), ref) < TOL["w4a16"]
+
+
+# ---------------------------------------------------------- rotate+quant ---
+@pytest.mark.parametrize("rot", [1, 64, 128])
+def test_rotate_quant_fp16(rot):
+    cfg = small_cfg(H=512, rot_block_h=rot, T=33)
+    L = synth.make_layer(cfg)
+    moe = _moe(L, cfg.T)
+    x_bits, logits = synth.make_tokens(cfg)
+    x, _ = upload_tokens(x_bits, logits)
+    xq, _ = moe.rotate_quant(x, "w4a16")
+    got = xq.cpu().numpy().view(np.float16).astype(np.float64)
+    ref = olayer.rotate_input(L, x_bits)
+    if rot == 1:
+        assert np.array_equal(got, ref.astype(np.float16).astype(np.float64))
+    else:
+        ulp = np.maximum(np.abs(np.spacing(ref.astype(np.float16))), np.abs(np.spacing(got.astype(np.float16))))
+        assert np.all(np.abs(got - ref) <= ulp.astype(np.float64))
+
+
+@pytest.mark.parametrize("rot", [1, 128])
+def test_rotate_quant_mxfp8(rot):
+    cfg = small_cfg(H=1024, rot_block_h=rot, T=17)
+    L = synth.make_layer(cfg)
+    moe = _moe(L, cfg.T)
+    x_bits, logits = synth.make_tokens(cfg)
+    x, _ = upload_tokens(x_bits, logits)
+    xq, xs = moe.rotate_quant(x, "w4a8")
+    codes, e8 = xq.cpu().numpy(), xs.cpu().numpy()
+    ref = olayer.rotate_input(L, x_bits)
+    rc, re8, rdeq = mxfp8.quantize_mxfp8(ref.astype(np.float32))
+    if rot == 1:
+        assert np.array_equal(codes, rc) and np.array_equal(e8, re8)
+    else:
+        assert (codes == rc).mean() > 0.995 and (e8 == re8).mean() > 0.99
+        deq = mxfp8.e4m3_decode(codes) * np.exp2(np.repeat(e8.astype(np.float64) - 127, 32, axis=1))
+        scale = np.exp2(np.repeat(re8.astype(np.float64) - 127, 32, axis=1))
+        # half an E4M3 ulp at the top of the range is 16 (in units of the block scale)
+        assert np.all(np.abs(deq - ref) <= scale * 32.0)
+
+
+# ---------------------------------------------------------------- layer ----
+@pytest.mark.parametrize("mode", ["w4a16", "w4a8"])
+def test_tiny_config(mode):
+    cfg = synth.CONFIGS["tiny"]
+    L = synth.make_layer(cfg)
+    moe = _moe(L, cfg.T)
+    err, _, _ = run_and_compare(moe, L, cfg, cfg.T, mode)
+    assert err < TOL[mode], err
+
+
+@pytest.mark.parametrize("mode", ["w4a16", "w4a8"])
+@pytest.mark.parametrize("kw", [
+    dict(),                                                     # rot 128/128, K=4
+    dict(bits=(2, 3, 4), I=320, rot_block_i=64, H=512),         # odd geometry, mixed K, 64-wide I blocks
+    dict(rot_block_h=1, rot_block_i=1),                         # identity rotations
+    dict(bits=(5, 6), E=8, topk=3),                             # wider codes
+    dict(T=200, E=8, topk=2),                                   # several 64-route blocks per expert
+])
+def test_small_layers(mode, kw):
+    cfg = small_cfg(**kw)
+    L = synth.make_layer(cfg)
+    moe = _moe(L, cfg.T)
+    err, _, _ = run_and_compare(moe, L, cfg, cfg.T, mode)
+    assert err < TOL[mode], err
+
+
+def test_deterministic_repeat_and_poisoned_workspace():
+    cfg = small_cfg(T=100, E=8, topk=2)
+    L = synth.make_layer(cfg)
+    moe = _moe(L, cfg.T)
+    x_bits, logits = synth.make_tokens(cfg)
+    x, lg = upload_tokens(x_bits, logits)
+    a = moe.forward_logits(x, lg, mode="w4a16").clone()
+    b = moe.forward_logits(x, lg, mode="w4a16").clone()
+    moe.workspace.fill_(0xFF)
+    c = moe.forward_logits(x, lg, mode="w4a16").clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b) and torch.equal(a, c)
+
+
+@pytest.mark.parametrize("mode", ["w4a16", "w4a8"])
+def test_token_permutation_equivariance_bitwise(mode):
+    cfg = small_cfg(T=50, E=8, topk=3)
+    L = synth.make_layer(cfg)
+    moe = _moe(L, cfg.T)
+    x_bits, logits = synth.make_tokens(cfg)
+    perm = synth.permutation(synth.Stream(2, 2), cfg.T)
+    x, lg = upload_tokens(x_bits, logits)
+    xp, lgp = upload_tokens(x_bits[perm], logits[perm])
+    a = moe.forward_logits(x, lg, mode=mode).cpu().numpy()
+    b = moe.forward_logits(xp, lgp, mode=mode).cpu().numpy()
+    assert np.array_equal(b, a[perm])
+
+
+def test_atomic_combine_within_tolerance():
+    cfg = small_cfg(T=64, E=8, topk=2)
+    L = synth.make_layer(cfg)
+    moe = _moe(L, cfg.T, deterministic=False)
+    err, _, _ = run_and_compare(moe, L, cfg, cfg.T, "w4a16")
+    assert err < TOL["w4a16"], err
+
+
+def test_forward_host_matches_device_call():
+    cfg = small_cfg(T=20)
+    L = synth.make_layer(cfg)
+    moe = _moe(L, cfg.T)
+    x_bits, logits = synth.make_tokens(cfg)
+    x, lg = upload_tokens(x_bits, logits)
+    dev = moe.forward_logits(x, lg, mode="auto").cpu()
+    xh = torch.from_numpy(x_bits.view(np.int16).copy()).pin_memory()
+    lh = torch.from_numpy(logits.copy()).pin_memory()
+    oh = torch.empty((cfg.T, cfg.H), dtype=torch.float32).pin_memory()
+    moe.forward_host(xh, lh, oh, mode="auto")
+    assert torch.equal(dev, oh)
+
+
+def test_auto_mode_switches_at_decode_rows():
+    cfg = small_cfg(T=16)
+    L = synth.make_layer(cfg)
+    moe = _moe(L, cfg.T, decode_max_rows=8)
+    x_bits, logits = synth.make_tokens(cfg)
+    for T, mode in ((8, "w4a8"), (9, "w4a16")):
+        x, lg = upload_tokens(x_bits[:T], logits[:T])
+        auto = moe.forward_logits(x, lg, mode="auto").cpu()
+        explicit = moe.forward_logits(x, lg, mode=mode).cpu()
+        assert torch.equal(auto, explicit)
+
+
+def test_host_validation_errors():
+    from trellis_quantized_moe_route_gb300.binding import TrellisMoEError
+    cfg = small_cfg(T=4)
+    L = synth.make_layer(cfg)
+    moe = _moe(L, 4)
+    x_bits, logits = synth.make_tokens(cfg, T=5)
+    x, lg = upload_tokens(x_bits, logits)
+    with pytest.raises(TrellisMoEError) as ei:
+        moe.forward_logits(x, lg)  # T=5 > max_tokens=4
+    assert ei.value.status == -1
+    with pytest.raises(TrellisMoEError) as ei:
+        moe.forward_logits(x[:4], lg[:4], mode=7)
+    assert ei.value.status == -1
+    ws, nb = moe.workspace, moe.workspace_bytes
+    moe.workspace_bytes = 1024
+    with pytest.raises(TrellisMoEError) as ei:
+        moe.forward_logits(x[:4], lg[:4])
+    assert ei.value.status == -3
+    moe.workspace_bytes = nb
+    moe.workspace = ws[16:]
+    moe.workspace_bytes = nb - 16
+    with pytest.raises(TrellisMoEError) as ei:
+        moe.forward_logits(x[:4], lg[:4])
+    assert ei.value.status == -3
+    moe.workspace, moe.workspace_bytes = ws, nb
+    out = moe.forward_logits(x[:0], lg[:0])
+    assert out.shape == (0, cfg.H)
+
+
+# ----------------------------------------------- the five workloads, full size ---
+def _sample(T, n, seed):
+    if T <= n:
+        return np.arange(T)
+    s = synth.Stream(seed, 77)
+    return np.unique(np.concatenate([[0, T - 1], s.below(n - 2, T)]))
+
+
+@pytest.mark.parametrize("T", [1, 2, 4, 8])
+def test_decode_config_full(T):
+    cfg = synth.CONFIGS["decode"]
+    L = synth.make_layer(cfg)
+    moe = _moe(L, 8)
+    err, _, _ = run_and_compare(moe, L, cfg, T, "w4a8")
+    assert err < TOL["w4a8"], err
+
+
+def test_prefill_config_full_sampled():
+    cfg = synth.CONFIGS["prefill"]
+    L = synth.make_layer(cfg)
+    moe = _moe(L, cfg.T)
+    err, _, _ = run_and_compare(moe, L, cfg, cfg.T, "w4a16", tokens=_sample(cfg.T, 8, 1))
+    assert err < TOL["w4a16"], err
+
+
+def test_odd_config_full_sampled():
+    cfg = synth.CONFIGS["odd"]
+    L = synth.make_layer(cfg)
+    moe = _moe(L, cfg.T)
+    err, _, _ = run_and_compare(moe, L, cfg, cfg.T, "w4a16", tokens=_sample(cfg.T, 8, 2))
+    assert err < TOL["w4a16"], err
+
+
+def test_large_config_decode_full():
+    cfg = synth.CONFIGS["large"]
+    L = synth.make_layer(cfg)
+    moe = _moe(L, 1)
+    err, _, _ = run_and_compare(moe, L, cfg, 1, "w4a8")
+    assert err < TOL["w4a8"], err
+
+
+def test_large_config_prefill_sampled():
+    cfg = synth.CONFIGS["large"]
+    L = synth.make_layer(cfg)
+    moe = _moe(L, cfg.T)
+    err, _, _ = run_and_compare(moe, L, cfg, cfg.T, "w4a16", tokens=_sample(cfg.T, 3, 3))
+    assert err < TOL["w4a16"], err

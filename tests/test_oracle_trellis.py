@@ -132,6 +132,8 @@ def test_vectorised_states_match_bitwise_loop(K):
     st = trellis.tile_states(words, K)
     for t in range(3):
         assert st[t].tolist() == trellis.tile_states_scalar(words[t], K)
+    many = synth.Stream(14, K).words16(16 * K * 500).reshape(500, 16 * K)
+    assert np.array_equal(trellis.tile_states_words(many, K), trellis.tile_states(many, K))
 
 
 @pytest.mark.parametrize("K", [2, 3, 4, 5, 6])

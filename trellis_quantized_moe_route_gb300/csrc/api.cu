@@ -1,0 +1,513 @@
+// C ABI of the trellis-MoE layer: host-side validation, workspace layout and
+// the launch sequence of one forward pass. Declared in include/trellis_moe.h.
+//
+// Lifecycle after the pages' own (sparkinfer PR #90 "moe: integrate EXL3
+// Trellis into the fused W4A16 API", Summary: plan -> prepare -> scratch/bind
+// -> run; flashinfer PR #69 "b12x fused MoE: TrellisMX ...", Description: the
+// plan declares the scratch bytes, bind carves them, no call allocates, and a
+// missing, short or misaligned arena is rejected).
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "../../include/trellis_moe.h"
+#include "launch.h"
+
+struct tm_layer {
+  tm_layer_desc desc;
+  std::vector<uint8_t> bits;
+  int uniform_k;       // trellis K of every expert, or 0 when mixed
+  int bi;              // FC1 half-row block (64 or 128)
+  int64_t* d_off1;     // [E] word offsets of each expert's FC1 block
+  int64_t* d_off2;     // [E]
+  uint8_t* d_bits;     // [E]
+  int device;
+  cudaEvent_t stage_ev[7];  // optional stage-boundary events (NULL = off)
+};
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+tm_status fail(tm_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+tm_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(TM_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Records stage-boundary event i if the caller asked for it.
+cudaError_t stage_mark(const tm_layer* layer, int i, cudaStream_t st) {
+  if (!layer->stage_ev[i]) return cudaSuccess;
+  return cudaEventRecordWithFlags(layer->stage_ev[i], st, cudaEventRecordExternal);
+}
+
+constexpr size_t kAlign = 256;
+constexpr int kBnMax = 64;
+constexpr int kBnMin = 8;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+// Regions of a workspace sized for T tokens (T*topk routes).
+struct Layout {
+  enum {
+    ERR, XQ, XS, ZQ, ZS, ROWS, SLOT_OF_ROUTE,
+    IDS, W, RANK, TILE_COUNTS, COUNTS, OFFSETS, BLOCK_EXPERT, NBLOCKS, ROUTE_OF_SLOT,
+    HOST_X, HOST_LOGITS, HOST_OUT, COUNT
+  };
+  size_t off[COUNT];
+  size_t bytes[COUNT];
+  size_t total;
+};
+
+Layout make_layout(const tm_layer_desc& d, int T) {
+  Layout L;
+  const size_t R = (size_t)T * d.topk;
+  const size_t slots = R + (size_t)d.E * (kBnMax - 1);
+  const size_t ntiles = (R + 1023) / 1024;
+  L.bytes[Layout::XQ] = (size_t)T * d.H * 2;
+  L.bytes[Layout::XS] = (size_t)T * (d.H / 32);
+  L.bytes[Layout::ZQ] = slots * d.I * 2;
+  L.bytes[Layout::ZS] = slots * (d.I / 32);
+  L.bytes[Layout::ROWS] = slots * d.H * 4;
+  L.bytes[Layout::SLOT_OF_ROUTE] = R * 4;
+  L.bytes[Layout::ERR] = 4;
+  L.bytes[Layout::IDS] = R * 4;
+  L.bytes[Layout::W] = R * 4;
+  L.bytes[Layout::RANK] = R * 4;
+  L.bytes[Layout::TILE_COUNTS] = ntiles * d.E * 4;
+  L.bytes[Layout::COUNTS] = (size_t)d.E * 4;
+  L.bytes[Layout::OFFSETS] = ((size_t)d.E + 1) * 4;
+  L.bytes[Layout::BLOCK_EXPERT] = (slots / kBnMin + 1) * 4;
+  L.bytes[Layout::NBLOCKS] = 4;
+  L.bytes[Layout::ROUTE_OF_SLOT] = slots * 4;
+  L.bytes[Layout::HOST_X] = (size_t)T * d.H * 2;
+  L.bytes[Layout::HOST_LOGITS] = (size_t)T * d.E * 4;
+  L.bytes[Layout::HOST_OUT] = (size_t)T * d.H * 4;
+  size_t o = 0;
+  for (int i = 0; i < Layout::COUNT; ++i) {
+    L.off[i] = o;
+    o += align_up(std::max<size_t>(L.bytes[i], 1));
+  }
+  L.total = o;
+  return L;
+}
+
+template <typename P>
+P* at(void* ws, const Layout& L, int region) {
+  return reinterpret_cast<P*>(reinterpret_cast<char*>(ws) + L.off[region]);
+}
+
+bool pow2_block_ok(int b) { return b == 1 || b == 64 || b == 128; }
+
+tm_status check_ws(const tm_layer* layer, int T, void* ws, size_t bytes, Layout* out) {
+  if (T > layer->desc.max_tokens) return fail(TM_EINVAL, "T=%d exceeds prepared max_tokens=%d", T, layer->desc.max_tokens);
+  const Layout L = make_layout(layer->desc, T);
+  if (ws == nullptr) return fail(TM_EWORKSPACE, "workspace is NULL");
+  if (((uintptr_t)ws) % kAlign != 0) return fail(TM_EWORKSPACE, "workspace must be %zu-byte aligned", kAlign);
+  if (bytes < L.total) return fail(TM_EWORKSPACE, "workspace has %zu bytes, %zu needed for T=%d", bytes, L.total, T);
+  *out = L;
+  return TM_OK;
+}
+
+int choose_bn(const tm_layer_desc& d, int T) {
+  const long R = (long)T * d.topk;
+  return (R < 4L * d.E) ? kBnMin : kBnMax;
+}
+
+tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, const float* w, int T, int mode,
+                    float* out, void* ws, const Layout& L, cudaStream_t st) {
+  const tm_layer_desc& d = layer->desc;
+  const bool w4a8 = (mode == TM_MODE_W4A8) || (mode == TM_MODE_AUTO && T <= d.decode_max_rows);
+  const int R = T * d.topk;
+  const int bn = choose_bn(d, T);
+  cudaError_t e;
+  uint32_t* err = at<uint32_t>(ws, L, Layout::ERR);
+  if ((e = cudaMemsetAsync(err, 0, 4, st)) != cudaSuccess) return cuda_fail(e, "clear error word");
+
+  tmoe::RouteMapArgs rm;
+  rm.ids = ids;
+  rm.R = R;
+  rm.E = d.E;
+  rm.block = bn;
+  rm.rank = at<int32_t>(ws, L, Layout::RANK);
+  rm.tile_counts = at<int32_t>(ws, L, Layout::TILE_COUNTS);
+  rm.counts = at<int32_t>(ws, L, Layout::COUNTS);
+  rm.offsets = at<int32_t>(ws, L, Layout::OFFSETS);
+  rm.block_expert = at<int32_t>(ws, L, Layout::BLOCK_EXPERT);
+  rm.nblocks = at<int32_t>(ws, L, Layout::NBLOCKS);
+  rm.route_of_slot = at<int32_t>(ws, L, Layout::ROUTE_OF_SLOT);
+  rm.slot_of_route = at<int32_t>(ws, L, Layout::SLOT_OF_ROUTE);
+  rm.err = err;
+  if ((e = tmoe::launch_route_map(rm, st)) != cudaSuccess) return cuda_fail(e, "route map");
+  if ((e = stage_mark(layer, 2, st)) != cudaSuccess) return cuda_fail(e, "stage event");
+
+  void* xq = at<void>(ws, L, Layout::XQ);
+  uint8_t* xs = at<uint8_t>(ws, L, Layout::XS);
+  if ((e = tmoe::launch_rotate_quant(x, d.in_suh, T, d.H, d.rot_block_h, w4a8, xq, xs, st)) != cudaSuccess)
+    return cuda_fail(e, "rotate+quantize");
+  if ((e = stage_mark(layer, 3, st)) != cudaSuccess) return cuda_fail(e, "stage event");
+
+  const int max_blocks = R / bn + std::min(d.E, R) + 1;
+  tmoe::FcArgs a1{};
+  a1.E = d.E; a1.H = d.H; a1.I = d.I; a1.topk = d.topk;
+  a1.rot_b = d.rot_block_i;
+  a1.payload = d.fc1_payload;
+  a1.word_off = layer->d_off1;
+  a1.bits = layer->d_bits;
+  a1.scale = d.fc1_scale;
+  a1.rot_tab = d.rot_tab;
+  a1.act = xq;
+  a1.act_scale = xs;
+  a1.route_of_slot = rm.route_of_slot;
+  a1.block_expert = rm.block_expert;
+  a1.nblocks = rm.nblocks;
+  a1.out_act = at<void>(ws, L, Layout::ZQ);
+  a1.out_scale = at<uint8_t>(ws, L, Layout::ZS);
+  if ((e = tmoe::launch_fc1(a1, w4a8, layer->bi, bn, layer->uniform_k, max_blocks, st)) != cudaSuccess)
+    return cuda_fail(e, "FC1");
+  if ((e = stage_mark(layer, 4, st)) != cudaSuccess) return cuda_fail(e, "stage event");
+
+  tmoe::FcArgs a2 = a1;
+  a2.rot_b = d.rot_block_h;
+  a2.payload = d.fc2_payload;
+  a2.word_off = layer->d_off2;
+  a2.scale = d.fc2_scale;
+  a2.rot_tab = d.out_svh;
+  a2.act = a1.out_act;
+  a2.act_scale = a1.out_scale;
+  a2.out_act = nullptr;
+  a2.out_scale = nullptr;
+  a2.route_w = w;
+  a2.atomic = d.deterministic ? 0 : 1;
+  if (a2.atomic) {
+    if ((e = cudaMemsetAsync(out, 0, (size_t)T * d.H * 4, st)) != cudaSuccess) return cuda_fail(e, "clear output");
+    a2.out_f32 = out;
+  } else {
+    a2.out_f32 = at<float>(ws, L, Layout::ROWS);
+  }
+  if ((e = tmoe::launch_fc2(a2, w4a8, bn, layer->uniform_k, max_blocks, st)) != cudaSuccess) return cuda_fail(e, "FC2");
+  if ((e = stage_mark(layer, 5, st)) != cudaSuccess) return cuda_fail(e, "stage event");
+  if (!a2.atomic) {
+    if ((e = tmoe::launch_combine(a2.out_f32, rm.slot_of_route, w, T, d.H, d.topk, out, st)) != cudaSuccess)
+      return cuda_fail(e, "combine");
+  }
+  if ((e = stage_mark(layer, 6, st)) != cudaSuccess) return cuda_fail(e, "stage event");
+  return TM_OK;
+}
+
+}  // namespace
+
+namespace tmoe {
+cudaError_t launch_fc1_f16(const FcArgs& a, int bi, int bn, int uniform_k, int max_blocks, cudaStream_t st);
+cudaError_t launch_fc1_e4m3(const FcArgs& a, int bi, int bn, int uniform_k, int max_blocks, cudaStream_t st);
+cudaError_t launch_fc2_f16(const FcArgs& a, int bn, int uniform_k, int max_blocks, cudaStream_t st);
+cudaError_t launch_fc2_e4m3(const FcArgs& a, int bn, int uniform_k, int max_blocks, cudaStream_t st);
+
+cudaError_t launch_fc1(const FcArgs& a, bool w4a8, int bi, int bn, int uniform_k, int max_blocks, cudaStream_t st) {
+  return w4a8 ? launch_fc1_e4m3(a, bi, bn, uniform_k, max_blocks, st) : launch_fc1_f16(a, bi, bn, uniform_k, max_blocks, st);
+}
+cudaError_t launch_fc2(const FcArgs& a, bool w4a8, int bn, int uniform_k, int max_blocks, cudaStream_t st) {
+  return w4a8 ? launch_fc2_e4m3(a, bn, uniform_k, max_blocks, st) : launch_fc2_f16(a, bn, uniform_k, max_blocks, st);
+}
+}  // namespace tmoe
+
+extern "C" {
+
+const char* trellis_moe_last_error(void) { return g_err; }
+
+tm_status trellis_moe_prepare(const tm_layer_desc* desc, tm_layer** out, size_t* workspace_bytes) {
+  g_err[0] = 0;
+  if (out) *out = nullptr;
+  if (!desc || !out) return fail(TM_EINVAL, "desc and out must be non-NULL");
+  const tm_layer_desc& d = *desc;
+  if (d.E < 1 || d.E > tmoe::kMaxExperts) return fail(TM_EUNSUPPORTED, "E=%d outside 1..%d", d.E, tmoe::kMaxExperts);
+  if (d.H < 128 || d.H % 128 != 0) return fail(TM_EUNSUPPORTED, "H=%d must be a positive multiple of 128", d.H);
+  if (d.I < 64 || d.I % 64 != 0) return fail(TM_EUNSUPPORTED, "I=%d must be a positive multiple of 64", d.I);
+  if (d.topk < 1 || d.topk > 32 || d.topk > d.E) return fail(TM_EINVAL, "topk=%d outside 1..min(E,32)", d.topk);
+  if (!pow2_block_ok(d.rot_block_h) || d.H % d.rot_block_h != 0)
+    return fail(TM_EUNSUPPORTED, "rot_block_h=%d must be 1, 64 or 128 and divide H", d.rot_block_h);
+  if (!pow2_block_ok(d.rot_block_i) || d.I % d.rot_block_i != 0)
+    return fail(TM_EUNSUPPORTED, "rot_block_i=%d must be 1, 64 or 128 and divide I", d.rot_block_i);
+  if (d.max_tokens < 1) return fail(TM_EINVAL, "max_tokens=%d must be >= 1", d.max_tokens);
+  if ((long)d.max_tokens * d.topk > (1L << 24)) return fail(TM_EUNSUPPORTED, "max_tokens*topk too large");
+  if (!d.bits_per_expert) return fail(TM_EINVAL, "bits_per_expert is NULL");
+  const void* ptrs[] = {d.fc1_payload, d.fc2_payload, d.fc1_scale, d.fc2_scale, d.in_suh, d.rot_tab, d.out_svh};
+  const char* names[] = {"fc1_payload", "fc2_payload", "fc1_scale", "fc2_scale", "in_suh", "rot_tab", "out_svh"};
+  for (int i = 0; i < 7; ++i) {
+    if (!ptrs[i]) return fail(TM_EINVAL, "%s is NULL", names[i]);
+    if (((uintptr_t)ptrs[i]) % 16 != 0) return fail(TM_EINVAL, "%s must be 16-byte aligned", names[i]);
+  }
+  tm_layer* L = new tm_layer();
+  L->desc = d;
+  for (int i = 0; i < 7; ++i) L->stage_ev[i] = nullptr;
+  L->bits.assign(d.bits_per_expert, d.bits_per_expert + d.E);
+  L->uniform_k = L->bits[0];
+  std::vector<int64_t> off1(d.E), off2(d.E);
+  int64_t o1 = 0, o2 = 0;
+  for (int e = 0; e < d.E; ++e) {
+    const int k = L->bits[e];
+    if (k < 2 || k > 6) {
+      delete L;
+      return fail(TM_EUNSUPPORTED, "expert %d has K=%d bits; supported 2..6", e, k);
+    }
+    if (k != L->uniform_k) L->uniform_k = 0;
+    off1[e] = o1;
+    off2[e] = o2;
+    o1 += (int64_t)(2 * d.I / 16) * (d.H / 16) * 16 * k;
+    o2 += (int64_t)(d.H / 16) * (d.I / 16) * 16 * k;
+  }
+  L->bi = (d.rot_block_i == 128 || (d.I % 128 == 0 && d.rot_block_i != 64)) ? 128 : 64;
+  if (d.I % L->bi != 0) L->bi = 64;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&L->device)) != cudaSuccess) { delete L; return cuda_fail(e, "cudaGetDevice"); }
+  L->d_off1 = L->d_off2 = nullptr;
+  L->d_bits = nullptr;
+  if ((e = cudaMalloc(&L->d_off1, d.E * 8)) != cudaSuccess ||
+      (e = cudaMalloc(&L->d_off2, d.E * 8)) != cudaSuccess ||
+      (e = cudaMalloc(&L->d_bits, d.E)) != cudaSuccess ||
+      (e = cudaMemcpy(L->d_off1, off1.data(), d.E * 8, cudaMemcpyHostToDevice)) != cudaSuccess ||
+      (e = cudaMemcpy(L->d_off2, off2.data(), d.E * 8, cudaMemcpyHostToDevice)) != cudaSuccess ||
+      (e = cudaMemcpy(L->d_bits, L->bits.data(), d.E, cudaMemcpyHostToDevice)) != cudaSuccess) {
+    cudaFree(L->d_off1);
+    cudaFree(L->d_off2);
+    cudaFree(L->d_bits);
+    delete L;
+    return cuda_fail(e, "upload descriptor tables");
+  }
+  *out = L;
+  if (workspace_bytes) *workspace_bytes = make_layout(d, d.max_tokens).total;
+  return TM_OK;
+}
+
+size_t trellis_moe_workspace_size(const tm_layer* layer, int32_t max_tokens) {
+  if (!layer || max_tokens < 0) return 0;
+  return make_layout(layer->desc, max_tokens).total;
+}
+
+void trellis_moe_destroy(tm_layer* layer) {
+  if (!layer) return;
+  cudaFree(layer->d_off1);
+  cudaFree(layer->d_off2);
+  cudaFree(layer->d_bits);
+  delete layer;
+}
+
+static tm_status check_mode(int32_t mode) {
+  if (mode != TM_MODE_AUTO && mode != TM_MODE_W4A16 && mode != TM_MODE_W4A8)
+    return fail(TM_EINVAL, "mode=%d is not a tm_mode", mode);
+  return TM_OK;
+}
+
+tm_status trellis_moe_forward(tm_layer* layer, const uint16_t* x, const int32_t* topk_ids, const float* topk_w,
+                              int32_t T, int32_t mode, float* out, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  g_err[0] = 0;
+  if (!layer) return fail(TM_EINVAL, "layer is NULL");
+  if (T < 0) return fail(TM_EINVAL, "T=%d < 0", T);
+  if (check_mode(mode) != TM_OK) return TM_EINVAL;
+  if (T == 0) return TM_OK;
+  if (!x || !topk_ids || !topk_w || !out) return fail(TM_EINVAL, "x, topk_ids, topk_w and out must be non-NULL");
+  Layout L;
+  tm_status s = check_ws(layer, T, workspace, workspace_bytes, &L);
+  if (s != TM_OK) return s;
+  cudaError_t e;
+  if ((e = stage_mark(layer, 0, (cudaStream_t)stream)) != cudaSuccess) return cuda_fail(e, "stage event");
+  return run_layer(layer, x, topk_ids, topk_w, T, mode, out, workspace, L, (cudaStream_t)stream);
+}
+
+tm_status trellis_moe_forward_logits(tm_layer* layer, const uint16_t* x, const float* logits, int32_t T,
+                                     int32_t mode, float* out, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  g_err[0] = 0;
+  if (!layer) return fail(TM_EINVAL, "layer is NULL");
+  if (T < 0) return fail(TM_EINVAL, "T=%d < 0", T);
+  if (check_mode(mode) != TM_OK) return TM_EINVAL;
+  if (T == 0) return TM_OK;
+  if (!x || !logits || !out) return fail(TM_EINVAL, "x, logits and out must be non-NULL");
+  Layout L;
+  tm_status s = check_ws(layer, T, workspace, workspace_bytes, &L);
+  if (s != TM_OK) return s;
+  cudaStream_t st = (cudaStream_t)stream;
+  int32_t* ids = at<int32_t>(workspace, L, Layout::IDS);
+  float* w = at<float>(workspace, L, Layout::W);
+  cudaError_t e;
+  if ((e = stage_mark(layer, 0, st)) != cudaSuccess) return cuda_fail(e, "stage event");
+  e = tmoe::launch_route_topk(logits, T, layer->desc.E, layer->desc.topk, ids, w, st);
+  if (e != cudaSuccess) return cuda_fail(e, "router");
+  if ((e = stage_mark(layer, 1, st)) != cudaSuccess) return cuda_fail(e, "stage event");
+  return run_layer(layer, x, ids, w, T, mode, out, workspace, L, st);
+}
+
+tm_status trellis_moe_forward_host(tm_layer* layer, const uint16_t* x_host, const float* logits_host, int32_t T,
+                                   int32_t mode, float* out_host, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+  g_err[0] = 0;
+  if (!layer) return fail(TM_EINVAL, "layer is NULL");
+  if (T < 0) return fail(TM_EINVAL, "T=%d < 0", T);
+  if (check_mode(mode) != TM_OK) return TM_EINVAL;
+  if (T == 0) return TM_OK;
+  if (!x_host || !logits_host || !out_host) return fail(TM_EINVAL, "x_host, logits_host and out_host must be non-NULL");
+  Layout L;
+  tm_status s = check_ws(layer, T, workspace, workspace_bytes, &L);
+  if (s != TM_OK) return s;
+  cudaStream_t st = (cudaStream_t)stream;
+  const tm_layer_desc& d = layer->desc;
+  uint16_t* dx = at<uint16_t>(workspace, L, Layout::HOST_X);
+  float* dl = at<float>(workspace, L, Layout::HOST_LOGITS);
+  float* dout = at<float>(workspace, L, Layout::HOST_OUT);
+  cudaError_t e;
+  if ((e = cudaMemcpyAsync(dx, x_host, (size_t)T * d.H * 2, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+    return cuda_fail(e, "copy x to device");
+  if ((e = cudaMemcpyAsync(dl, logits_host, (size_t)T * d.E * 4, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+    return cuda_fail(e, "copy logits to device");
+  int32_t* ids = at<int32_t>(workspace, L, Layout::IDS);
+  float* w = at<float>(workspace, L, Layout::W);
+  if ((e = stage_mark(layer, 0, st)) != cudaSuccess) return cuda_fail(e, "stage event");
+  if ((e = tmoe::launch_route_topk(dl, T, d.E, d.topk, ids, w, st)) != cudaSuccess) return cuda_fail(e, "router");
+  if ((e = stage_mark(layer, 1, st)) != cudaSuccess) return cuda_fail(e, "stage event");
+  s = run_layer(layer, dx, ids, w, T, mode, dout, workspace, L, st);
+  if (s != TM_OK) return s;
+  if ((e = cudaMemcpyAsync(out_host, dout, (size_t)T * d.H * 4, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+    return cuda_fail(e, "copy out to host");
+  if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "synchronize");
+  return TM_OK;
+}
+
+tm_status trellis_moe_route(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* ids, float* w,
+                            void* stream) {
+  g_err[0] = 0;
+  if (T < 0) return fail(TM_EINVAL, "T=%d < 0", T);
+  if (E < 1 || E > tmoe::kMaxExperts) return fail(TM_EUNSUPPORTED, "E=%d outside 1..%d", E, tmoe::kMaxExperts);
+  if (k < 1 || k > 32 || k > E) return fail(TM_EINVAL, "k=%d outside 1..min(E,32)", k);
+  if (T == 0) return TM_OK;
+  if (!logits || !ids || !w) return fail(TM_EINVAL, "logits, ids and w must be non-NULL");
+  cudaError_t e = tmoe::launch_route_topk(logits, T, E, k, ids, w, (cudaStream_t)stream);
+  return e == cudaSuccess ? TM_OK : cuda_fail(e, "router");
+}
+
+tm_status trellis_moe_route_map(tm_layer* layer, const int32_t* topk_ids, int32_t T, int32_t block, int32_t* counts,
+                                int32_t* offsets, int32_t* route_of_slot, int32_t* slot_of_route, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  g_err[0] = 0;
+  if (!layer) return fail(TM_EINVAL, "layer is NULL");
+  if (T < 0) return fail(TM_EINVAL, "T=%d < 0", T);
+  if (block < 1 || block > kBnMax * 4) return fail(TM_EINVAL, "block=%d outside 1..%d", block, kBnMax * 4);
+  if (T == 0) return TM_OK;
+  if (!topk_ids || !counts || !offsets || !route_of_slot || !slot_of_route)
+    return fail(TM_EINVAL, "route map arguments must be non-NULL");
+  Layout L;
+  tm_status s = check_ws(layer, T, workspace, workspace_bytes, &L);
+  if (s != TM_OK) return s;
+  const tm_layer_desc& d = layer->desc;
+  const int R = T * d.topk;
+  const size_t need_blocks = ((size_t)R + (size_t)d.E * (block - 1)) / block + 1;
+  if (need_blocks * 4 > L.bytes[Layout::BLOCK_EXPERT]) return fail(TM_EWORKSPACE, "workspace too small for block=%d", block);
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t* err = at<uint32_t>(workspace, L, Layout::ERR);
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(err, 0, 4, st)) != cudaSuccess) return cuda_fail(e, "clear error word");
+  tmoe::RouteMapArgs rm;
+  rm.ids = topk_ids;
+  rm.R = R;
+  rm.E = d.E;
+  rm.block = block;
+  rm.rank = at<int32_t>(workspace, L, Layout::RANK);
+  rm.tile_counts = at<int32_t>(workspace, L, Layout::TILE_COUNTS);
+  rm.counts = counts;
+  rm.offsets = offsets;
+  rm.block_expert = at<int32_t>(workspace, L, Layout::BLOCK_EXPERT);
+  rm.nblocks = at<int32_t>(workspace, L, Layout::NBLOCKS);
+  rm.route_of_slot = route_of_slot;
+  rm.slot_of_route = slot_of_route;
+  rm.err = err;
+  e = tmoe::launch_route_map(rm, st);
+  return e == cudaSuccess ? TM_OK : cuda_fail(e, "route map");
+}
+
+tm_status trellis_moe_rotate_quant(tm_layer* layer, const uint16_t* x, int32_t T, int32_t mode, void* xq,
+                                   uint8_t* xs, void* stream) {
+  g_err[0] = 0;
+  if (!layer) return fail(TM_EINVAL, "layer is NULL");
+  if (T < 0) return fail(TM_EINVAL, "T=%d < 0", T);
+  if (mode != TM_MODE_W4A16 && mode != TM_MODE_W4A8) return fail(TM_EINVAL, "mode must be W4A16 or W4A8");
+  if (T == 0) return TM_OK;
+  if (!x || !xq || (mode == TM_MODE_W4A8 && !xs)) return fail(TM_EINVAL, "x, xq (and xs for W4A8) must be non-NULL");
+  if (((uintptr_t)x) % 8 || ((uintptr_t)xq) % 8) return fail(TM_EINVAL, "x and xq must be 8-byte aligned");
+  const tm_layer_desc& d = layer->desc;
+  cudaError_t e = tmoe::launch_rotate_quant(x, d.in_suh, T, d.H, d.rot_block_h, mode == TM_MODE_W4A8, xq, xs,
+                                          (cudaStream_t)stream);
+  return e == cudaSuccess ? TM_OK : cuda_fail(e, "rotate+quantize");
+}
+
+tm_status trellis_moe_decode_tiles(tm_layer* layer, int32_t proj, int32_t expert, int32_t tile0, int32_t ntiles,
+                                   int32_t mode, void* dst, void* stream) {
+  g_err[0] = 0;
+  if (!layer) return fail(TM_EINVAL, "layer is NULL");
+  const tm_layer_desc& d = layer->desc;
+  if (proj != 1 && proj != 2) return fail(TM_EINVAL, "proj=%d must be 1 or 2", proj);
+  if (expert < 0 || expert >= d.E) return fail(TM_EINVAL, "expert=%d outside 0..%d", expert, d.E - 1);
+  if (mode != TM_MODE_W4A16 && mode != TM_MODE_W4A8) return fail(TM_EINVAL, "mode must be W4A16 or W4A8");
+  const long tiles = (long)(proj == 1 ? 2 * d.I : d.H) / 16 * ((proj == 1 ? d.H : d.I) / 16);
+  if (tile0 < 0 || ntiles < 0 || tile0 + (long)ntiles > tiles)
+    return fail(TM_EINVAL, "tiles %d..%d outside 0..%ld", tile0, tile0 + ntiles, tiles);
+  if (ntiles == 0) return TM_OK;
+  if (!dst || ((uintptr_t)dst) % 16) return fail(TM_EINVAL, "dst must be non-NULL and 16-byte aligned");
+  const int K = layer->bits[expert];
+  int64_t off = 0;
+  for (int e = 0; e < expert; ++e)
+    off += (int64_t)tiles * 16 * layer->bits[e];
+  const int16_t* base = (proj == 1 ? d.fc1_payload : d.fc2_payload) + off + (int64_t)tile0 * 16 * K;
+  cudaError_t e = tmoe::launch_decode_tiles(base, K, ntiles, mode == TM_MODE_W4A8, dst, (cudaStream_t)stream);
+  return e == cudaSuccess ? TM_OK : cuda_fail(e, "decode tiles");
+}
+
+tm_status trellis_moe_workspace_region(const tm_layer* layer, int32_t T, int32_t which, size_t* offset,
+                                       size_t* bytes) {
+  g_err[0] = 0;
+  if (!layer || !offset || !bytes) return fail(TM_EINVAL, "NULL argument");
+  if (T < 0) return fail(TM_EINVAL, "T=%d < 0", T);
+  static const int map[] = {Layout::XQ, Layout::XS, Layout::ZQ, Layout::ZS, Layout::ROWS, Layout::SLOT_OF_ROUTE, Layout::ERR};
+  if (which < 0 || which >= (int)(sizeof(map) / sizeof(map[0]))) return fail(TM_EINVAL, "unknown region %d", which);
+  const Layout L = make_layout(layer->desc, T);
+  *offset = L.off[map[which]];
+  *bytes = L.bytes[map[which]];
+  return TM_OK;
+}
+
+tm_status trellis_moe_set_stage_events(tm_layer* layer, void* const* events, int32_t n) {
+  g_err[0] = 0;
+  if (!layer) return fail(TM_EINVAL, "layer is NULL");
+  if (events == nullptr || n == 0) {
+    for (int i = 0; i < 7; ++i) layer->stage_ev[i] = nullptr;
+    return TM_OK;
+  }
+  if (n != 7) return fail(TM_EINVAL, "n=%d: pass 7 events (NULL entries allowed) or none", n);
+  for (int i = 0; i < 7; ++i) layer->stage_ev[i] = (cudaEvent_t)events[i];
+  return TM_OK;
+}
+
+tm_status trellis_moe_poll_error(tm_layer* layer, void* workspace, uint32_t* flags, void* stream) {
+  g_err[0] = 0;
+  if (!layer || !workspace || !flags) return fail(TM_EINVAL, "NULL argument");
+  // The error word is the first region of every layout, at offset 0.
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t h = 0;
+  cudaError_t e;
+  if ((e = cudaMemcpyAsync(&h, workspace, 4, cudaMemcpyDeviceToHost, st)) != cudaSuccess) return cuda_fail(e, "read error word");
+  if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "synchronize");
+  if ((e = cudaMemsetAsync(workspace, 0, 4, st)) != cudaSuccess) return cuda_fail(e, "clear error word");
+  *flags = h;
+  if (h != 0) return fail(TM_EDEVICE, "device error flags 0x%x (bit 0: expert id out of range)", h);
+  return TM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,225 @@
+// Device helpers shared by the trellis-MoE kernels (sm_103a).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tmoe {
+
+// ---------------------------------------------------------------------------
+// MCG codebook (sparkinfer PR #90 "moe: integrate EXL3 Trellis into the fused
+// W4A16 API", review of intrinsics.py: multiplier 0xCBAC1FED, mask 0x8fff8fff,
+// third constant 0x3b603b60). A 16-bit state s maps to
+//   y = ((s * 0xCBAC1FED) & 0x8fff8fff) ^ 0x3b603b60,
+// whose two 16-bit halves are fp16 numbers; the weight is their fp16 sum.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kMcgMult = 0xCBAC1FEDu;
+constexpr uint32_t kMcgMask = 0x8FFF8FFFu;
+constexpr uint32_t kMcgXor = 0x3B603B60u;
+
+__device__ __forceinline__ uint32_t mcg_raw(uint32_t s) {
+  return ((s * kMcgMult) & kMcgMask) ^ kMcgXor;
+}
+
+// Two weights from the raw codebook words of two states: (cb(a), cb(b)) as a
+// half2 with cb(a) in the low half. One fp16x2 add rounds each sum to nearest.
+__device__ __forceinline__ uint32_t cb_pair_from_raw(uint32_t ya, uint32_t yb) {
+  uint32_t lo = __byte_perm(ya, yb, 0x5410);
+  uint32_t hi = __byte_perm(ya, yb, 0x7632);
+  __half2 r = __hadd2(*reinterpret_cast<__half2*>(&lo), *reinterpret_cast<__half2*>(&hi));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// fp16x2 -> two E4M3 bytes (round to nearest even, saturate to +-448), low byte
+// from the low half.
+__device__ __forceinline__ uint32_t e4m3x2_from_half2(uint32_t h2) {
+  __half2_raw r;
+  r.x = (unsigned short)(h2 & 0xFFFF);
+  r.y = (unsigned short)(h2 >> 16);
+  return (uint32_t)__nv_cvt_halfraw2_to_fp8x2(r, __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ uint32_t e4m3x2_from_float2(float lo, float hi) {
+  float2 v = make_float2(lo, hi);
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
+}
+
+// Swap the two 16-bit words of a little-endian 32-bit load so that the first
+// stored word is the most significant (tile streams are MSB first, words in
+// storage order).
+__device__ __forceinline__ uint32_t swap_words(uint32_t v) { return __byte_perm(v, 0, 0x1032); }
+
+// ---------------------------------------------------------------------------
+// Trellis states. Bit p of a tile's stream is bit (15 - p%16) of word p/16;
+// the state of weight j is the 16 bits starting at stream bit (j+1)K-16
+// (mod 256K), first bit most significant. A "run" is 8 consecutive states
+// j0..j0+7 with j0 % 8 == 0 (half a tile row).
+// ---------------------------------------------------------------------------
+
+// Raw words for a run, any K in 2..6: the 64 stream bits starting at the word
+// holding bit q0 = (j0+1)K-16 (mod 256K). Returns the window as hi:lo and the
+// bit offset of state j0 inside it.
+template <int K>
+__device__ __forceinline__ void run_window_generic(const uint16_t* __restrict__ tile, int j0,
+                                                   uint32_t& hi, uint32_t& lo, int& off) {
+  constexpr int NB = 256 * K;
+  constexpr int NW = 16 * K;
+  int q0 = (j0 + 1) * K - 16;
+  if (q0 < 0) q0 += NB;
+  const int w = q0 >> 4;
+  off = q0 & 15;
+  const uint32_t w0 = __ldg(tile + w);
+  const uint32_t w1 = __ldg(tile + (w + 1) % NW);
+  const uint32_t w2 = __ldg(tile + (w + 2) % NW);
+  const uint32_t w3 = __ldg(tile + (w + 3) % NW);
+  hi = (w0 << 16) | w1;
+  lo = (w2 << 16) | w3;
+}
+
+// States of a run from its window (off + 7K <= 48 holds for every run start
+// j0 % 8 == 0 and K in 2..6).
+template <int K>
+__device__ __forceinline__ void run_states_generic(uint32_t hi, uint32_t lo, int off, uint32_t (&s)[8]) {
+  const uint64_t v = ((uint64_t)hi << 32) | lo;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) s[i] = (uint32_t)(v >> (48 - off - i * K)) & 0xFFFFu;
+}
+
+// K = 4 fast path. Row r of a tile is words 4r..4r+3; the run (r, h) needs
+// the 32-bit word pair starting at word 4r+2h (cur) and the pair before it
+// (prev, wrapping around the tile). Both are 4-byte aligned loads.
+__device__ __forceinline__ void run_load_k4(const uint16_t* __restrict__ tile, int row, int h,
+                                            uint32_t& prev, uint32_t& cur) {
+  const uint32_t* t32 = reinterpret_cast<const uint32_t*>(tile);
+  const int c = 2 * row + h;          // 32-bit word index of cur, 0..31
+  cur = __ldg(t32 + c);
+  prev = __ldg(t32 + ((c + 31) & 31));
+}
+
+// States of a K = 4 run: with V = prev:cur (as stream-order 64 bits), state i
+// sits at V >> (28 - 4i). Pairs (i, i+4) come out of one funnel shift.
+__device__ __forceinline__ void run_states_k4(uint32_t prev_raw, uint32_t cur_raw, uint32_t (&s)[8]) {
+  const uint32_t P = swap_words(prev_raw);
+  const uint32_t C = swap_words(cur_raw);
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const uint32_t q = (m == 3) ? C : __funnelshift_r(C, P, 12 - 4 * m);
+    s[m] = q >> 16;
+    s[m + 4] = q & 0xFFFFu;
+  }
+}
+
+// Decoded fp16 weights of a run as 4 half2 registers: (w0,w1), (w2,w3), (w4,w5), (w6,w7).
+__device__ __forceinline__ void run_weights_f16(const uint32_t (&s)[8], uint32_t (&w)[4]) {
+  uint32_t y[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) y[i] = mcg_raw(s[i]);
+#pragma unroll
+  for (int p = 0; p < 4; ++p) w[p] = cb_pair_from_raw(y[2 * p], y[2 * p + 1]);
+}
+
+// E4M3 weights of a run as 2 registers of 4 bytes: (w0..w3), (w4..w7).
+__device__ __forceinline__ void run_weights_e4m3(const uint32_t (&s)[8], uint32_t (&q)[2]) {
+  uint32_t w[4];
+  run_weights_f16(s, w);
+  q[0] = e4m3x2_from_half2(w[0]) | (e4m3x2_from_half2(w[1]) << 16);
+  q[1] = e4m3x2_from_half2(w[2]) | (e4m3x2_from_half2(w[3]) << 16);
+}
+
+// ---------------------------------------------------------------------------
+// Warp Walsh-Hadamard transform (Sylvester order) of a vector spread over the
+// warp, PER consecutive values per lane (lane l holds v[PER*l .. PER*l+PER-1]),
+// applied independently to blocks of B entries (B a power of two, B <= 32*PER).
+// Butterfly: for h = 1, 2, 4, ...: (x[i], x[i+h]) <- (x[i] + x[i+h], x[i] - x[i+h]).
+// ---------------------------------------------------------------------------
+template <int PER>
+__device__ __forceinline__ void warp_fwht(float (&v)[PER], int B) {
+  // in-register stages
+#pragma unroll
+  for (int h = 1; h < PER; h <<= 1) {
+    if (h < B) {
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        if ((i & h) == 0) {
+          const float a = v[i], b = v[i + h];
+          v[i] = a + b;
+          v[i + h] = a - b;
+        }
+      }
+    }
+  }
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int lh = 1; lh < 32; lh <<= 1) {
+    if (lh * PER < B) {
+      const bool upper = (lane & lh) != 0;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const float o = __shfl_xor_sync(0xFFFFFFFFu, v[i], lh);
+        v[i] = upper ? (o - v[i]) : (v[i] + o);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ float hadamard_scale(int B) {
+  // 1/sqrt(B) rounded to fp32 (B = 128: 0.088388347648...)
+  return B == 128 ? 0.08838834764831845f : (B == 64 ? 0.125f : (B == 32 ? 0.17677669529663687f : 1.0f));
+}
+
+// UE8M0 exponent of a block from its max |v|: e = ceil(log2(fp32(amax/448))),
+// clamped to [-127, 127]; amax == 0 gives -127 (flashinfer PR #69 "b12x fused
+// MoE: TrellisMX (procedural NPK) source format with an in-tree P8 runtime",
+// Evidence, precision notes: exponent from the exact FP32 bits of amax/448).
+__device__ __forceinline__ int e8m0_exponent(float amax) {
+  const float q = __fdiv_rn(amax, 448.0f);
+  const uint32_t b = __float_as_uint(q) & 0x7FFFFFFFu;
+  if (b == 0) return -127;
+  const int ex = (int)(b >> 23);
+  const uint32_t man = b & 0x7FFFFFu;
+  int e;
+  if (ex == 0) {
+    e = (32 - __clz(man - 1)) - 149;  // ceil(log2(man)) - 149
+  } else {
+    e = ex - 127 + (man != 0 ? 1 : 0);
+  }
+  return max(-127, min(127, e));
+}
+
+// 2^e as a float, exact for e in [-149, 127].
+__device__ __forceinline__ float exp2_int(int e) {
+  if (e >= -126) return __uint_as_float((uint32_t)(e + 127) << 23);
+  return __uint_as_float(1u << (e + 149));
+}
+
+// ---------------------------------------------------------------------------
+// Warp-level MMA (legacy mma.sync) wrappers.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%10,%10,%10};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// cp.async 16 bytes global -> shared; src_bytes = 0 zero-fills.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+
+}  // namespace tmoe
