@@ -31,6 +31,9 @@ Readings where the pages are silent (each listed in the design doc):
 """
 from __future__ import annotations
 
+import concurrent.futures
+import os
+
 import numpy as np
 
 MCG_MULT = 0xCBAC1FED
@@ -99,9 +102,24 @@ def tile_states_scalar(words, K: int) -> list:
     return out
 
 
+def tile_states_words(words: np.ndarray, K: int) -> np.ndarray:
+    """The same states read as 16-bit windows of 32-bit word pairs: with
+    q = (j+1)K-16 mod 256K, w = q // 16 and o = q % 16, the window is the low
+    16 bits of ((word[w] << 16 | word[w+1]) >> (16 - o)), words taken
+    circularly. Equal to tile_states (tested); used for speed."""
+    words = np.asarray(words)
+    nw = 16 * K
+    assert words.shape[-1] == nw, (words.shape, K)
+    u = words.astype(np.int16).view(np.uint16).astype(np.uint32)
+    q = ((np.arange(256) + 1) * K - 16) % (256 * K)
+    w, o = q // 16, q % 16
+    pair = (u[..., w] << np.uint32(16)) | u[..., (w + 1) % nw]
+    return (pair >> (16 - o).astype(np.uint32)) & np.uint32(0xFFFF)
+
+
 def decode_tiles_fp16(words: np.ndarray, K: int) -> np.ndarray:
     """Decoded weights of tiles in weight order j: [..., 16K] -> float16 [..., 256]."""
-    return codebook_fp16(tile_states(words, K))
+    return codebook_fp16(tile_states_words(words, K))
 
 
 def place_tile(w256: np.ndarray) -> np.ndarray:
@@ -122,13 +140,22 @@ def expert_payload(payload: np.ndarray, rows: int, cols: int, bits: np.ndarray, 
     return np.asarray(payload[start:start + int(counts[e])]).reshape(rows // 16, cols // 16, 16 * K)
 
 
-def decode_matrix(tiles: np.ndarray, K: int, chunk: int = 2048) -> np.ndarray:
+def decode_matrix(tiles: np.ndarray, K: int, chunk: int = 16384) -> np.ndarray:
     """Dense float16 [rows, cols] from one expert's tiles [rows/16][cols/16][16K]."""
     tr, tc, nw = tiles.shape
     assert nw == 16 * K
     flat = tiles.reshape(tr * tc, nw)
     out = np.empty((tr * tc, 256), dtype=np.float16)
-    for a in range(0, tr * tc, chunk):
+
+    def work(a):
         out[a:a + chunk] = decode_tiles_fp16(flat[a:a + chunk], K)
+
+    starts = range(0, tr * tc, chunk)
+    if len(starts) > 1:
+        with concurrent.futures.ThreadPoolExecutor(min(len(starts), os.cpu_count() or 1)) as ex:
+            list(ex.map(work, starts))
+    else:
+        for a in starts:
+            work(a)
     w = out.reshape(tr, tc, 16, 16).transpose(0, 2, 1, 3)
     return np.ascontiguousarray(w.reshape(tr * 16, tc * 16))
