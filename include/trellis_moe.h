@@ -184,6 +184,25 @@ tm_status trellis_moe_set_stage_events(tm_layer* layer, void* const* events, int
  * was set, else TM_OK. */
 tm_status trellis_moe_poll_error(tm_layer* layer, void* workspace, uint32_t* flags, void* stream);
 
+/* Route map with no scratch from the caller and no allocation. No counterpart
+ * on the source pages: it exists for callers that cannot allocate or lend
+ * device memory -- code running while a CUDA graph is being captured (where
+ * cudaMalloc is not allowed), hosts that own all device memory through a fixed
+ * plan and pass only inputs and outputs, and latency-critical loops that must
+ * not enter the allocator after start-up because allocation can synchronise
+ * the device. Same arguments and results as trellis_moe_route_map, with the
+ * layer's E and topk passed directly. Its scratch is one static device array
+ * of about 10 KB per GPU, held while the library is loaded; limits:
+ * T*topk <= 1024 routes, E <= 256 (TM_EUNSUPPORTED beyond, with a message).
+ * The first call on a device looks up that array's device address, so make it
+ * before any stream capture. All calls on a device share the array: calls
+ * whose kernels overlap on the GPU race, so order them on one stream. Every
+ * call clears what must start at zero. Dropped (out-of-range) ids get
+ * slot_of_route -1 as in trellis_moe_route_map; no error word is kept. */
+tm_status trellis_moe_route_map_static(const int32_t* topk_ids, int32_t T, int32_t E, int32_t topk,
+                                       int32_t block, int32_t* counts, int32_t* offsets,
+                                       int32_t* route_of_slot, int32_t* slot_of_route, void* stream);
+
 /* Message of the last failed call on this thread ("" if none). */
 const char* trellis_moe_last_error(void);
 

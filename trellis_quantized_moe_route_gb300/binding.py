@@ -30,7 +30,7 @@ EXPORTED = [
     "trellis_moe_forward_logits", "trellis_moe_forward_host", "trellis_moe_route",
     "trellis_moe_route_map", "trellis_moe_rotate_quant", "trellis_moe_decode_tiles",
     "trellis_moe_workspace_region", "trellis_moe_set_stage_events", "trellis_moe_poll_error",
-    "trellis_moe_last_error", "trellis_moe_destroy",
+    "trellis_moe_last_error", "trellis_moe_destroy", "trellis_moe_route_map_static",
 ]
 
 
@@ -79,6 +79,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "trellis_moe_poll_error": (I32, [P, P, ctypes.POINTER(ctypes.c_uint32), P]),
         "trellis_moe_last_error": (ctypes.c_char_p, []),
         "trellis_moe_destroy": (None, [P]),
+        "trellis_moe_route_map_static": (I32, [P, I32, I32, I32, I32, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -127,6 +128,23 @@ def route(logits, k: int, stream=None):
     w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
     _check(lib.trellis_moe_route(_ptr(logits), T, E, k, _ptr(ids), _ptr(w), _stream_ptr(stream)))
     return ids, w
+
+
+def route_map_static(ids, E: int, block: int, stream=None):
+    """Route map through trellis_moe_route_map_static: no workspace and no
+    allocation inside the library (for callers that cannot provide scratch).
+    The result tensors here are allocated by torch, in the caller's code."""
+    torch = _torch()
+    lib = load_library()
+    T, k = int(ids.shape[0]), int(ids.shape[1])
+    R = T * k
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    ros = torch.empty(R + E * (block - 1) + 1, dtype=torch.int32, device="cuda")
+    sor = torch.empty(max(R, 1), dtype=torch.int32, device="cuda")
+    _check(lib.trellis_moe_route_map_static(_ptr(ids), T, E, k, block, _ptr(counts), _ptr(offsets), _ptr(ros),
+                                            _ptr(sor), _stream_ptr(stream)))
+    return {"counts": counts, "offsets": offsets, "route_of_slot": ros, "slot_of_route": sor[:R]}
 
 
 class TrellisMoE:

@@ -207,6 +207,8 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
 }  // namespace
 
 namespace tmoe {
+void set_last_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+
 cudaError_t launch_fc1_f16(const FcArgs& a, int bi, int bn, int uniform_k, int max_blocks, cudaStream_t st);
 cudaError_t launch_fc1_e4m3(const FcArgs& a, int bi, int bn, int uniform_k, int max_blocks, cudaStream_t st);
 cudaError_t launch_fc2_f16(const FcArgs& a, int bn, int uniform_k, int max_blocks, cudaStream_t st);

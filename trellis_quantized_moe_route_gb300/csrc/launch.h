@@ -60,6 +60,9 @@ cudaError_t launch_fc2(const FcArgs& a, bool w4a8, int bn, int uniform_k, int ma
 cudaError_t launch_combine(const float* rows, const int32_t* slot_of_route, const float* w, int T, int H, int k,
                            float* out, cudaStream_t st);
 
+// Sets the calling thread's message returned by trellis_moe_last_error().
+void set_last_error(const char* msg);
+
 cudaError_t launch_decode_tiles(const int16_t* tiles, int K, int ntiles, bool e4m3, void* dst, cudaStream_t st);
 
 }  // namespace tmoe
