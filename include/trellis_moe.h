@@ -104,12 +104,12 @@ tm_status trellis_moe_prepare(const tm_layer_desc* desc, tm_layer** out, size_t*
 size_t trellis_moe_workspace_size(const tm_layer* layer, int32_t max_tokens);
 
 /* Full layer from given routes.
- *   x        bf16 [T, H] activations
+ *   x        bf16 [T, H] activations (8-byte aligned)
  *   topk_ids int32 [T, topk] expert ids; out-of-range ids are dropped from the
  *            sum and flagged in the device error word (trellis_moe_poll_error)
  *   topk_w   fp32 [T, topk] route weights
  *   mode     tm_mode
- *   out      fp32 [T, H] result (overwritten)
+ *   out      fp32 [T, H] result (overwritten; 16-byte aligned)
  *   workspace >= trellis_moe_workspace_size(layer, T) bytes, 256-byte aligned;
  *            contents on entry are ignored (any bytes give the same result).
  * T = 0 is a no-op. Errors: TM_EINVAL, TM_EWORKSPACE, TM_ECUDA. */

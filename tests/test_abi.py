@@ -64,3 +64,4 @@ def test_host_validation_without_gpu(lib):
     assert lib.trellis_moe_forward(None, P(8), P(8), P(8), 1, 0, P(8), P(256), 1 << 20, None) == -1
     assert lib.trellis_moe_set_stage_events(None, None, 0) == -1
     lib.trellis_moe_destroy(None)
+

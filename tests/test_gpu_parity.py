@@ -328,3 +328,76 @@ def test_large_config_prefill_sampled():
     moe = _moe(L, cfg.T)
     err, _, _ = run_and_compare(moe, L, cfg, cfg.T, "w4a16", tokens=_sample(cfg.T, 3, 3))
     assert err < TOL["w4a16"], err
+
+
+# ------------------------------------- decode-rows path (T*topk small) ---
+# These shapes keep T*topk below 4*E, which selects the split-K decode kernels.
+DECODE_SHAPES = [
+    dict(T=4, E=16, topk=2, bits=(2, 3, 4), I=320, rot_block_i=64, H=512),   # mixed K, 64-wide I blocks
+    dict(T=3, E=32, topk=4),                                                 # K=4, rotation blocks 128
+    dict(T=8, E=64, topk=8, bits=(5,), H=512, I=256),                        # generic K=5 decode
+    dict(T=2, E=16, topk=3, rot_block_h=1, rot_block_i=1),                   # identity rotations
+    dict(T=1, E=8, topk=8, H=1024, I=512),                                   # every expert, one token
+]
+
+
+@pytest.mark.parametrize("mode", ["w4a8", "w4a16"])
+@pytest.mark.parametrize("kw", DECODE_SHAPES)
+def test_decode_path_layers(mode, kw):
+    cfg = small_cfg(**kw)
+    assert cfg.T * cfg.topk < 4 * cfg.E
+    L = synth.make_layer(cfg)
+    moe = _moe(L, cfg.T)
+    err, _, _ = run_and_compare(moe, L, cfg, cfg.T, mode)
+    assert err < TOL[mode], err
+
+
+def test_decode_path_deterministic_poisoned_and_atomic():
+    cfg = small_cfg(T=6, E=32, topk=4)
+    L = synth.make_layer(cfg)
+    moe = _moe(L, cfg.T)
+    x_bits, logits = synth.make_tokens(cfg)
+    x, lg = upload_tokens(x_bits, logits)
+    a = moe.forward_logits(x, lg, mode="w4a8").clone()
+    moe.workspace.fill_(0xFF)
+    b = moe.forward_logits(x, lg, mode="w4a8").clone()
+    moe.workspace.fill_(0x7F)
+    c = moe.forward_logits(x, lg, mode="w4a8").clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b) and torch.equal(a, c)
+    perm = synth.permutation(synth.Stream(4, 4), cfg.T)
+    xp, lgp = upload_tokens(x_bits[perm], logits[perm])
+    p = moe.forward_logits(xp, lgp, mode="w4a8").cpu().numpy()
+    assert np.array_equal(p, a.cpu().numpy()[perm])
+    atomic = _moe(L, cfg.T, deterministic=False)
+    err, _, _ = run_and_compare(atomic, L, cfg, cfg.T, "w4a8")
+    assert err < TOL["w4a8"], err
+
+
+def test_decode_path_drops_bad_ids():
+    cfg = small_cfg(T=3, E=32, topk=4)
+    L = synth.make_layer(cfg)
+    moe = _moe(L, cfg.T)
+    x_bits, logits = synth.make_tokens(cfg)
+    ids, w = oracle_routes(logits, cfg.topk)
+    bad = ids.copy()
+    bad[0, 3] = 40
+    bad[2, 0] = -3
+    x, _ = upload_tokens(x_bits, logits)
+    out = moe.forward(x, torch.from_numpy(bad).cuda(), torch.from_numpy(w.astype(np.float32)).cuda(), mode="w4a8")
+    assert moe.poll_error() == 1
+    w2 = w.copy()
+    w2[0, 3] = 0.0
+    w2[2, 0] = 0.0
+    ref = olayer.layer_forward(L, x_bits, np.clip(bad, 0, cfg.E - 1), w2, mode="w4a8")
+    assert rel_row_err(out.cpu().numpy(), ref) < TOL["w4a8"]
+
+
+def test_workspace_size_monotonic_in_tokens():
+    """A workspace sized for T tokens serves every smaller T, although the
+    decode path's scratch exists only for small T."""
+    cfg = small_cfg(T=64, E=16, topk=4)
+    moe = _moe(synth.make_layer(cfg), 64)
+    sizes = [int(moe.lib.trellis_moe_workspace_size(moe.handle, t)) for t in range(0, 65)]
+    assert all(a <= b for a, b in zip(sizes, sizes[1:]))
+    assert sizes[-1] == moe.workspace_bytes

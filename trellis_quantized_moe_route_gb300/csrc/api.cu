@@ -56,12 +56,50 @@ constexpr int kBnMin = 8;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
+// FC1 half-row block: the epilogue needs whole rotation blocks of I.
+int fc1_bi(const tm_layer_desc& d) {
+  int bi = (d.rot_block_i == 128 || (d.I % 128 == 0 && d.rot_block_i != 64)) ? 128 : 64;
+  if (d.I % bi != 0) bi = 64;
+  return bi;
+}
+
+// Decode-rows path plan: used when T*topk <= 1024 and experts see fewer than
+// 4 routes on average (route blocks of 8).
+struct DecPlan {
+  bool use;
+  int max_blocks, bi, units1, parts1, units2, s1, k1, s2, k2;
+  size_t partial_floats, cnt_ints;
+};
+
+DecPlan dec_plan(const tm_layer_desc& d, int T) {
+  DecPlan p{};
+  const long R = (long)T * d.topk;
+  p.use = R >= 1 && R <= 1024 && R < 4L * d.E;
+  p.bi = fc1_bi(d);
+  p.units1 = d.I / p.bi;
+  p.parts1 = 2 * p.bi / 128;
+  p.units2 = d.H / 128;
+  p.max_blocks = (int)(R / 8 + std::min<long>(d.E, R) + 1);
+  const long active = std::max<long>(1, std::min<long>(d.E, R));
+  auto split = [](int kdim, int s, int& kc) {
+    kc = ((kdim + s - 1) / s + 63) / 64 * 64;
+    return (kdim + kc - 1) / kc;
+  };
+  p.s1 = split(d.H, tmoe::dec_ksplit(d.H, active * p.units1 * p.parts1), p.k1);
+  p.s2 = split(d.I, tmoe::dec_ksplit(d.I, active * p.units2), p.k2);
+  p.partial_floats = (size_t)p.max_blocks *
+                     std::max<size_t>((size_t)p.units1 * p.s1 * 2 * p.bi, (size_t)p.units2 * p.s2 * 128) * 8;
+  p.cnt_ints = (size_t)p.max_blocks * (p.units1 + p.units2) + (size_t)T * p.units2;
+  if (!p.use) p.partial_floats = p.cnt_ints = 0;
+  return p;
+}
+
 // Regions of a workspace sized for T tokens (T*topk routes).
 struct Layout {
   enum {
     ERR, XQ, XS, ZQ, ZS, ROWS, SLOT_OF_ROUTE,
     IDS, W, RANK, TILE_COUNTS, COUNTS, OFFSETS, BLOCK_EXPERT, NBLOCKS, ROUTE_OF_SLOT,
-    HOST_X, HOST_LOGITS, HOST_OUT, COUNT
+    HOST_X, HOST_LOGITS, HOST_OUT, DEC_PARTIAL, DEC_CNT, COUNT
   };
   size_t off[COUNT];
   size_t bytes[COUNT];
@@ -92,6 +130,17 @@ Layout make_layout(const tm_layer_desc& d, int T) {
   L.bytes[Layout::HOST_X] = (size_t)T * d.H * 2;
   L.bytes[Layout::HOST_LOGITS] = (size_t)T * d.E * 4;
   L.bytes[Layout::HOST_OUT] = (size_t)T * d.H * 4;
+  // The decode path's scratch is not monotonic in T (larger T switches to the
+  // general path), so size it for the worst T' <= T: a workspace that fits T
+  // then fits every smaller call too.
+  size_t dec_partial = 0, dec_cnt = 0;
+  for (int t = 1; t <= T && (long)t * d.topk <= 1024; ++t) {
+    const DecPlan dp = dec_plan(d, t);
+    dec_partial = std::max(dec_partial, dp.partial_floats);
+    dec_cnt = std::max(dec_cnt, dp.cnt_ints);
+  }
+  L.bytes[Layout::DEC_PARTIAL] = dec_partial * 4;
+  L.bytes[Layout::DEC_CNT] = dec_cnt * 4;
   size_t o = 0;
   for (int i = 0; i < Layout::COUNT; ++i) {
     L.off[i] = o;
@@ -123,15 +172,33 @@ int choose_bn(const tm_layer_desc& d, int T) {
   return (R < 4L * d.E) ? kBnMin : kBnMax;
 }
 
-tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, const float* w, int T, int mode,
-                    float* out, void* ws, const Layout& L, cudaStream_t st) {
+tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids, const float* w,
+                          const float* logits, int T, bool w4a8, float* out, void* ws, const Layout& L,
+                          const DecPlan& dp, cudaStream_t st);
+
+// One forward pass. With `logits` non-NULL the router runs first (fused into
+// the decode-path prologue) and writes ids and w into the workspace.
+tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, const float* w, const float* logits,
+                    int T, int mode, float* out, void* ws, const Layout& L, cudaStream_t st) {
   const tm_layer_desc& d = layer->desc;
   const bool w4a8 = (mode == TM_MODE_W4A8) || (mode == TM_MODE_AUTO && T <= d.decode_max_rows);
   const int R = T * d.topk;
   const int bn = choose_bn(d, T);
   cudaError_t e;
   uint32_t* err = at<uint32_t>(ws, L, Layout::ERR);
+  if (logits) {
+    ids = at<int32_t>(ws, L, Layout::IDS);
+    w = at<float>(ws, L, Layout::W);
+  }
+  const DecPlan dp = dec_plan(d, T);
+  // (the decode prologue clears the error word itself)
+  if (dp.use) return run_decode_path(layer, x, ids, w, logits, T, w4a8, out, ws, L, dp, st);
   if ((e = cudaMemsetAsync(err, 0, 4, st)) != cudaSuccess) return cuda_fail(e, "clear error word");
+  if (logits) {
+    e = tmoe::launch_route_topk(logits, T, d.E, d.topk, const_cast<int32_t*>(ids), const_cast<float*>(w), st);
+    if (e != cudaSuccess) return cuda_fail(e, "router");
+    if ((e = stage_mark(layer, 1, st)) != cudaSuccess) return cuda_fail(e, "stage event");
+  }
 
   tmoe::RouteMapArgs rm;
   rm.ids = ids;
@@ -204,6 +271,105 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
   return TM_OK;
 }
 
+tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids, const float* w,
+                          const float* logits, int T, bool w4a8, float* out, void* ws, const Layout& L,
+                          const DecPlan& dp, cudaStream_t st) {
+  const tm_layer_desc& d = layer->desc;
+  const int R = T * d.topk;
+  cudaError_t e;
+  tmoe::DecPrologueArgs pa{};
+  pa.logits = logits;
+  pa.ids_out = const_cast<int32_t*>(ids);
+  pa.w_out = const_cast<float*>(w);
+  pa.rm.ids = ids;
+  pa.rm.R = R;
+  pa.rm.E = d.E;
+  pa.rm.block = 8;
+  pa.rm.rank = at<int32_t>(ws, L, Layout::RANK);
+  pa.rm.tile_counts = at<int32_t>(ws, L, Layout::TILE_COUNTS);
+  pa.rm.counts = at<int32_t>(ws, L, Layout::COUNTS);
+  pa.rm.offsets = at<int32_t>(ws, L, Layout::OFFSETS);
+  pa.rm.block_expert = at<int32_t>(ws, L, Layout::BLOCK_EXPERT);
+  pa.rm.nblocks = at<int32_t>(ws, L, Layout::NBLOCKS);
+  pa.rm.route_of_slot = at<int32_t>(ws, L, Layout::ROUTE_OF_SLOT);
+  pa.rm.slot_of_route = at<int32_t>(ws, L, Layout::SLOT_OF_ROUTE);
+  pa.rm.err = at<uint32_t>(ws, L, Layout::ERR);
+  pa.x = x;
+  pa.suh = d.in_suh;
+  pa.T = T;
+  pa.H = d.H;
+  pa.topk = d.topk;
+  pa.rot_b = d.rot_block_h;
+  pa.w4a8 = w4a8 ? 1 : 0;
+  pa.xq = at<void>(ws, L, Layout::XQ);
+  pa.xs = at<uint8_t>(ws, L, Layout::XS);
+  pa.zero_i32 = at<int32_t>(ws, L, Layout::DEC_CNT);
+  pa.n_zero_i32 = (int)dp.cnt_ints;
+  pa.out = out;
+  pa.out_n = (long)T * d.H;
+  if ((e = tmoe::launch_dec_prologue(pa, st)) != cudaSuccess) return cuda_fail(e, "decode prologue");
+  for (int i = 1; i <= 3; ++i)
+    if ((e = stage_mark(layer, i, st)) != cudaSuccess) return cuda_fail(e, "stage event");
+
+  tmoe::DecArgs d1{};
+  tmoe::FcArgs& a1 = d1.f;
+  a1.E = d.E; a1.H = d.H; a1.I = d.I; a1.topk = d.topk;
+  a1.rot_b = d.rot_block_i;
+  a1.payload = d.fc1_payload;
+  a1.word_off = layer->d_off1;
+  a1.bits = layer->d_bits;
+  a1.scale = d.fc1_scale;
+  a1.rot_tab = d.rot_tab;
+  a1.act = pa.xq;
+  a1.act_scale = pa.xs;
+  a1.route_of_slot = pa.rm.route_of_slot;
+  a1.block_expert = pa.rm.block_expert;
+  a1.nblocks = pa.rm.nblocks;
+  a1.out_act = at<void>(ws, L, Layout::ZQ);
+  a1.out_scale = at<uint8_t>(ws, L, Layout::ZS);
+  a1.route_w = w;
+  a1.atomic = d.deterministic ? 0 : 1;
+  d1.ksplit = dp.s1;
+  d1.kchunk = dp.k1;
+  d1.parts = dp.parts1;
+  d1.units_m = dp.units1;
+  d1.bi = dp.bi;
+  d1.partial = at<float>(ws, L, Layout::DEC_PARTIAL);
+  d1.unit_cnt = pa.zero_i32;
+  d1.tok_cnt = nullptr;
+  d1.slot_of_route = pa.rm.slot_of_route;
+  d1.route_w = w;
+  d1.out = out;
+  d1.T = T;
+  if ((e = tmoe::launch_dec_fc(d1, 1, w4a8, layer->uniform_k, dp.max_blocks, st)) != cudaSuccess)
+    return cuda_fail(e, "FC1 (decode rows)");
+  if ((e = stage_mark(layer, 4, st)) != cudaSuccess) return cuda_fail(e, "stage event");
+
+  tmoe::DecArgs d2 = d1;
+  tmoe::FcArgs& a2 = d2.f;
+  a2.rot_b = d.rot_block_h;
+  a2.payload = d.fc2_payload;
+  a2.word_off = layer->d_off2;
+  a2.scale = d.fc2_scale;
+  a2.rot_tab = d.out_svh;
+  a2.act = a1.out_act;
+  a2.act_scale = a1.out_scale;
+  a2.out_act = nullptr;
+  a2.out_scale = nullptr;
+  a2.out_f32 = at<float>(ws, L, Layout::ROWS);
+  d2.ksplit = dp.s2;
+  d2.kchunk = dp.k2;
+  d2.parts = 1;
+  d2.units_m = dp.units2;
+  d2.unit_cnt = pa.zero_i32 + (size_t)dp.max_blocks * dp.units1;
+  d2.tok_cnt = pa.zero_i32 + (size_t)dp.max_blocks * (dp.units1 + dp.units2);
+  if ((e = tmoe::launch_dec_fc(d2, 2, w4a8, layer->uniform_k, dp.max_blocks, st)) != cudaSuccess)
+    return cuda_fail(e, "FC2 (decode rows)");
+  for (int i = 5; i <= 6; ++i)
+    if ((e = stage_mark(layer, i, st)) != cudaSuccess) return cuda_fail(e, "stage event");
+  return TM_OK;
+}
+
 }  // namespace
 
 namespace tmoe {
@@ -267,8 +433,7 @@ tm_status trellis_moe_prepare(const tm_layer_desc* desc, tm_layer** out, size_t*
     o1 += (int64_t)(2 * d.I / 16) * (d.H / 16) * 16 * k;
     o2 += (int64_t)(d.H / 16) * (d.I / 16) * 16 * k;
   }
-  L->bi = (d.rot_block_i == 128 || (d.I % 128 == 0 && d.rot_block_i != 64)) ? 128 : 64;
-  if (d.I % L->bi != 0) L->bi = 64;
+  L->bi = fc1_bi(d);
   cudaError_t e;
   if ((e = cudaGetDevice(&L->device)) != cudaSuccess) { delete L; return cuda_fail(e, "cudaGetDevice"); }
   L->d_off1 = L->d_off2 = nullptr;
@@ -318,12 +483,13 @@ tm_status trellis_moe_forward(tm_layer* layer, const uint16_t* x, const int32_t*
   if (check_mode(mode) != TM_OK) return TM_EINVAL;
   if (T == 0) return TM_OK;
   if (!x || !topk_ids || !topk_w || !out) return fail(TM_EINVAL, "x, topk_ids, topk_w and out must be non-NULL");
+  if (((uintptr_t)x) % 8 || ((uintptr_t)out) % 16) return fail(TM_EINVAL, "x must be 8-byte and out 16-byte aligned");
   Layout L;
   tm_status s = check_ws(layer, T, workspace, workspace_bytes, &L);
   if (s != TM_OK) return s;
   cudaError_t e;
   if ((e = stage_mark(layer, 0, (cudaStream_t)stream)) != cudaSuccess) return cuda_fail(e, "stage event");
-  return run_layer(layer, x, topk_ids, topk_w, T, mode, out, workspace, L, (cudaStream_t)stream);
+  return run_layer(layer, x, topk_ids, topk_w, nullptr, T, mode, out, workspace, L, (cudaStream_t)stream);
 }
 
 tm_status trellis_moe_forward_logits(tm_layer* layer, const uint16_t* x, const float* logits, int32_t T,
@@ -335,18 +501,14 @@ tm_status trellis_moe_forward_logits(tm_layer* layer, const uint16_t* x, const f
   if (check_mode(mode) != TM_OK) return TM_EINVAL;
   if (T == 0) return TM_OK;
   if (!x || !logits || !out) return fail(TM_EINVAL, "x, logits and out must be non-NULL");
+  if (((uintptr_t)x) % 8 || ((uintptr_t)out) % 16) return fail(TM_EINVAL, "x must be 8-byte and out 16-byte aligned");
   Layout L;
   tm_status s = check_ws(layer, T, workspace, workspace_bytes, &L);
   if (s != TM_OK) return s;
   cudaStream_t st = (cudaStream_t)stream;
-  int32_t* ids = at<int32_t>(workspace, L, Layout::IDS);
-  float* w = at<float>(workspace, L, Layout::W);
   cudaError_t e;
   if ((e = stage_mark(layer, 0, st)) != cudaSuccess) return cuda_fail(e, "stage event");
-  e = tmoe::launch_route_topk(logits, T, layer->desc.E, layer->desc.topk, ids, w, st);
-  if (e != cudaSuccess) return cuda_fail(e, "router");
-  if ((e = stage_mark(layer, 1, st)) != cudaSuccess) return cuda_fail(e, "stage event");
-  return run_layer(layer, x, ids, w, T, mode, out, workspace, L, st);
+  return run_layer(layer, x, nullptr, nullptr, logits, T, mode, out, workspace, L, st);
 }
 
 tm_status trellis_moe_forward_host(tm_layer* layer, const uint16_t* x_host, const float* logits_host, int32_t T,
@@ -371,12 +533,8 @@ tm_status trellis_moe_forward_host(tm_layer* layer, const uint16_t* x_host, cons
     return cuda_fail(e, "copy x to device");
   if ((e = cudaMemcpyAsync(dl, logits_host, (size_t)T * d.E * 4, cudaMemcpyHostToDevice, st)) != cudaSuccess)
     return cuda_fail(e, "copy logits to device");
-  int32_t* ids = at<int32_t>(workspace, L, Layout::IDS);
-  float* w = at<float>(workspace, L, Layout::W);
   if ((e = stage_mark(layer, 0, st)) != cudaSuccess) return cuda_fail(e, "stage event");
-  if ((e = tmoe::launch_route_topk(dl, T, d.E, d.topk, ids, w, st)) != cudaSuccess) return cuda_fail(e, "router");
-  if ((e = stage_mark(layer, 1, st)) != cudaSuccess) return cuda_fail(e, "stage event");
-  s = run_layer(layer, dx, ids, w, T, mode, dout, workspace, L, st);
+  s = run_layer(layer, dx, nullptr, nullptr, dl, T, mode, dout, workspace, L, st);
   if (s != TM_OK) return s;
   if ((e = cudaMemcpyAsync(out_host, dout, (size_t)T * d.H * 4, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
     return cuda_fail(e, "copy out to host");

@@ -99,15 +99,91 @@ __device__ __forceinline__ void run_load_k4(const uint16_t* __restrict__ tile, i
 }
 
 // States of a K = 4 run: with V = prev:cur (as stream-order 64 bits), state i
-// sits at V >> (28 - 4i). Pairs (i, i+4) come out of one funnel shift.
+// sits at V >> (28 - 4i). Only the high word of prev and both words of cur
+// are needed: A = (prev.hi << 16) | cur.lo holds stream bits 16..47 of V, and
+// the 32-bit window at shift n of A:cur (n >= 16, so cur.lo is shifted out)
+// holds states m (high half) and m+4 (low half) for n = 28 - 4m.
 __device__ __forceinline__ void run_states_k4(uint32_t prev_raw, uint32_t cur_raw, uint32_t (&s)[8]) {
-  const uint32_t P = swap_words(prev_raw);
-  const uint32_t C = swap_words(cur_raw);
+  const uint32_t A = __byte_perm(prev_raw, cur_raw, 0x3254);
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
-    const uint32_t q = (m == 3) ? C : __funnelshift_r(C, P, 12 - 4 * m);
+    const uint32_t q = __funnelshift_r(cur_raw, A, 28 - 4 * m);
     s[m] = q >> 16;
     s[m + 4] = q & 0xFFFFu;
+  }
+}
+
+// Raw codebook words y[i] = mcg_raw(state i) of a K = 4 run, with the state
+// split done by the integer multiply unit instead of the ALU:
+// for a window q = [s_hi : s_lo], s_hi = umulhi(q, 2^16), x_hi = s_hi * M and
+// x_lo = q * M - x_hi * 2^16 = s_lo * M (mod 2^32). `k16` must be 65536 and
+// `nk16` 0xFFFF0000, passed at run time so they stay multiplies.
+__device__ __forceinline__ void run_mcg_k4(uint32_t prev_raw, uint32_t cur_raw, uint32_t k16, uint32_t nk16,
+                                           uint32_t (&y)[8]) {
+  const uint32_t A = __byte_perm(prev_raw, cur_raw, 0x3254);
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const uint32_t q = __funnelshift_r(cur_raw, A, 28 - 4 * m);
+    const uint32_t sh = __umulhi(q, k16);
+    const uint32_t xh = sh * kMcgMult;
+    const uint32_t xl = q * kMcgMult + xh * nk16;
+    y[m] = (xh & kMcgMask) ^ kMcgXor;
+    y[m + 4] = (xl & kMcgMask) ^ kMcgXor;
+  }
+}
+
+// Weights from raw codebook words: fp16 pairs (w0,w1) .. (w6,w7).
+__device__ __forceinline__ void raw_to_f16(const uint32_t (&y)[8], uint32_t (&w)[4]) {
+#pragma unroll
+  for (int p = 0; p < 4; ++p) w[p] = cb_pair_from_raw(y[2 * p], y[2 * p + 1]);
+}
+
+// fp16x2 -> two E4M3 bytes with the native conversion instruction.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(uint32_t h2) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h2));
+  return r;
+}
+
+// E4M3 bytes from raw codebook words: (w0..w3), (w4..w7). Each weight is the
+// fp16 sum of its word's halves (one fp16 add with half selectors), paired
+// and converted two at a time.
+__device__ __forceinline__ void raw_to_e4m3(const uint32_t (&y)[8], uint32_t (&q)[2]) {
+  __half hw[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __half2 v = *reinterpret_cast<const __half2*>(&y[i]);
+    hw[i] = __hadd(__low2half(v), __high2half(v));
+  }
+  uint32_t c[4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    __half2 t = __halves2half2(hw[2 * p], hw[2 * p + 1]);
+    c[p] = cvt_e4m3x2(*reinterpret_cast<uint32_t*>(&t));
+  }
+  q[0] = __byte_perm(c[0], c[1], 0x5410);
+  q[1] = __byte_perm(c[2], c[3], 0x5410);
+}
+
+// Two E4M3 bytes (low byte first) -> fp16x2, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t b2) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)b2));
+  return r;
+}
+
+// W4A8 weights for the fp16 tensor path: each weight is the E4M3 rounding of
+// its fp16 codebook value, returned as the (exactly representable) fp16 value;
+// pairs (w0,w1) .. (w6,w7). Products of such weights with E4M3 activations
+// held in fp16 are exact, so an fp16 MMA with fp32 accumulation computes the
+// same sums as an E4M3 MMA (up to summation order).
+__device__ __forceinline__ void raw_to_e4m3_f16(const uint32_t (&y)[8], uint32_t (&w)[4]) {
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const __half2 va = *reinterpret_cast<const __half2*>(&y[2 * p]);
+    const __half2 vb = *reinterpret_cast<const __half2*>(&y[2 * p + 1]);
+    __half2 t = __halves2half2(__hadd(__low2half(va), __high2half(va)), __hadd(__low2half(vb), __high2half(vb)));
+    w[p] = e4m3x2_to_f16x2(cvt_e4m3x2(*reinterpret_cast<uint32_t*>(&t)));
   }
 }
 
@@ -124,8 +200,8 @@ __device__ __forceinline__ void run_weights_f16(const uint32_t (&s)[8], uint32_t
 __device__ __forceinline__ void run_weights_e4m3(const uint32_t (&s)[8], uint32_t (&q)[2]) {
   uint32_t w[4];
   run_weights_f16(s, w);
-  q[0] = e4m3x2_from_half2(w[0]) | (e4m3x2_from_half2(w[1]) << 16);
-  q[1] = e4m3x2_from_half2(w[2]) | (e4m3x2_from_half2(w[3]) << 16);
+  q[0] = __byte_perm(cvt_e4m3x2(w[0]), cvt_e4m3x2(w[1]), 0x5410);
+  q[1] = __byte_perm(cvt_e4m3x2(w[2]), cvt_e4m3x2(w[3]), 0x5410);
 }
 
 // ---------------------------------------------------------------------------

@@ -45,6 +45,46 @@ struct FcArgs {
   int atomic;
 };
 
+// Decode-rows path (few tokens): one fused prologue, then FC1 and FC2 as
+// split-K kernels whose last-arriving CTA per unit finishes the epilogue.
+struct DecPrologueArgs {
+  const float* logits;      // router logits [T, E], or nullptr when ids are given
+  int32_t* ids_out;         // router outputs (when logits != nullptr)
+  float* w_out;
+  RouteMapArgs rm;          // rm.ids = given ids or ids_out
+  const uint16_t* x;        // bf16 [T, H]
+  const uint16_t* suh;      // fp16 [H]
+  int T, H, topk, rot_b, w4a8;
+  void* xq;                 // fp16 or E4M3 [T, H]
+  uint8_t* xs;              // E8M0 [T, H/32]
+  int32_t* zero_i32;        // counters to clear
+  int n_zero_i32;
+  float* out;               // [T, H], cleared here (tokens without a valid route stay 0)
+  long out_n;
+};
+
+struct DecArgs {
+  FcArgs f;
+  int ksplit;               // S: CTAs along the contraction axis per unit part
+  int kchunk;               // columns per split (multiple of 64)
+  int parts;                // 128-row CTAs per epilogue unit (FC1: 2*BI/128, FC2: 1)
+  int units_m;              // epilogue units per route block (FC1: I/BI, FC2: H/128)
+  int bi;                   // FC1 half-row block (64 or 128)
+  float* partial;           // [max_blocks*units_m][S][unit_rows][8] fp32
+  int32_t* unit_cnt;        // [max_blocks*units_m] arrival counters
+  int32_t* tok_cnt;         // FC2: [T][units_m] completion counters
+  const int32_t* slot_of_route;
+  const float* route_w;     // [T*topk]
+  float* out;               // FC2: final output [T, H]
+  int T;
+};
+
+cudaError_t launch_dec_prologue(const DecPrologueArgs& a, cudaStream_t st);
+cudaError_t launch_dec_fc(const DecArgs& d, int proj, bool w4a8, int uniform_k, int max_blocks, cudaStream_t st);
+// Split-K factor the decode path uses for a contraction of `kdim` columns when
+// `units` 128-row CTAs per split exist (also sizes the workspace).
+int dec_ksplit(int kdim, long units);
+
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t st);
 cudaError_t launch_route_map(const RouteMapArgs& a, cudaStream_t st);
 int route_map_tiles(int R);

@@ -1,0 +1,54 @@
+// Device body of the fused rotate + quantize step, shared by the stand-alone
+// kernel (rotate.cu) and the fused decode prologue (dec.cu).
+#pragma once
+
+#include "launch.h"
+
+namespace tmoe {
+
+// One warp per (token, 128-wide chunk of H); lane l holds entries 4l..4l+3.
+template <bool W4A8>
+static __device__ __forceinline__ void rotate_quant_warp(const uint16_t* __restrict__ x,
+                                                         const uint16_t* __restrict__ suh, int T, int H, int rot_b,
+                                                         void* __restrict__ xq, uint8_t* __restrict__ xs, int gw) {
+  const int lane = threadIdx.x & 31;
+  const int chunks = H >> 7;
+  if (gw >= T * chunks) return;
+  const int t = gw / chunks, c = gw % chunks;
+  const size_t base = (size_t)t * H + (size_t)c * 128 + 4 * lane;
+  const uint2 xr = __ldg(reinterpret_cast<const uint2*>(x + base));
+  const uint2 sr = __ldg(reinterpret_cast<const uint2*>(suh + (size_t)c * 128 + 4 * lane));
+  float v[4];
+  const uint32_t xw[2] = {xr.x, xr.y};
+  const uint32_t sw[2] = {sr.x, sr.y};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t xb = (xw[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
+    const uint32_t sb = (sw[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
+    v[i] = __uint_as_float(xb << 16) * __half2float(__ushort_as_half((unsigned short)sb));
+  }
+  warp_fwht<4>(v, rot_b);
+  const float sc = hadamard_scale(rot_b);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] *= sc;
+  if (!W4A8) {
+    __half2 a = __floats2half2_rn(v[0], v[1]);
+    __half2 b = __floats2half2_rn(v[2], v[3]);
+    uint2 o;
+    o.x = *reinterpret_cast<uint32_t*>(&a);
+    o.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(xq) + base) = o;
+  } else {
+    // 32-element block = 8 lanes
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const int e = e8m0_exponent(amax);
+    const float inv = exp2_int(-e);
+    const uint32_t q = e4m3x2_from_float2(v[0] * inv, v[1] * inv) | (e4m3x2_from_float2(v[2] * inv, v[3] * inv) << 16);
+    *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(xq) + base) = q;
+    if ((lane & 7) == 0) xs[(size_t)t * (H >> 5) + (size_t)c * 4 + (lane >> 3)] = (uint8_t)(e + 127);
+  }
+}
+
+}  // namespace tmoe
