@@ -252,7 +252,8 @@ def run_ours(args, rank, world):
     else:
         flops = 2 * R * 2 * cfg.I * cfg.H
         achieved = flops / (stages_us["fc1"] * 1e-6) / 1e12
-        roof = {"bound": "tensor", "kernel": "k_fc<W4A16,FC1>", "achieved": round(achieved, 2),
+        kname = "k_tc_fc<FC1> (tcgen05, doubled-K fp16)" if mode == "w4a16" else "k_fc<W4A8,FC1> (mma.sync)"
+        roof = {"bound": "tensor", "kernel": kname, "achieved": round(achieved, 2),
                 "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4),
                 "traffic": None, "peak_source": pk["source"] + " (bf16 dense burst; fp16 runs at the bf16 rate)",
                 "flops_per_launch": flops}
@@ -281,7 +282,7 @@ def run_ours(args, rank, world):
            "steps": e2e_steps, "api": "trellis_moe_forward_host"}
 
     decode_path = R <= 1024 and R < 4 * cfg.E   # the library's decode-rows path (3 kernels)
-    launches_per_step = 3 if decode_path else 6 + (2 if R > 1024 else 0)
+    launches_per_step = 3 if decode_path else 6 + (2 if R > 1024 else 0)  # router, route map (1 or 3), rotate, FC1, FC2, combine
     res = {
         "metric": METRIC, "value": round(args.steps * T * world / (total_ms / 1e3), 2), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,

@@ -53,6 +53,7 @@ cudaError_t stage_mark(const tm_layer* layer, int i, cudaStream_t st) {
 constexpr size_t kAlign = 256;
 constexpr int kBnMax = 64;
 constexpr int kBnMin = 8;
+constexpr int kBlockMax = 256;  // largest route block (tcgen05 path): expert segments pad to it
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -109,9 +110,9 @@ struct Layout {
 Layout make_layout(const tm_layer_desc& d, int T) {
   Layout L;
   const size_t R = (size_t)T * d.topk;
-  const size_t slots = R + (size_t)d.E * (kBnMax - 1);
+  const size_t slots = R + (size_t)d.E * (kBlockMax - 1);
   const size_t ntiles = (R + 1023) / 1024;
-  L.bytes[Layout::XQ] = (size_t)T * d.H * 2;
+  L.bytes[Layout::XQ] = slots * d.H * 2;  // fp16 in slot order (tcgen05 path), else [T][H] fp16 or E4M3
   L.bytes[Layout::XS] = (size_t)T * (d.H / 32);
   L.bytes[Layout::ZQ] = slots * d.I * 2;
   L.bytes[Layout::ZS] = slots * (d.I / 32);
@@ -183,7 +184,10 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
   const tm_layer_desc& d = layer->desc;
   const bool w4a8 = (mode == TM_MODE_W4A8) || (mode == TM_MODE_AUTO && T <= d.decode_max_rows);
   const int R = T * d.topk;
-  const int bn = choose_bn(d, T);
+  // W4A16 outside the decode regime runs on the tcgen05 kernels (route blocks
+  // of up to 256 routes); W4A8 there keeps the mma.sync kernels.
+  const bool use_tc = !w4a8 && tmoe::tc_supported(d.H, d.I, layer->bi, d.rot_block_h, d.rot_block_i);
+  const int bn = use_tc ? tmoe::tc_route_block() : choose_bn(d, T);
   cudaError_t e;
   uint32_t* err = at<uint32_t>(ws, L, Layout::ERR);
   if (logits) {
@@ -219,7 +223,9 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
 
   void* xq = at<void>(ws, L, Layout::XQ);
   uint8_t* xs = at<uint8_t>(ws, L, Layout::XS);
-  if ((e = tmoe::launch_rotate_quant(x, d.in_suh, T, d.H, d.rot_block_h, w4a8, xq, xs, st)) != cudaSuccess)
+  // the tcgen05 path reads x~ in slot order (one copy per route)
+  if ((e = tmoe::launch_rotate_quant(x, d.in_suh, T, d.H, d.rot_block_h, w4a8, xq, xs, st,
+                                     use_tc ? rm.slot_of_route : nullptr, d.topk)) != cudaSuccess)
     return cuda_fail(e, "rotate+quantize");
   if ((e = stage_mark(layer, 3, st)) != cudaSuccess) return cuda_fail(e, "stage event");
 
@@ -239,8 +245,16 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
   a1.nblocks = rm.nblocks;
   a1.out_act = at<void>(ws, L, Layout::ZQ);
   a1.out_scale = at<uint8_t>(ws, L, Layout::ZS);
-  if ((e = tmoe::launch_fc1(a1, w4a8, layer->bi, bn, layer->uniform_k, max_blocks, st)) != cudaSuccess)
-    return cuda_fail(e, "FC1");
+  tmoe::TcArgs t1{};
+  t1.f = a1;
+  t1.bi = layer->bi;
+  t1.err = err;
+  t1.act_rows = (int)(R + (size_t)d.E * (kBlockMax - 1));  // slots
+  if (use_tc)
+    e = tmoe::launch_tc_fc(t1, 1, layer->uniform_k, max_blocks, st);
+  else
+    e = tmoe::launch_fc1(a1, w4a8, layer->bi, bn, layer->uniform_k, max_blocks, st);
+  if (e != cudaSuccess) return cuda_fail(e, "FC1");
   if ((e = stage_mark(layer, 4, st)) != cudaSuccess) return cuda_fail(e, "stage event");
 
   tmoe::FcArgs a2 = a1;
@@ -261,7 +275,16 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
   } else {
     a2.out_f32 = at<float>(ws, L, Layout::ROWS);
   }
-  if ((e = tmoe::launch_fc2(a2, w4a8, bn, layer->uniform_k, max_blocks, st)) != cudaSuccess) return cuda_fail(e, "FC2");
+  tmoe::TcArgs t2{};
+  t2.f = a2;
+  t2.bi = layer->bi;
+  t2.err = err;
+  t2.act_rows = (int)(R + (size_t)d.E * (kBlockMax - 1));  // slots
+  if (use_tc)
+    e = tmoe::launch_tc_fc(t2, 2, layer->uniform_k, max_blocks, st);
+  else
+    e = tmoe::launch_fc2(a2, w4a8, bn, layer->uniform_k, max_blocks, st);
+  if (e != cudaSuccess) return cuda_fail(e, "FC2");
   if ((e = stage_mark(layer, 5, st)) != cudaSuccess) return cuda_fail(e, "stage event");
   if (!a2.atomic) {
     if ((e = tmoe::launch_combine(a2.out_f32, rm.slot_of_route, w, T, d.H, d.topk, out, st)) != cudaSuccess)

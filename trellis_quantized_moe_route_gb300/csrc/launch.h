@@ -1,6 +1,7 @@
 // Internal kernel launchers of the trellis-MoE library.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -85,12 +86,27 @@ cudaError_t launch_dec_fc(const DecArgs& d, int proj, bool w4a8, int uniform_k, 
 // `units` 128-row CTAs per split exist (also sizes the workspace).
 int dec_ksplit(int kdim, long units);
 
+// Prefill path on tcgen05 (W4A16): x~ [slots][H] and z~ [slots][I] fp16 in
+// slot order, route blocks of tc_route_block() slots.
+struct TcArgs {
+  FcArgs f;
+  int bi;          // FC1 half-row block (64 or 128)
+  uint32_t* err;   // device error word (bit 1: a pipeline wait gave up)
+  int act_rows;    // rows of the activation operand, in slot order: slots
+  CUtensorMap amap;  // filled by launch_tc_fc: the activations as [act_rows][K] fp16, box 64 x 128, 128-byte swizzle
+};
+cudaError_t launch_tc_fc(const TcArgs& args, int proj, int uniform_k, int max_blocks, cudaStream_t st);
+int tc_route_block();
+// Geometry the tcgen05 kernels handle (H, I, FC1 half-row block, rotation blocks).
+bool tc_supported(int H, int I, int bi, int rot_h, int rot_i);
+
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t st);
 cudaError_t launch_route_map(const RouteMapArgs& a, cudaStream_t st);
 int route_map_tiles(int R);
 
 cudaError_t launch_rotate_quant(const uint16_t* x, const uint16_t* suh, int T, int H, int rot_b, bool w4a8,
-                                void* xq, uint8_t* xs, cudaStream_t st);
+                                void* xq, uint8_t* xs, cudaStream_t st, const int32_t* slot_of_route = nullptr,
+                                int topk = 0);
 
 // FC kernels. `bn` is the route block (8 or 64), `bi` the FC1 half-row block
 // (64 or 128), `uniform_k` the trellis K of every expert or 0 when mixed.

@@ -9,19 +9,21 @@ namespace tmoe {
 template <bool W4A8>
 __global__ void __launch_bounds__(256) k_rotate_quant(const uint16_t* __restrict__ x, const uint16_t* __restrict__ suh,
                                                       int T, int H, int rot_b, void* __restrict__ xq,
-                                                      uint8_t* __restrict__ xs) {
-  rotate_quant_warp<W4A8>(x, suh, T, H, rot_b, xq, xs, (blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+                                                      uint8_t* __restrict__ xs, const int32_t* __restrict__ slot_of_route,
+                                                      int topk) {
+  rotate_quant_warp<W4A8>(x, suh, T, H, rot_b, xq, xs, (blockIdx.x * blockDim.x + threadIdx.x) >> 5, slot_of_route,
+                          topk);
 }
 
 cudaError_t launch_rotate_quant(const uint16_t* x, const uint16_t* suh, int T, int H, int rot_b, bool w4a8,
-                                void* xq, uint8_t* xs, cudaStream_t st) {
+                                void* xq, uint8_t* xs, cudaStream_t st, const int32_t* slot_of_route, int topk) {
   if (T == 0) return cudaSuccess;
   const long warps = (long)T * (H / 128);
   const int blocks = (int)((warps * 32 + 255) / 256);
   if (w4a8)
-    k_rotate_quant<true><<<blocks, 256, 0, st>>>(x, suh, T, H, rot_b, xq, xs);
+    k_rotate_quant<true><<<blocks, 256, 0, st>>>(x, suh, T, H, rot_b, xq, xs, nullptr, 0);
   else
-    k_rotate_quant<false><<<blocks, 256, 0, st>>>(x, suh, T, H, rot_b, xq, xs);
+    k_rotate_quant<false><<<blocks, 256, 0, st>>>(x, suh, T, H, rot_b, xq, xs, slot_of_route, topk);
   return cudaGetLastError();
 }
 

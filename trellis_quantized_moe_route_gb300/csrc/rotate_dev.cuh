@@ -7,10 +7,14 @@
 namespace tmoe {
 
 // One warp per (token, 128-wide chunk of H); lane l holds entries 4l..4l+3.
+// With `slot_of_route` (fp16 only) the rotated row is stored once per route of
+// the token, at the route's slot: x~ in slot order, [slots][H].
 template <bool W4A8>
 static __device__ __forceinline__ void rotate_quant_warp(const uint16_t* __restrict__ x,
                                                          const uint16_t* __restrict__ suh, int T, int H, int rot_b,
-                                                         void* __restrict__ xq, uint8_t* __restrict__ xs, int gw) {
+                                                         void* __restrict__ xq, uint8_t* __restrict__ xs, int gw,
+                                                         const int32_t* __restrict__ slot_of_route = nullptr,
+                                                         int topk = 0) {
   const int lane = threadIdx.x & 31;
   const int chunks = H >> 7;
   if (gw >= T * chunks) return;
@@ -37,7 +41,15 @@ static __device__ __forceinline__ void rotate_quant_warp(const uint16_t* __restr
     uint2 o;
     o.x = *reinterpret_cast<uint32_t*>(&a);
     o.y = *reinterpret_cast<uint32_t*>(&b);
-    *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(xq) + base) = o;
+    if (slot_of_route == nullptr) {
+      *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(xq) + base) = o;
+    } else {
+      for (int k = 0; k < topk; ++k) {
+        const int slot = slot_of_route[(size_t)t * topk + k];
+        if (slot >= 0)
+          *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(xq) + (size_t)slot * H + (size_t)c * 128 + 4 * lane) = o;
+      }
+    }
   } else {
     // 32-element block = 8 lanes
     float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));

@@ -1,0 +1,712 @@
+// Prefill contraction on the 5th-generation tensor cores (sm_103a, W4A16).
+//
+// A persistent, warp-specialised kernel; one CTA per SM walks work units
+// (route block rb of up to 256 routes of one expert) x (block mb of N weight
+// rows: FC1 takes bi gate rows and the bi matching up rows, N = 2 bi; FC2
+// takes N output columns). The contraction runs in stages of 64 columns:
+//
+//   warp 12     (payload)   streams the stage's trellis payload (4 tiles per
+//                           tile row) into a 4-deep ring with bulk copies;
+//   warp 13     (activation) one thread loads a stage's activation rows (slot
+//                           order, one 128-row box per accumulator) into a
+//                           128-byte swizzled operand with TMA;
+//   warps 0-7   (expanders) decode the stage's N x 64 weights from the payload
+//                           into a second swizzled operand, each codebook value
+//                           the fp16 sum of its word's two halves as the
+//                           codebook defines it;
+//   warp 14     (issuer)    one thread issues tcgen05.mma with the routes as M
+//                           (one or two accumulators of 128 routes) and the
+//                           weight rows as N, and commits each stage to the
+//                           mbarriers that free its operand slots;
+//   warps 8-11  (epilogue)  one TMEM lane (route) per thread, so the block
+//                           Hadamard transforms run inside a thread's registers
+//                           (FC1: H -> svh -> SiLU(gate)*up -> suh_down -> H, as
+//                           in sparkinfer PR #90 "moe: integrate EXL3 Trellis
+//                           into the fused W4A16 API", review of kernel.py;
+//                           FC2: scale, H, down_svh).
+//
+// Tensor memory holds two 256-column accumulator buffers: a unit of up to 128
+// routes takes one (alternating), a unit of up to 256 routes takes both, so
+// the epilogue of one unit overlaps the contraction of the next. Every
+// hand-off is an mbarrier (full/empty rings of 3 activation, 2 decoded and 4
+// payload stages, full/empty per accumulator buffer); no role waits on a
+// block-wide barrier. Waits are bounded in wall time; on a timeout the CTA
+// raises the error word, drains its copies and MMAs and releases its tensor
+// memory.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "launch.h"
+#include "tc.cuh"
+
+namespace tmoe {
+
+constexpr int kTcThreads = 512;        // warpgroups: 2 expander, 1 epilogue, 1 loader/issuer
+// Registers per thread after the split (sum x 128 threads = 512 x 128, the
+// launch budget: the kernel must be compiled at 128 registers, which the
+// launcher checks, or setmaxnreg.inc could wait for registers never freed).
+constexpr int kRegExp = 112, kRegEpi = 232, kRegAux = 56, kRegLaunch = 128;
+static_assert(128 * (2 * kRegExp + kRegEpi + kRegAux) <= kTcThreads * kRegLaunch, "register split over budget");
+constexpr int kTcExp = 256;            // expander threads
+constexpr int kTcEpiWarps = 4;
+constexpr int kEvecBytes = 2048;       // per epilogue warp: the unit's folded scale / sign vectors (fp32)
+constexpr int kTcBN = 256;             // routes per route block
+constexpr int kTcKS = 64;              // contraction columns per stage
+constexpr int kSA = 3, kSB = 2, kSW = 4;
+constexpr int kABytes = 256 * 128;     // activation operand: 256 routes x 128 bytes
+constexpr int kBBytes = 256 * 128;     // decoded operand: 256 weight rows x 128 bytes
+constexpr uint64_t kTcWaitNs = 2000000000ull;
+
+// Payload of one stage: 16 tile rows x 4 tiles of 32K bytes.
+__host__ __device__ inline int tc_wslot_bytes(int kmax) { return 16 * 4 * 32 * kmax; }
+// Dynamic shared memory: activation ring, decoded ring, payload ring, the
+// epilogue warps' vectors (plus 1024 bytes to align the base).
+__host__ __device__ inline int tc_smem_total(int kmax) {
+  return 1024 + kSA * kABytes + kSB * kBBytes + kSW * tc_wslot_bytes(kmax) + kTcEpiWarps * kEvecBytes;
+}
+
+struct TcBars {
+  uint64_t fullA[kSA], emptyA[kSA], fullB[kSB], emptyB[kSB], fullW[kSW], emptyW[kSW], accFull[2], accEmpty[2];
+};
+
+// Work unit geometry shared by every role.
+template <int PROJ, int NR>
+struct TcGeom {
+  int mblocks, kdim, nst, tiles_k, bi;
+  __device__ __forceinline__ explicit TcGeom(const TcArgs& args) {
+    const FcArgs& a = args.f;
+    bi = (PROJ == 1) ? NR / 2 : 0;
+    mblocks = (PROJ == 1) ? a.I / bi : a.H / NR;
+    kdim = (PROJ == 1) ? a.H : a.I;
+    nst = kdim / kTcKS;
+    tiles_k = kdim >> 4;
+  }
+  // first weight row of tile row tr of block mb
+  __device__ __forceinline__ int tile_row0(const FcArgs& a, int mb, int tr) const {
+    if (PROJ == 1) {
+      const int m = 16 * tr;
+      return (m < bi) ? mb * bi + m : a.I + mb * bi + (m - bi);
+    }
+    return mb * NR + 16 * tr;
+  }
+};
+
+// Window of a run for any K from a tile in shared memory (see run_window_generic).
+template <int K>
+__device__ __forceinline__ void run_window_smem(const uint16_t* tile, int j0, uint32_t& hi, uint32_t& lo, int& off) {
+  constexpr int NB = 256 * K;
+  constexpr int NW = 16 * K;
+  int q0 = (j0 + 1) * K - 16;
+  if (q0 < 0) q0 += NB;
+  const int w = q0 >> 4;
+  off = q0 & 15;
+  const uint32_t w0 = tile[w], w1 = tile[(w + 1) % NW], w2 = tile[(w + 2) % NW], w3 = tile[(w + 3) % NW];
+  hi = (w0 << 16) | w1;
+  lo = (w2 << 16) | w3;
+}
+
+__device__ __forceinline__ void sts128(unsigned char* p, const uint32_t (&w)[4]) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Expand one stage: NR weight rows x 64 columns from the payload slot `wsl`
+// (tile row tr of the stage at tr * 4 * 32K bytes, its 4 tiles contiguous)
+// into the swizzled operand `bsl`. Thread t takes row t % NR and 8 * NR / 256
+// of the row's 8 chunks of 8 columns; chunk c of a row is run (tile c / 2,
+// half c % 2) of the row's trellis tiles.
+template <int NR, int K>
+__device__ __forceinline__ void tc_expand_stage(const unsigned char* wsl, unsigned char* bsl, int tid,
+                                                uint32_t k16, uint32_t nk16) {
+  constexpr int CPT = 8 * NR / 256;
+  const int n = tid % NR;
+  const int c0 = (tid / NR) * CPT;
+  const int rr = n & 15;
+  const unsigned char* trow = wsl + (n >> 4) * 4 * 32 * K;
+  unsigned char* brow = bsl + (n >> 3) * 1024 + (n & 7) * 128;
+  const uint32_t sw = (uint32_t)(n & 7);
+  if (K == 4) {
+    // A K=4 tile row rr is the 32-bit words 2rr (first 8 weights) and 2rr+1;
+    // a run also needs the word before it, which for the first half is the
+    // previous row's second word (row 15's for row 0), held by lane-1 (lane+15).
+    const int lane = tid & 31;
+    const int src = (lane & 16) | ((lane + 15) & 15);
+#pragma unroll
+    for (int tt = 0; tt < CPT / 2; ++tt) {
+      const int t = c0 / 2 + tt;
+      const uint2 cw = *reinterpret_cast<const uint2*>(trow + t * 128 + 8 * rr);
+      const uint32_t pw = __shfl_sync(0xFFFFFFFFu, cw.y, src);
+      uint32_t y[8], w[4];
+      run_mcg_k4(pw, cw.x, k16, nk16, y);
+      raw_to_f16(y, w);
+      sts128(brow + (((uint32_t)(2 * t) ^ sw) << 4), w);
+      run_mcg_k4(cw.x, cw.y, k16, nk16, y);
+      raw_to_f16(y, w);
+      sts128(brow + (((uint32_t)(2 * t + 1) ^ sw) << 4), w);
+    }
+  } else {
+#pragma unroll
+    for (int cc = 0; cc < CPT; ++cc) {
+      const int c = c0 + cc;
+      uint32_t hi, lo, s8[8], y[8], w[4];
+      int off;
+      run_window_smem<K>(reinterpret_cast<const uint16_t*>(trow + (c >> 1) * 32 * K), 16 * rr + 8 * (c & 1), hi, lo,
+                         off);
+      run_states_generic<K>(hi, lo, off, s8);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) y[q] = mcg_raw(s8[q]);
+      raw_to_f16(y, w);
+      sts128(brow + (((uint32_t)c ^ sw) << 4), w);
+    }
+  }
+}
+
+// Bounded wait used while draining after an abort (ignores the abort flag).
+__device__ __forceinline__ void mbar_wait_drain(uint64_t* mbar, uint32_t parity) {
+  const uint32_t a = smem_u32(mbar);
+  const uint64_t t0 = global_ns();
+  while (!mbar_try(a, parity) && global_ns() - t0 < kTcWaitNs / 4) {
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Epilogues: the calling thread owns one route (one TMEM lane) and the unit's
+// N accumulator columns. All TMEM accesses are warp-collective; only threads
+// of valid routes store.
+// ---------------------------------------------------------------------------
+// L (a multiple of 32) accumulator columns of this thread's TMEM lane into
+// column pairs (warp-collective): every load in flight before the one wait.
+template <int L>
+__device__ __forceinline__ void ld_cols2(uint32_t taddr, float2 (&w)[L / 2]) {
+  uint32_t r[L / 32][32];
+#pragma unroll
+  for (int j = 0; j < L / 32; ++j) tmem_ld32(taddr + 32 * j, r[j]);
+  tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < L / 32; ++j) {
+    reg_fence32(r[j]);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[16 * j + i] = make_float2(__uint_as_float(r[j][2 * i]), __uint_as_float(r[j][2 * i + 1]));
+  }
+}
+template <int L>
+__device__ __forceinline__ void st_cols2(uint32_t taddr, const float2 (&w)[L / 2]) {
+#pragma unroll
+  for (int j = 0; j < L / 32; ++j) {
+    uint32_t r[32];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      r[2 * i] = __float_as_uint(w[16 * j + i].x);
+      r[2 * i + 1] = __float_as_uint(w[16 * j + i].y);
+    }
+    tmem_st32(taddr + 32 * j, r);
+  }
+  tmem_st_wait();
+}
+
+// Block FWHT (blocks of B <= L, natural order, unnormalised) on L values held
+// as pairs: the distance-1 level inside each pair, every wider level on whole
+// pairs with packed fp32 adds.
+template <int L>
+__device__ __forceinline__ void fwht2(float2 (&w)[L / 2], int B) {
+  if (B > 1) {
+#pragma unroll
+    for (int j = 0; j < L / 2; ++j) w[j] = make_float2(w[j].x + w[j].y, w[j].x - w[j].y);
+  }
+  const float2 m1 = make_float2(-1.0f, -1.0f);
+#pragma unroll
+  for (int h = 1; h < L / 2; h <<= 1) {  // pair distance h = element distance 2h
+    if (2 * h < B) {
+#pragma unroll
+      for (int j = 0; j < L / 2; ++j) {
+        if ((j & h) == 0) {
+          const float2 x = w[j], y = w[j + h];
+          w[j] = __fadd2_rn(x, y);
+          w[j + h] = __ffma2_rn(y, m1, x);
+        }
+      }
+    }
+  }
+}
+
+// w[j] *= f[j] for L fp32 factors in shared memory (16-byte aligned).
+template <int L>
+__device__ __forceinline__ void scale2(float2 (&w)[L / 2], const float* f) {
+#pragma unroll
+  for (int j = 0; j < L / 2; j += 2) {
+    const float4 q = *reinterpret_cast<const float4*>(f + 2 * j);
+    w[j] = __fmul2_rn(w[j], make_float2(q.x, q.y));
+    w[j + 1] = __fmul2_rn(w[j + 1], make_float2(q.z, q.w));
+  }
+}
+
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// SiLU(g) = g * sigmoid(g) = h * (1 + tanh(h)) with h = g / 2.
+__device__ __forceinline__ float2 silu2(float2 g) {
+  const float2 h = __fmul2_rn(g, make_float2(0.5f, 0.5f));
+  return __ffma2_rn(h, make_float2(tanh_fast(h.x), tanh_fast(h.y)), h);
+}
+
+// FC1 for the route of this thread (epilogue warps hold 232 registers):
+// gate -> scale, H, hs * svh, SiLU, parked in its TMEM columns; up -> scale,
+// H, hs * svh * suh_down, times SiLU(gate); H; hs; the z~ row of the slot
+// (fp16). ev (fp32, BI each): gate scale, hs * gate svh, up scale,
+// hs * up svh * down suh.
+template <int BI>
+__device__ __forceinline__ void tc_epi_fc1(const FcArgs& a, const float* ev, int mb, int slot, bool valid,
+                                           uint32_t taddr) {
+  const float hs = hadamard_scale(a.rot_b);
+  float2 w[BI / 2];
+  ld_cols2<BI>(taddr, w);
+  scale2<BI>(w, ev);
+  fwht2<BI>(w, a.rot_b);
+  scale2<BI>(w, ev + BI);
+#pragma unroll
+  for (int j = 0; j < BI / 2; ++j) w[j] = silu2(w[j]);
+  st_cols2<BI>(taddr, w);
+  ld_cols2<BI>(taddr + BI, w);
+  scale2<BI>(w, ev + 2 * BI);
+  fwht2<BI>(w, a.rot_b);
+  scale2<BI>(w, ev + 3 * BI);
+#pragma unroll
+  for (int c = 0; c < BI; c += 64) {
+    float2 g[32];
+    ld_cols2<64>(taddr + c, g);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) w[c / 2 + j] = __fmul2_rn(w[c / 2 + j], g[j]);
+  }
+  fwht2<BI>(w, a.rot_b);
+  if (valid) {
+    const float2 h2s = make_float2(hs, hs);
+    uint16_t* z = reinterpret_cast<uint16_t*>(a.out_act) + (size_t)slot * a.I + mb * BI;
+#pragma unroll
+    for (int j = 0; j < BI / 2; j += 4) {
+      uint32_t pk[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        __half2 h2 = __float22half2_rn(__fmul2_rn(w[j + i], h2s));
+        pk[i] = *reinterpret_cast<uint32_t*>(&h2);
+      }
+      *reinterpret_cast<uint4*>(z + 2 * j) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+  }
+}
+
+// FC2: per 128 output columns scale, rotate, hs * down_svh, then the fp32 row
+// of the slot (deterministic) or weighted atomics into the token's output row.
+// ev (fp32): NR output scales, then NR values hs * down_svh.
+template <int NR>
+__device__ __forceinline__ void tc_epi_fc2(const FcArgs& a, const float* ev, int mb, int slot, int route, bool valid,
+                                           uint32_t taddr) {
+  const float wr = (valid && a.atomic) ? a.route_w[route] : 0.0f;
+#pragma unroll 1
+  for (int h = 0; h < NR / 128; ++h) {
+    const int col0 = mb * NR + h * 128;
+    float2 w[64];
+    ld_cols2<128>(taddr + h * 128, w);
+    scale2<128>(w, ev + h * 128);
+    fwht2<128>(w, a.rot_b);
+    scale2<128>(w, ev + NR + h * 128);
+    if (!valid) continue;
+    if (!a.atomic) {
+      float* o = a.out_f32 + (size_t)slot * a.H + col0;
+#pragma unroll
+      for (int j = 0; j < 64; j += 2)
+        *reinterpret_cast<float4*>(o + 2 * j) = make_float4(w[j].x, w[j].y, w[j + 1].x, w[j + 1].y);
+    } else {
+      float* o = a.out_f32 + (size_t)(route / a.topk) * a.H + col0;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        atomicAdd(o + 2 * j, wr * w[j].x);
+        atomicAdd(o + 2 * j + 1, wr * w[j].y);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Roles. Every role walks the same unit sequence u = blockIdx.x, +gridDim.x, ...
+// and the same global stage counter g, so ring slots and phases agree.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int tc_macc(const FcArgs& a, int slot0) {
+  // valid routes are a prefix of the block: a second accumulator iff route 128 exists
+  return (a.route_of_slot[slot0 + 128] >= 0) ? 2 : 1;
+}
+
+// Accumulator buffers of a unit: one alternating buffer for <= 128 routes,
+// both (acc 0 in buffer 0, acc 1 in buffer 1) for more.
+struct TcAccPlan {
+  int nb = 0;          // buffer of the next one-accumulator unit
+  int uses[2] = {0, 0};
+  __device__ __forceinline__ int buf(int macc, int acc) const { return macc == 2 ? acc : nb; }
+  __device__ __forceinline__ void advance(int macc) { nb = (macc == 2) ? 0 : (nb ^ 1); }
+};
+
+template <int PROJ, int KB, int NR>
+__device__ __forceinline__ void tc_expanders(const TcArgs& args, const TcGeom<PROJ, NR>& G, int units, TcBars& B,
+                                             const unsigned char* wring, unsigned char* bring, volatile int* abort) {
+  const FcArgs& a = args.f;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const uint32_t k16 = 0x10000u + (uint32_t)((unsigned)G.nst >> 30), nk16 = 0u - k16;
+  const int wsz = tc_wslot_bytes(KB > 0 ? KB : 6);
+  int g = 0;
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int rb = u / G.mblocks;
+    const int K = (KB > 0) ? KB : a.bits[a.block_expert[rb]];
+    for (int s = 0; s < G.nst; ++s, ++g) {
+      const int ws = g % kSW, bs = g % kSB;
+      bool ok = mbar_wait_abort(&B.fullW[ws], (g / kSW) & 1, abort, kTcWaitNs);
+      if (ok && g >= kSB) ok = mbar_wait_abort(&B.emptyB[bs], ((g / kSB) - 1) & 1, abort, kTcWaitNs);
+      if (!__all_sync(0xFFFFFFFFu, ok)) return;
+      const unsigned char* wsl = wring + ws * wsz;
+      unsigned char* bsl = bring + bs * kBBytes;
+      if (KB > 0) {
+        tc_expand_stage<NR, (KB > 0 ? KB : 4)>(wsl, bsl, tid, k16, nk16);
+      } else {
+        switch (K) {
+          case 2: tc_expand_stage<NR, 2>(wsl, bsl, tid, k16, nk16); break;
+          case 3: tc_expand_stage<NR, 3>(wsl, bsl, tid, k16, nk16); break;
+          case 4: tc_expand_stage<NR, 4>(wsl, bsl, tid, k16, nk16); break;
+          case 5: tc_expand_stage<NR, 5>(wsl, bsl, tid, k16, nk16); break;
+          default: tc_expand_stage<NR, 6>(wsl, bsl, tid, k16, nk16); break;
+        }
+      }
+      fence_proxy_async();  // generic-proxy stores -> visible to the tensor core
+      __syncwarp();
+      if (lane == 0) {      // one arrival per warp
+        mbar_arrive(&B.fullB[bs]);
+        mbar_arrive(&B.emptyW[ws]);
+      }
+    }
+  }
+}
+
+template <int PROJ, int KB, int NR>
+__device__ __forceinline__ void tc_epilogue(const TcArgs& args, const TcGeom<PROJ, NR>& G, int units, TcBars& B,
+                                            float* ev, uint32_t tmem, volatile int* abort) {
+  const FcArgs& a = args.f;
+  const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;  // TMEM lane quarter of this warp
+  TcAccPlan plan;
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int rb = u / G.mblocks, mb = u - rb * G.mblocks;
+    const int e = a.block_expert[rb];
+    const int slot0 = rb * kTcBN;
+    const int macc = tc_macc(a, slot0);
+    // this warp's copy of the unit's vectors, converted to fp32 and folded
+    // (its reads of the last unit are done)
+    __syncwarp();
+    {
+      const float hs = hadamard_scale(a.rot_b);
+      if (PROJ == 1) {
+        const int bi = NR / 2, c0 = mb * bi;
+        const uint16_t* s1 = a.scale + (size_t)e * 2 * a.I + c0;
+        const uint16_t* rt = a.rot_tab + (size_t)e * 3 * a.I + c0;
+        for (int c = lane; c < bi; c += 32) {
+          const float sg = __half2float(__ushort_as_half(s1[c]));
+          const float su = __half2float(__ushort_as_half(s1[a.I + c]));
+          const float vg = __half2float(__ushort_as_half(rt[c]));
+          const float vu = __half2float(__ushort_as_half(rt[a.I + c]));
+          const float vd = __half2float(__ushort_as_half(rt[2 * a.I + c]));
+          ev[c] = sg;
+          ev[bi + c] = hs * vg;
+          ev[2 * bi + c] = su;
+          ev[3 * bi + c] = hs * vu * vd;
+        }
+      } else {
+        const uint16_t* s2 = a.scale + (size_t)e * a.H + mb * NR;
+        const uint16_t* sv = a.rot_tab + (size_t)e * a.H + mb * NR;
+        for (int c = lane; c < NR; c += 32) {
+          ev[c] = __half2float(__ushort_as_half(s2[c]));
+          ev[NR + c] = hs * __half2float(__ushort_as_half(sv[c]));
+        }
+      }
+    }
+    __syncwarp();
+    for (int acc = 0; acc < macc; ++acc) {
+      const int b = plan.buf(macc, acc);
+      const bool ok = mbar_wait_abort(&B.accFull[b], plan.uses[b] & 1, abort, kTcWaitNs);
+      if (!__all_sync(0xFFFFFFFFu, ok)) return;
+      tc_fence_after();
+      const int n = acc * 128 + 32 * q + lane;
+      const int route = a.route_of_slot[slot0 + n];
+      const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 256);
+      if (PROJ == 1)
+        tc_epi_fc1<NR / 2>(a, ev, mb, slot0 + n, route >= 0, taddr);
+      else
+        tc_epi_fc2<NR>(a, ev, mb, slot0 + n, route, route >= 0, taddr);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.accEmpty[b]);
+      plan.uses[b]++;
+    }
+    plan.advance(macc);
+  }
+}
+
+template <int PROJ, int KB, int NR>
+__device__ __forceinline__ void tc_payload_loader(const TcArgs& args, const TcGeom<PROJ, NR>& G, int units, TcBars& B,
+                                                  unsigned char* wring, volatile int* abort) {
+  const FcArgs& a = args.f;
+  const int lane = threadIdx.x & 31;
+  const int wsz = tc_wslot_bytes(KB > 0 ? KB : 6);
+  int g = 0, gw = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+    const int rb = u / G.mblocks, mb = u - rb * G.mblocks;
+    const int e = a.block_expert[rb];
+    const int K = (KB > 0) ? KB : a.bits[e];
+    const uint32_t wbytes = 4 * 32 * K;  // one tile row of a stage
+    const uint16_t* wsrc = reinterpret_cast<const uint16_t*>(a.payload);
+    if (lane < NR / 16) wsrc += a.word_off[e] + (size_t)(G.tile_row0(a, mb, lane) >> 4) * G.tiles_k * 16 * K;
+    for (int s = 0; s < G.nst; ++s, ++g) {
+      const int ws = g % kSW;
+      const bool okw = (g < kSW) || mbar_wait_abort(&B.emptyW[ws], ((g / kSW) - 1) & 1, abort, kTcWaitNs);
+      if (!__all_sync(0xFFFFFFFFu, okw)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&B.fullW[ws], (NR / 16) * wbytes);
+      __syncwarp();
+      if (lane < NR / 16) bulk_g2s(wring + ws * wsz + lane * wbytes, wsrc + (size_t)s * 4 * 16 * K, wbytes, &B.fullW[ws]);
+      gw = g + 1;
+    }
+  }
+  if (!ok && lane == 0)  // copies in flight land before the CTA exits
+    for (int gg = (gw > kSW ? gw - kSW : 0); gg < gw; ++gg) mbar_wait_drain(&B.fullW[gg % kSW], (gg / kSW) & 1);
+}
+
+// TMA load of a 64-column x 128-row box of the activations (slot order) into
+// the swizzled operand.
+__device__ __forceinline__ void tma_tile2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n"
+      ::"r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(mbar))
+      : "memory");
+}
+
+// Lane 0 loads each stage's activation operand: one box per 128 routes. Rows
+// of padding routes hold whatever the slot holds; they only reach accumulator
+// rows that no epilogue stores.
+template <int PROJ, int KB, int NR>
+__device__ __forceinline__ void tc_act_loader(const TcArgs& args, const TcGeom<PROJ, NR>& G, int units, TcBars& B,
+                                              unsigned char* aring, volatile int* abort) {
+  const FcArgs& a = args.f;
+  const CUtensorMap* map = &args.amap;
+  int g = 0, ga = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+    const int slot0 = (u / G.mblocks) * kTcBN;
+    const int macc = tc_macc(a, slot0);
+    for (int s = 0; s < G.nst; ++s, ++g) {
+      const int as = g % kSA;
+      if (g >= kSA && !mbar_wait_abort(&B.emptyA[as], ((g / kSA) - 1) & 1, abort, kTcWaitNs)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(&B.fullA[as], (uint32_t)macc * 128 * 128);
+      unsigned char* dst = aring + as * kABytes;
+      tma_tile2d(dst, map, s * kTcKS, slot0, &B.fullA[as]);
+      if (macc == 2) tma_tile2d(dst + 128 * 128, map, s * kTcKS, slot0 + 128, &B.fullA[as]);
+      ga = g + 1;
+    }
+  }
+  if (!ok)  // copies in flight land before the CTA exits
+    for (int gg = (ga > kSA ? ga - kSA : 0); gg < ga; ++gg) mbar_wait_drain(&B.fullA[gg % kSA], (gg / kSA) & 1);
+}
+
+template <int PROJ, int KB, int NR>
+__device__ __forceinline__ void tc_issuer(const TcArgs& args, const TcGeom<PROJ, NR>& G, int units, TcBars& B,
+                                          const unsigned char* aring, const unsigned char* bring, uint32_t tmem,
+                                          volatile int* abort) {
+  const FcArgs& a = args.f;
+  const uint32_t idesc = idesc_f16(128, NR);
+  const uint64_t adesc0 = smem_desc_sw128(smem_u32(aring));
+  const uint64_t bdesc0 = smem_desc_sw128(smem_u32(bring));
+  TcAccPlan plan;
+  int g = 0, glast = -1;
+  bool ok = true;
+  for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+    const int macc = tc_macc(a, (u / G.mblocks) * kTcBN);
+    for (int acc = 0; acc < macc && ok; ++acc) {  // the unit's buffers drained by the epilogue
+      const int b = plan.buf(macc, acc);
+      if (plan.uses[b] > 0) ok = mbar_wait_abort(&B.accEmpty[b], (plan.uses[b] - 1) & 1, abort, kTcWaitNs);
+    }
+    if (!ok) break;
+    tc_fence_after();
+    const uint32_t d0 = tmem + (uint32_t)(plan.buf(macc, 0) * 256);
+    for (int s = 0; s < G.nst; ++s, ++g) {
+      const int as = g % kSA, bs = g % kSB;
+      if (!mbar_wait_abort(&B.fullA[as], (g / kSA) & 1, abort, kTcWaitNs) ||
+          !mbar_wait_abort(&B.fullB[bs], (g / kSB) & 1, abort, kTcWaitNs)) {
+        ok = false;
+        break;
+      }
+      fence_proxy_async();  // cp.async / st.shared operand writes -> visible to the tensor core
+      tc_fence_after();
+      const uint64_t ad = adesc0 + (uint64_t)(as * (kABytes >> 4));
+      const uint64_t bd = bdesc0 + (uint64_t)(bs * (kBBytes >> 4));
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint32_t accum = (s > 0 || kk > 0) ? 1u : 0u;
+        tc_mma_f16(d0, ad + 2 * kk, bd + 2 * kk, idesc, accum);
+        if (macc == 2) tc_mma_f16(tmem + 256, ad + 1024 + 2 * kk, bd + 2 * kk, idesc, accum);
+      }
+      tc_commit(&B.emptyA[as]);
+      tc_commit(&B.emptyB[bs]);
+      glast = g;
+    }
+    if (!ok) break;
+    for (int acc = 0; acc < macc; ++acc) {
+      const int b = plan.buf(macc, acc);
+      tc_commit(&B.accFull[b]);
+      plan.uses[b]++;
+    }
+    plan.advance(macc);
+  }
+  if (*abort && glast >= 0) mbar_wait_drain(&B.emptyB[glast % kSB], (glast / kSB) & 1);
+}
+
+template <int N>
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N)); }
+template <int N>
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N)); }
+
+template <int PROJ, int KB, int NR>
+__global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__ TcArgs args) {
+  extern __shared__ unsigned char tc_smem_raw[];
+  __shared__ __align__(8) TcBars bars;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int s_abort;
+  constexpr int kmax = KB > 0 ? KB : 6;
+  unsigned char* smem = tc_smem_raw + ((1024u - (smem_u32(tc_smem_raw) & 1023u)) & 1023u);
+  unsigned char* aring = smem;
+  unsigned char* bring = aring + kSA * kABytes;
+  unsigned char* wring = bring + kSB * kBBytes;
+  unsigned char* evec = wring + kSW * tc_wslot_bytes(kmax);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const TcGeom<PROJ, NR> G(args);
+  const int units = *args.f.nblocks * G.mblocks;
+  if (tid == 0) {
+    for (int i = 0; i < kSA; ++i) {
+      mbar_init(&bars.fullA[i], 1);   // the loader's expect_tx arrival; the gathers complete the bytes
+      mbar_init(&bars.emptyA[i], 1);
+    }
+    for (int i = 0; i < kSB; ++i) {
+      mbar_init(&bars.fullB[i], kTcExp / 32);
+      mbar_init(&bars.emptyB[i], 1);
+    }
+    for (int i = 0; i < kSW; ++i) {
+      mbar_init(&bars.fullW[i], 1);
+      mbar_init(&bars.emptyW[i], kTcExp / 32);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.accFull[i], 1);
+      mbar_init(&bars.accEmpty[i], kTcEpiWarps);
+    }
+    s_abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0) tmem_alloc(&tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile int* abort = &s_abort;
+  if (warp < 8) {
+    regs_dec<kRegExp>();
+    tc_expanders<PROJ, KB, NR>(args, G, units, bars, wring, bring, abort);
+  } else if (warp < 12) {
+    regs_inc<kRegEpi>();
+    tc_epilogue<PROJ, KB, NR>(args, G, units, bars, reinterpret_cast<float*>(evec + (warp - 8) * kEvecBytes), tmem, abort);
+  } else {
+    regs_dec<kRegAux>();
+    if (warp == 12)
+      tc_payload_loader<PROJ, KB, NR>(args, G, units, bars, wring, abort);
+    else if (warp == 13 && (tid & 31) == 0)
+      tc_act_loader<PROJ, KB, NR>(args, G, units, bars, aring, abort);
+    else if (warp == 14 && (tid & 31) == 0)
+      tc_issuer<PROJ, KB, NR>(args, G, units, bars, aring, bring, tmem, abort);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && *abort) atomicOr(args.err, 2u);
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+template <int PROJ, int KB, int NR>
+static cudaError_t launch_tc_t(const TcArgs& args, int max_blocks, cudaStream_t st) {
+  auto kern = k_tc_fc<PROJ, KB, NR>;
+  constexpr int kmax = KB > 0 ? KB : 6;
+  static bool attr_done = false;  // first forward call, before any capture
+  if (!attr_done) {
+    cudaFuncAttributes fa;
+    cudaError_t err = cudaFuncGetAttributes(&fa, kern);
+    if (err != cudaSuccess) return err;
+    if (fa.numRegs != kRegLaunch) return cudaErrorInvalidConfiguration;  // the register split assumes 128
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_smem_total(kmax));
+    if (err != cudaSuccess) return err;
+    attr_done = true;
+  }
+  int dev = 0, sms = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  const int mblocks = (PROJ == 1) ? args.f.I / args.bi : args.f.H / NR;
+  const long units = (long)max_blocks * mblocks;
+  const int grid = (int)std::max<long>(1, std::min<long>(units, sms));
+  kern<<<grid, kTcThreads, tc_smem_total(kmax), st>>>(args);
+  return cudaGetLastError();
+}
+
+int tc_route_block() { return kTcBN; }
+
+bool tc_supported(int H, int I, int bi, int rot_h, int rot_i) {
+  return H % 128 == 0 && I % 64 == 0 && (bi == 64 || bi == 128) && I % bi == 0 && rot_h <= 128 && rot_i <= bi;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+cudaError_t launch_tc_fc(const TcArgs& args_in, int proj, int uniform_k, int max_blocks, cudaStream_t st) {
+  TcArgs args = args_in;
+  {
+    // the activation operand [act_rows][K] fp16 in boxes of 64 columns (128
+    // bytes, the swizzle span) x 128 rows
+    const int kdim = (proj == 1) ? args.f.H : args.f.I;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)kdim, (cuuint64_t)args.act_rows};
+    cuuint64_t strides[1] = {(cuuint64_t)kdim * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kTcKS, 128};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(&args.amap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(args.f.act), dims, strides,
+                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  const bool k4 = uniform_k == 4;
+  if (proj == 1) {
+    if (args.bi == 128) return k4 ? launch_tc_t<1, 4, 256>(args, max_blocks, st) : launch_tc_t<1, 0, 256>(args, max_blocks, st);
+    return k4 ? launch_tc_t<1, 4, 128>(args, max_blocks, st) : launch_tc_t<1, 0, 128>(args, max_blocks, st);
+  }
+  if (args.f.H % 256 == 0)
+    return k4 ? launch_tc_t<2, 4, 256>(args, max_blocks, st) : launch_tc_t<2, 0, 256>(args, max_blocks, st);
+  return k4 ? launch_tc_t<2, 4, 128>(args, max_blocks, st) : launch_tc_t<2, 0, 128>(args, max_blocks, st);
+}
+
+}  // namespace tmoe
