@@ -5,21 +5,23 @@
 // rows: FC1 takes bi gate rows and the bi matching up rows, N = 2 bi; FC2
 // takes N output columns). The contraction runs in stages of 64 columns:
 //
-//   warp 12     (payload)   streams the stage's trellis payload (4 tiles per
+//   warp 16     (payload)   streams the stage's trellis payload (4 tiles per
 //                           tile row) into a 4-deep ring with bulk copies;
-//   warp 13     (activation) one thread loads a stage's activation rows (slot
+//   warp 17     (activation) one thread loads a stage's activation rows (slot
 //                           order, one 128-row box per accumulator) into a
 //                           128-byte swizzled operand with TMA;
 //   warps 0-7   (expanders) decode the stage's N x 64 weights from the payload
 //                           into a second swizzled operand, each codebook value
 //                           the fp16 sum of its word's two halves as the
 //                           codebook defines it;
-//   warp 14     (issuer)    one thread issues tcgen05.mma with the routes as M
+//   warp 18     (issuer)    one thread issues tcgen05.mma with the routes as M
 //                           (one or two accumulators of 128 routes) and the
 //                           weight rows as N, and commits each stage to the
 //                           mbarriers that free its operand slots;
-//   warps 8-11  (epilogue)  one TMEM lane (route) per thread, so the block
-//                           Hadamard transforms run inside a thread's registers
+//   warps 8-15  (epilogue)  one TMEM lane (route) per thread and two warps per
+//                           lane quarter, each taking half of every column
+//                           block, so the block Hadamard transforms run inside
+//                           registers plus one exchange level across the pair
 //                           (FC1: H -> svh -> SiLU(gate)*up -> suh_down -> H, as
 //                           in sparkinfer PR #90 "moe: integrate EXL3 Trellis
 //                           into the fused W4A16 API", review of kernel.py;
@@ -28,7 +30,7 @@
 // Tensor memory holds two 256-column accumulator buffers: a unit of up to 128
 // routes takes one (alternating), a unit of up to 256 routes takes both, so
 // the epilogue of one unit overlaps the contraction of the next. Every
-// hand-off is an mbarrier (full/empty rings of 3 activation, 2 decoded and 4
+// hand-off is an mbarrier (full/empty rings of 2 activation, 3 decoded and 4
 // payload stages, full/empty per accumulator buffer); no role waits on a
 // block-wide barrier. Waits are bounded in wall time; on a timeout the CTA
 // raises the error word, drains its copies and MMAs and releases its tensor
@@ -42,18 +44,20 @@
 
 namespace tmoe {
 
-constexpr int kTcThreads = 512;        // warpgroups: 2 expander, 1 epilogue, 1 loader/issuer
-// Registers per thread after the split (sum x 128 threads = 512 x 128, the
-// launch budget: the kernel must be compiled at 128 registers, which the
-// launcher checks, or setmaxnreg.inc could wait for registers never freed).
-constexpr int kRegExp = 112, kRegEpi = 232, kRegAux = 56, kRegLaunch = 128;
-static_assert(128 * (2 * kRegExp + kRegEpi + kRegAux) <= kTcThreads * kRegLaunch, "register split over budget");
+constexpr int kTcThreads = 640;        // warpgroups: 2 expander, 2 epilogue, 1 loader/issuer
+// Registers per thread after the split: expanders keep the launch count, the
+// loader/issuer warpgroup gives registers up, the epilogue warpgroups take
+// them (sum x 128 threads <= 640 x 96, the launch budget: the kernel must be
+// compiled at 96 registers, which the launcher checks, or setmaxnreg.inc
+// could wait for registers never freed).
+constexpr int kRegExp = 96, kRegEpi = 128, kRegAux = 32, kRegLaunch = 96;
+static_assert(128 * (2 * kRegExp + 2 * kRegEpi + kRegAux) <= kTcThreads * kRegLaunch, "register split over budget");
 constexpr int kTcExp = 256;            // expander threads
-constexpr int kTcEpiWarps = 4;
-constexpr int kEvecBytes = 2048;       // per epilogue warp: the unit's folded scale / sign vectors (fp32)
+constexpr int kTcEpiWarps = 8;         // two per TMEM lane quarter, one per column half
+constexpr int kEvecBytes = 1024;       // per epilogue warp: its half of the unit's folded vectors (fp32)
 constexpr int kTcBN = 256;             // routes per route block
 constexpr int kTcKS = 64;              // contraction columns per stage
-constexpr int kSA = 3, kSB = 2, kSW = 4;
+constexpr int kSA = 2, kSB = 3, kSW = 4;
 constexpr int kABytes = 256 * 128;     // activation operand: 256 routes x 128 bytes
 constexpr int kBBytes = 256 * 128;     // decoded operand: 256 weight rows x 128 bytes
 constexpr uint64_t kTcWaitNs = 2000000000ull;
@@ -68,6 +72,7 @@ __host__ __device__ inline int tc_smem_total(int kmax) {
 
 struct TcBars {
   uint64_t fullA[kSA], emptyA[kSA], fullB[kSB], emptyB[kSB], fullW[kSW], emptyW[kSW], accFull[2], accEmpty[2];
+  uint64_t pair[4];  // epilogue warp pairs, one per TMEM lane quarter
 };
 
 // Work unit geometry shared by every role.
@@ -251,40 +256,96 @@ __device__ __forceinline__ float2 silu2(float2 g) {
   return __ffma2_rn(h, make_float2(tanh_fast(h.x), tanh_fast(h.y)), h);
 }
 
-// FC1 for the route of this thread (epilogue warps hold 232 registers):
-// gate -> scale, H, hs * svh, SiLU, parked in its TMEM columns; up -> scale,
-// H, hs * svh * suh_down, times SiLU(gate); H; hs; the z~ row of the slot
-// (fp16). ev (fp32, BI each): gate scale, hs * gate svh, up scale,
-// hs * up svh * down suh.
-template <int BI>
-__device__ __forceinline__ void tc_epi_fc1(const FcArgs& a, const float* ev, int mb, int slot, bool valid,
-                                           uint32_t taddr) {
-  const float hs = hadamard_scale(a.rot_b);
-  float2 w[BI / 2];
-  ld_cols2<BI>(taddr, w);
-  scale2<BI>(w, ev);
-  fwht2<BI>(w, a.rot_b);
-  scale2<BI>(w, ev + BI);
+// The two epilogue warps of a TMEM lane quarter split every block of columns
+// in halves; a rotation block wider than a half needs its last butterfly
+// level across the pair, exchanged through tensor memory around a bounded
+// two-warp barrier.
+struct PairSync {
+  uint64_t* bar;
+  int phase;
+};
+__device__ __forceinline__ bool pair_sync(PairSync& p, volatile int* abort) {
+  tmem_st_wait();  // this warp's tensor-memory stores are complete
+  tc_fence_before();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(p.bar);
+  const bool ok = mbar_wait_abort(p.bar, p.phase & 1, abort, kTcWaitNs);
+  ++p.phase;
+  tc_fence_after();
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+// Last butterfly level with the partner's half at `theirs` (TMEM columns):
+// the lower warp keeps mine + theirs, the upper theirs - mine.
+template <int HF>
+__device__ __forceinline__ void combine_half(float2 (&w)[HF / 2], uint32_t theirs, int h) {
+  const float2 m1 = make_float2(-1.0f, -1.0f);
 #pragma unroll
-  for (int j = 0; j < BI / 2; ++j) w[j] = silu2(w[j]);
-  st_cols2<BI>(taddr, w);
-  ld_cols2<BI>(taddr + BI, w);
-  scale2<BI>(w, ev + 2 * BI);
-  fwht2<BI>(w, a.rot_b);
-  scale2<BI>(w, ev + 3 * BI);
+  for (int c = 0; c < HF; c += 32) {
+    float2 t[16];
+    ld_cols2<32>(theirs + c, t);
 #pragma unroll
-  for (int c = 0; c < BI; c += 64) {
-    float2 g[32];
-    ld_cols2<64>(taddr + c, g);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) w[c / 2 + j] = __fmul2_rn(w[c / 2 + j], g[j]);
+    for (int j = 0; j < 16; ++j)
+      w[c / 2 + j] = (h == 0) ? __fadd2_rn(w[c / 2 + j], t[j]) : __ffma2_rn(w[c / 2 + j], m1, t[j]);
   }
-  fwht2<BI>(w, a.rot_b);
-  if (valid) {
-    const float2 h2s = make_float2(hs, hs);
-    uint16_t* z = reinterpret_cast<uint16_t*>(a.out_act) + (size_t)slot * a.I + mb * BI;
+}
+
+// FC1, half h of the route's gate and up columns (HF = BI / 2 each). Gate ->
+// scale, H, hs * svh, SiLU; up -> scale, H, hs * svh * suh_down, times
+// SiLU(gate); H; hs; this half of the z~ row (fp16). Tensor-memory plan for
+// the exchange case: each warp publishes its half in place, reads the
+// partner's, then parks SiLU(gate) in the partner's gate half (which only it
+// reads from then on) and later publishes its final half there too.
+// ev (fp32, HF each): gate scale, hs * gate svh, up scale, hs * up svh * down suh.
+template <int BI>
+__device__ __forceinline__ bool tc_epi_fc1(const FcArgs& a, const float* ev, int mb, int slot, bool valid,
+                                           uint32_t tg, int h, PairSync& ps, volatile int* abort) {
+  constexpr int HF = BI / 2;
+  const bool xch = a.rot_b > HF;
+  const uint32_t mine = h * HF, other = (1 - h) * HF;
+  const uint32_t tu = tg + BI;
+  const uint32_t park = xch ? other : mine;
+  float2 w[HF / 2];
+  ld_cols2<HF>(tg + mine, w);
+  scale2<HF>(w, ev);
+  fwht2<HF>(w, a.rot_b);
+  if (xch) {
+    st_cols2<HF>(tg + mine, w);
+    if (!pair_sync(ps, abort)) return false;
+    combine_half<HF>(w, tg + other, h);
+  }
+  scale2<HF>(w, ev + HF);
 #pragma unroll
-    for (int j = 0; j < BI / 2; j += 4) {
+  for (int j = 0; j < HF / 2; ++j) w[j] = silu2(w[j]);
+  st_cols2<HF>(tg + park, w);
+  ld_cols2<HF>(tu + mine, w);
+  scale2<HF>(w, ev + 2 * HF);
+  fwht2<HF>(w, a.rot_b);
+  if (xch) {
+    st_cols2<HF>(tu + mine, w);
+    if (!pair_sync(ps, abort)) return false;
+    combine_half<HF>(w, tu + other, h);
+  }
+  scale2<HF>(w, ev + 3 * HF);
+#pragma unroll
+  for (int c = 0; c < HF; c += 32) {
+    float2 g[16];
+    ld_cols2<32>(tg + park + c, g);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) w[c / 2 + j] = __fmul2_rn(w[c / 2 + j], g[j]);
+  }
+  fwht2<HF>(w, a.rot_b);
+  if (xch) {
+    st_cols2<HF>(tg + park, w);
+    if (!pair_sync(ps, abort)) return false;
+    combine_half<HF>(w, tg + mine, h);
+  }
+  if (valid) {
+    const float hs = hadamard_scale(a.rot_b);
+    const float2 h2s = make_float2(hs, hs);
+    uint16_t* z = reinterpret_cast<uint16_t*>(a.out_act) + (size_t)slot * a.I + mb * BI + h * HF;
+#pragma unroll
+    for (int j = 0; j < HF / 2; j += 4) {
       uint32_t pk[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -294,38 +355,48 @@ __device__ __forceinline__ void tc_epi_fc1(const FcArgs& a, const float* ev, int
       *reinterpret_cast<uint4*>(z + 2 * j) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
   }
+  return true;
 }
 
-// FC2: per 128 output columns scale, rotate, hs * down_svh, then the fp32 row
-// of the slot (deterministic) or weighted atomics into the token's output row.
-// ev (fp32): NR output scales, then NR values hs * down_svh.
+// FC2, half h of each 128-column block of the route's NR output columns:
+// scale, H, hs * down_svh, then the fp32 row of the slot (deterministic) or
+// weighted atomics into the token's output row.
+// ev (fp32): per block, 64 output scales then 64 values hs * down_svh.
 template <int NR>
-__device__ __forceinline__ void tc_epi_fc2(const FcArgs& a, const float* ev, int mb, int slot, int route, bool valid,
-                                           uint32_t taddr) {
+__device__ __forceinline__ bool tc_epi_fc2(const FcArgs& a, const float* ev, int mb, int slot, int route, bool valid,
+                                           uint32_t tb, int h, PairSync& ps, volatile int* abort) {
   const float wr = (valid && a.atomic) ? a.route_w[route] : 0.0f;
+  const uint32_t mine = h * 64, other = (1 - h) * 64;
 #pragma unroll 1
-  for (int h = 0; h < NR / 128; ++h) {
-    const int col0 = mb * NR + h * 128;
-    float2 w[64];
-    ld_cols2<128>(taddr + h * 128, w);
-    scale2<128>(w, ev + h * 128);
-    fwht2<128>(w, a.rot_b);
-    scale2<128>(w, ev + NR + h * 128);
+  for (int blk = 0; blk < NR / 128; ++blk) {
+    const uint32_t t0 = tb + blk * 128;
+    float2 w[32];
+    ld_cols2<64>(t0 + mine, w);
+    scale2<64>(w, ev + blk * 128);
+    fwht2<64>(w, a.rot_b);
+    if (a.rot_b > 64) {
+      st_cols2<64>(t0 + mine, w);
+      if (!pair_sync(ps, abort)) return false;
+      combine_half<64>(w, t0 + other, h);
+    }
+    scale2<64>(w, ev + blk * 128 + 64);
     if (!valid) continue;
+    const int col0 = mb * NR + blk * 128 + h * 64;
     if (!a.atomic) {
       float* o = a.out_f32 + (size_t)slot * a.H + col0;
 #pragma unroll
-      for (int j = 0; j < 64; j += 2)
+      for (int j = 0; j < 32; j += 2)
         *reinterpret_cast<float4*>(o + 2 * j) = make_float4(w[j].x, w[j].y, w[j + 1].x, w[j + 1].y);
     } else {
       float* o = a.out_f32 + (size_t)(route / a.topk) * a.H + col0;
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
+      for (int j = 0; j < 32; ++j) {
         atomicAdd(o + 2 * j, wr * w[j].x);
         atomicAdd(o + 2 * j + 1, wr * w[j].y);
       }
     }
   }
+  return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -389,39 +460,38 @@ template <int PROJ, int KB, int NR>
 __device__ __forceinline__ void tc_epilogue(const TcArgs& args, const TcGeom<PROJ, NR>& G, int units, TcBars& B,
                                             float* ev, uint32_t tmem, volatile int* abort) {
   const FcArgs& a = args.f;
-  const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;  // TMEM lane quarter of this warp
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp & 3;           // TMEM lane quarter
+  const int h = (warp - 8) >> 2;    // column half
+  PairSync ps{&B.pair[q], 0};
   TcAccPlan plan;
   for (int u = blockIdx.x; u < units; u += gridDim.x) {
     const int rb = u / G.mblocks, mb = u - rb * G.mblocks;
     const int e = a.block_expert[rb];
     const int slot0 = rb * kTcBN;
     const int macc = tc_macc(a, slot0);
-    // this warp's copy of the unit's vectors, converted to fp32 and folded
+    // this warp's half of the unit's vectors, converted to fp32 and folded
     // (its reads of the last unit are done)
     __syncwarp();
     {
       const float hs = hadamard_scale(a.rot_b);
       if (PROJ == 1) {
-        const int bi = NR / 2, c0 = mb * bi;
+        const int bi = NR / 2, hf = bi / 2, c0 = mb * bi + h * hf;
         const uint16_t* s1 = a.scale + (size_t)e * 2 * a.I + c0;
         const uint16_t* rt = a.rot_tab + (size_t)e * 3 * a.I + c0;
-        for (int c = lane; c < bi; c += 32) {
-          const float sg = __half2float(__ushort_as_half(s1[c]));
-          const float su = __half2float(__ushort_as_half(s1[a.I + c]));
-          const float vg = __half2float(__ushort_as_half(rt[c]));
-          const float vu = __half2float(__ushort_as_half(rt[a.I + c]));
-          const float vd = __half2float(__ushort_as_half(rt[2 * a.I + c]));
-          ev[c] = sg;
-          ev[bi + c] = hs * vg;
-          ev[2 * bi + c] = su;
-          ev[3 * bi + c] = hs * vu * vd;
+        for (int c = lane; c < hf; c += 32) {
+          ev[c] = __half2float(__ushort_as_half(s1[c]));
+          ev[hf + c] = hs * __half2float(__ushort_as_half(rt[c]));
+          ev[2 * hf + c] = __half2float(__ushort_as_half(s1[a.I + c]));
+          ev[3 * hf + c] = hs * __half2float(__ushort_as_half(rt[a.I + c])) * __half2float(__ushort_as_half(rt[2 * a.I + c]));
         }
       } else {
         const uint16_t* s2 = a.scale + (size_t)e * a.H + mb * NR;
         const uint16_t* sv = a.rot_tab + (size_t)e * a.H + mb * NR;
-        for (int c = lane; c < NR; c += 32) {
-          ev[c] = __half2float(__ushort_as_half(s2[c]));
-          ev[NR + c] = hs * __half2float(__ushort_as_half(sv[c]));
+        for (int i = lane; i < NR / 2; i += 32) {
+          const int blk = i >> 6, c = blk * 128 + h * 64 + (i & 63);
+          ev[blk * 128 + (i & 63)] = __half2float(__ushort_as_half(s2[c]));
+          ev[blk * 128 + 64 + (i & 63)] = hs * __half2float(__ushort_as_half(sv[c]));
         }
       }
     }
@@ -434,10 +504,9 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& args, const TcGeom<PRO
       const int n = acc * 128 + 32 * q + lane;
       const int route = a.route_of_slot[slot0 + n];
       const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 256);
-      if (PROJ == 1)
-        tc_epi_fc1<NR / 2>(a, ev, mb, slot0 + n, route >= 0, taddr);
-      else
-        tc_epi_fc2<NR>(a, ev, mb, slot0 + n, route, route >= 0, taddr);
+      const bool done = (PROJ == 1) ? tc_epi_fc1<NR / 2>(a, ev, mb, slot0 + n, route >= 0, taddr, h, ps, abort)
+                                    : tc_epi_fc2<NR>(a, ev, mb, slot0 + n, route, route >= 0, taddr, h, ps, abort);
+      if (!done) return;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.accEmpty[b]);
@@ -607,6 +676,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__
       mbar_init(&bars.accFull[i], 1);
       mbar_init(&bars.accEmpty[i], kTcEpiWarps);
     }
+    for (int i = 0; i < 4; ++i) mbar_init(&bars.pair[i], 2);
     s_abort = 0;
     mbar_fence_init();
   }
@@ -617,18 +687,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__
   const uint32_t tmem = tmem_slot;
   volatile int* abort = &s_abort;
   if (warp < 8) {
-    regs_dec<kRegExp>();
-    tc_expanders<PROJ, KB, NR>(args, G, units, bars, wring, bring, abort);
-  } else if (warp < 12) {
+    tc_expanders<PROJ, KB, NR>(args, G, units, bars, wring, bring, abort);  // at the launch count
+  } else if (warp < 16) {
     regs_inc<kRegEpi>();
     tc_epilogue<PROJ, KB, NR>(args, G, units, bars, reinterpret_cast<float*>(evec + (warp - 8) * kEvecBytes), tmem, abort);
   } else {
     regs_dec<kRegAux>();
-    if (warp == 12)
+    if (warp == 16)
       tc_payload_loader<PROJ, KB, NR>(args, G, units, bars, wring, abort);
-    else if (warp == 13 && (tid & 31) == 0)
+    else if (warp == 17 && (tid & 31) == 0)
       tc_act_loader<PROJ, KB, NR>(args, G, units, bars, aring, abort);
-    else if (warp == 14 && (tid & 31) == 0)
+    else if (warp == 18 && (tid & 31) == 0)
       tc_issuer<PROJ, KB, NR>(args, G, units, bars, aring, bring, tmem, abort);
   }
   tc_fence_before();
