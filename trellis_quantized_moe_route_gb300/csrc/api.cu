@@ -118,7 +118,7 @@ Layout make_layout(const tm_layer_desc& d, int T) {
   L.bytes[Layout::ZS] = slots * (d.I / 32);
   L.bytes[Layout::ROWS] = slots * d.H * 4;
   L.bytes[Layout::SLOT_OF_ROUTE] = R * 4;
-  L.bytes[Layout::ERR] = 4;
+  L.bytes[Layout::ERR] = 16;  // error word, then the tcgen05 kernels' unit counters
   L.bytes[Layout::IDS] = R * 4;
   L.bytes[Layout::W] = R * 4;
   L.bytes[Layout::RANK] = R * 4;
@@ -197,7 +197,7 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
   const DecPlan dp = dec_plan(d, T);
   // (the decode prologue clears the error word itself)
   if (dp.use) return run_decode_path(layer, x, ids, w, logits, T, w4a8, out, ws, L, dp, st);
-  if ((e = cudaMemsetAsync(err, 0, 4, st)) != cudaSuccess) return cuda_fail(e, "clear error word");
+  if ((e = cudaMemsetAsync(err, 0, 16, st)) != cudaSuccess) return cuda_fail(e, "clear error word");
   if (logits) {
     e = tmoe::launch_route_topk(logits, T, d.E, d.topk, const_cast<int32_t*>(ids), const_cast<float*>(w), st);
     if (e != cudaSuccess) return cuda_fail(e, "router");
@@ -249,6 +249,7 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
   t1.f = a1;
   t1.bi = layer->bi;
   t1.err = err;
+  t1.sched = err + 1;
   t1.act_rows = (int)(R + (size_t)d.E * (kBlockMax - 1));  // slots
   if (use_tc)
     e = tmoe::launch_tc_fc(t1, 1, layer->uniform_k, max_blocks, st);
@@ -279,6 +280,7 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
   t2.f = a2;
   t2.bi = layer->bi;
   t2.err = err;
+  t2.sched = err + 2;
   t2.act_rows = (int)(R + (size_t)d.E * (kBlockMax - 1));  // slots
   if (use_tc)
     e = tmoe::launch_tc_fc(t2, 2, layer->uniform_k, max_blocks, st);
@@ -597,7 +599,7 @@ tm_status trellis_moe_route_map(tm_layer* layer, const int32_t* topk_ids, int32_
   cudaStream_t st = (cudaStream_t)stream;
   uint32_t* err = at<uint32_t>(workspace, L, Layout::ERR);
   cudaError_t e;
-  if ((e = cudaMemsetAsync(err, 0, 4, st)) != cudaSuccess) return cuda_fail(e, "clear error word");
+  if ((e = cudaMemsetAsync(err, 0, 16, st)) != cudaSuccess) return cuda_fail(e, "clear error word");
   tmoe::RouteMapArgs rm;
   rm.ids = topk_ids;
   rm.R = R;

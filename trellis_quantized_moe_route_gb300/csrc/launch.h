@@ -92,6 +92,7 @@ struct TcArgs {
   FcArgs f;
   int bi;          // FC1 half-row block (64 or 128)
   uint32_t* err;   // device error word (bit 1: a pipeline wait gave up)
+  uint32_t* sched; // device unit counter, zero before the launch
   int act_rows;    // rows of the activation operand, in slot order: slots
   CUtensorMap amap;  // filled by launch_tc_fc: the activations as [act_rows][K] fp16, box 64 x 128, 128-byte swizzle
 };

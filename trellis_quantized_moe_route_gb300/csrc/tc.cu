@@ -1,11 +1,13 @@
 // Prefill contraction on the 5th-generation tensor cores (sm_103a, W4A16).
 //
-// A persistent, warp-specialised kernel; one CTA per SM walks work units
+// A persistent, warp-specialised kernel; one CTA per SM takes work units
 // (route block rb of up to 256 routes of one expert) x (block mb of N weight
 // rows: FC1 takes bi gate rows and the bi matching up rows, N = 2 bi; FC2
 // takes N output columns). The contraction runs in stages of 64 columns:
 //
-//   warp 16     (payload)   streams the stage's trellis payload (4 tiles per
+//   warp 16     (payload)   claims units from a device counter, publishes them
+//                           to the other roles through a small ring, and
+//                           streams each stage's trellis payload (4 tiles per
 //                           tile row) into a 4-deep ring with bulk copies;
 //   warp 17     (activation) one thread loads a stage's activation rows (slot
 //                           order, one 128-row box per accumulator) into a
@@ -73,6 +75,7 @@ __host__ __device__ inline int tc_smem_total(int kmax) {
 struct TcBars {
   uint64_t fullA[kSA], emptyA[kSA], fullB[kSB], emptyB[kSB], fullW[kSW], emptyW[kSW], accFull[2], accEmpty[2];
   uint64_t pair[4];  // epilogue warp pairs, one per TMEM lane quarter
+  uint64_t fullU[4], emptyU[4];  // unit ring: the scheduler's picks, read by every role in order
 };
 
 // Work unit geometry shared by every role.
@@ -408,6 +411,41 @@ __device__ __forceinline__ int tc_macc(const FcArgs& a, int slot0) {
   return (a.route_of_slot[slot0 + 128] >= 0) ? 2 : 1;
 }
 
+// Unit ring. The payload warp, the first role to need a unit, claims units
+// from a device counter (so a CTA that drew cheap units draws more; the claim
+// for the next unit is issued one unit early to hide its latency) and
+// publishes each pick, -1 when none is left; every other role reads the picks
+// in order and frees an entry once read.
+constexpr int kUnitRing = 4;
+constexpr int kUnitConsumers = 8 + kTcEpiWarps + 2;  // expander warps, epilogue warps, act and issuer threads
+
+// Next unit for a consumer warp (all lanes) or a single consumer thread;
+// -1 when the units are done or a wait gave up (then *ok = false).
+__device__ __forceinline__ int pop_unit_warp(TcBars& B, volatile int* uring, int& i, volatile int* abort, bool* ok) {
+  const int slot = i % kUnitRing;
+  const bool w = mbar_wait_abort(&B.fullU[slot], (i / kUnitRing) & 1, abort, kTcWaitNs);
+  if (!__all_sync(0xFFFFFFFFu, w)) {
+    *ok = false;
+    return -1;
+  }
+  const int u = uring[slot];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&B.emptyU[slot]);
+  ++i;
+  return u;
+}
+__device__ __forceinline__ int pop_unit_thread(TcBars& B, volatile int* uring, int& i, volatile int* abort, bool* ok) {
+  const int slot = i % kUnitRing;
+  if (!mbar_wait_abort(&B.fullU[slot], (i / kUnitRing) & 1, abort, kTcWaitNs)) {
+    *ok = false;
+    return -1;
+  }
+  const int u = uring[slot];
+  mbar_arrive(&B.emptyU[slot]);
+  ++i;
+  return u;
+}
+
 // Accumulator buffers of a unit: one alternating buffer for <= 128 routes,
 // both (acc 0 in buffer 0, acc 1 in buffer 1) for more.
 struct TcAccPlan {
@@ -418,14 +456,15 @@ struct TcAccPlan {
 };
 
 template <int PROJ, int KB, int NR>
-__device__ __forceinline__ void tc_expanders(const TcArgs& args, const TcGeom<PROJ, NR>& G, int units, TcBars& B,
+__device__ __forceinline__ void tc_expanders(const TcArgs& args, const TcGeom<PROJ, NR>& G, volatile int* uring, TcBars& B,
                                              const unsigned char* wring, unsigned char* bring, volatile int* abort) {
   const FcArgs& a = args.f;
   const int tid = threadIdx.x, lane = tid & 31;
   const uint32_t k16 = 0x10000u + (uint32_t)((unsigned)G.nst >> 30), nk16 = 0u - k16;
   const int wsz = tc_wslot_bytes(KB > 0 ? KB : 6);
-  int g = 0;
-  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+  int g = 0, iu = 0;
+  bool ok = true;
+  for (int u; (u = pop_unit_warp(B, uring, iu, abort, &ok)) >= 0;) {
     const int rb = u / G.mblocks;
     const int K = (KB > 0) ? KB : a.bits[a.block_expert[rb]];
     for (int s = 0; s < G.nst; ++s, ++g) {
@@ -457,7 +496,7 @@ __device__ __forceinline__ void tc_expanders(const TcArgs& args, const TcGeom<PR
 }
 
 template <int PROJ, int KB, int NR>
-__device__ __forceinline__ void tc_epilogue(const TcArgs& args, const TcGeom<PROJ, NR>& G, int units, TcBars& B,
+__device__ __forceinline__ void tc_epilogue(const TcArgs& args, const TcGeom<PROJ, NR>& G, volatile int* uring, TcBars& B,
                                             float* ev, uint32_t tmem, volatile int* abort) {
   const FcArgs& a = args.f;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -465,7 +504,9 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& args, const TcGeom<PRO
   const int h = (warp - 8) >> 2;    // column half
   PairSync ps{&B.pair[q], 0};
   TcAccPlan plan;
-  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+  int iu = 0;
+  bool ok = true;
+  for (int u; (u = pop_unit_warp(B, uring, iu, abort, &ok)) >= 0;) {
     const int rb = u / G.mblocks, mb = u - rb * G.mblocks;
     const int e = a.block_expert[rb];
     const int slot0 = rb * kTcBN;
@@ -504,9 +545,13 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& args, const TcGeom<PRO
       const int n = acc * 128 + 32 * q + lane;
       const int route = a.route_of_slot[slot0 + n];
       const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 256);
-      const bool done = (PROJ == 1) ? tc_epi_fc1<NR / 2>(a, ev, mb, slot0 + n, route >= 0, taddr, h, ps, abort)
-                                    : tc_epi_fc2<NR>(a, ev, mb, slot0 + n, route, route >= 0, taddr, h, ps, abort);
-      if (!done) return;
+      // a lane quarter without valid routes has nothing to store (both warps
+      // of the pair see the same lanes, so they skip together)
+      if (__any_sync(0xFFFFFFFFu, route >= 0)) {
+        const bool done = (PROJ == 1) ? tc_epi_fc1<NR / 2>(a, ev, mb, slot0 + n, route >= 0, taddr, h, ps, abort)
+                                      : tc_epi_fc2<NR>(a, ev, mb, slot0 + n, route, route >= 0, taddr, h, ps, abort);
+        if (!done) return;
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.accEmpty[b]);
@@ -517,14 +562,32 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& args, const TcGeom<PRO
 }
 
 template <int PROJ, int KB, int NR>
-__device__ __forceinline__ void tc_payload_loader(const TcArgs& args, const TcGeom<PROJ, NR>& G, int units, TcBars& B,
-                                                  unsigned char* wring, volatile int* abort) {
+__device__ __forceinline__ void tc_payload_loader(const TcArgs& args, const TcGeom<PROJ, NR>& G, int units,
+                                                  volatile int* uring, TcBars& B, unsigned char* wring,
+                                                  volatile int* abort) {
   const FcArgs& a = args.f;
   const int lane = threadIdx.x & 31;
   const int wsz = tc_wslot_bytes(KB > 0 ? KB : 6);
   int g = 0, gw = 0;
   bool ok = true;
-  for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+  uint32_t next = (lane == 0) ? atomicAdd(args.sched, 1u) : 0u;
+  for (int iu = 0;; ++iu) {
+    const int slot = iu % kUnitRing;
+    if (iu >= kUnitRing) {
+      const bool okr = mbar_wait_abort(&B.emptyU[slot], ((iu / kUnitRing) - 1) & 1, abort, kTcWaitNs);
+      if (!__all_sync(0xFFFFFFFFu, okr)) {
+        ok = false;
+        break;
+      }
+    }
+    const uint32_t claimed = __shfl_sync(0xFFFFFFFFu, next, 0);
+    const int u = (claimed < (uint32_t)units) ? (int)claimed : -1;
+    if (lane == 0) {
+      uring[slot] = u;
+      mbar_arrive(&B.fullU[slot]);  // release: the pick is visible to the waiters
+      if (u >= 0) next = atomicAdd(args.sched, 1u);
+    }
+    if (u < 0) break;
     const int rb = u / G.mblocks, mb = u - rb * G.mblocks;
     const int e = a.block_expert[rb];
     const int K = (KB > 0) ? KB : a.bits[e];
@@ -543,6 +606,7 @@ __device__ __forceinline__ void tc_payload_loader(const TcArgs& args, const TcGe
       if (lane < NR / 16) bulk_g2s(wring + ws * wsz + lane * wbytes, wsrc + (size_t)s * 4 * 16 * K, wbytes, &B.fullW[ws]);
       gw = g + 1;
     }
+    if (!ok) break;
   }
   if (!ok && lane == 0)  // copies in flight land before the CTA exits
     for (int gg = (gw > kSW ? gw - kSW : 0); gg < gw; ++gg) mbar_wait_drain(&B.fullW[gg % kSW], (gg / kSW) & 1);
@@ -561,13 +625,13 @@ __device__ __forceinline__ void tma_tile2d(void* dst, const CUtensorMap* map, in
 // of padding routes hold whatever the slot holds; they only reach accumulator
 // rows that no epilogue stores.
 template <int PROJ, int KB, int NR>
-__device__ __forceinline__ void tc_act_loader(const TcArgs& args, const TcGeom<PROJ, NR>& G, int units, TcBars& B,
-                                              unsigned char* aring, volatile int* abort) {
+__device__ __forceinline__ void tc_act_loader(const TcArgs& args, const TcGeom<PROJ, NR>& G, volatile int* uring,
+                                              TcBars& B, unsigned char* aring, volatile int* abort) {
   const FcArgs& a = args.f;
   const CUtensorMap* map = &args.amap;
-  int g = 0, ga = 0;
+  int g = 0, ga = 0, iu = 0;
   bool ok = true;
-  for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+  for (int u; ok && (u = pop_unit_thread(B, uring, iu, abort, &ok)) >= 0;) {
     const int slot0 = (u / G.mblocks) * kTcBN;
     const int macc = tc_macc(a, slot0);
     for (int s = 0; s < G.nst; ++s, ++g) {
@@ -588,7 +652,7 @@ __device__ __forceinline__ void tc_act_loader(const TcArgs& args, const TcGeom<P
 }
 
 template <int PROJ, int KB, int NR>
-__device__ __forceinline__ void tc_issuer(const TcArgs& args, const TcGeom<PROJ, NR>& G, int units, TcBars& B,
+__device__ __forceinline__ void tc_issuer(const TcArgs& args, const TcGeom<PROJ, NR>& G, volatile int* uring, TcBars& B,
                                           const unsigned char* aring, const unsigned char* bring, uint32_t tmem,
                                           volatile int* abort) {
   const FcArgs& a = args.f;
@@ -596,9 +660,9 @@ __device__ __forceinline__ void tc_issuer(const TcArgs& args, const TcGeom<PROJ,
   const uint64_t adesc0 = smem_desc_sw128(smem_u32(aring));
   const uint64_t bdesc0 = smem_desc_sw128(smem_u32(bring));
   TcAccPlan plan;
-  int g = 0, glast = -1;
+  int g = 0, glast = -1, iu = 0;
   bool ok = true;
-  for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+  for (int u; ok && (u = pop_unit_thread(B, uring, iu, abort, &ok)) >= 0;) {
     const int macc = tc_macc(a, (u / G.mblocks) * kTcBN);
     for (int acc = 0; acc < macc && ok; ++acc) {  // the unit's buffers drained by the epilogue
       const int b = plan.buf(macc, acc);
@@ -650,6 +714,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__
   __shared__ __align__(8) TcBars bars;
   __shared__ uint32_t tmem_slot;
   __shared__ int s_abort;
+  __shared__ int s_uring[kUnitRing];
   constexpr int kmax = KB > 0 ? KB : 6;
   unsigned char* smem = tc_smem_raw + ((1024u - (smem_u32(tc_smem_raw) & 1023u)) & 1023u);
   unsigned char* aring = smem;
@@ -677,6 +742,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__
       mbar_init(&bars.accEmpty[i], kTcEpiWarps);
     }
     for (int i = 0; i < 4; ++i) mbar_init(&bars.pair[i], 2);
+    for (int i = 0; i < kUnitRing; ++i) {
+      mbar_init(&bars.fullU[i], 1);
+      mbar_init(&bars.emptyU[i], kUnitConsumers);
+    }
     s_abort = 0;
     mbar_fence_init();
   }
@@ -686,19 +755,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   volatile int* abort = &s_abort;
+  volatile int* uring = s_uring;
   if (warp < 8) {
-    tc_expanders<PROJ, KB, NR>(args, G, units, bars, wring, bring, abort);  // at the launch count
+    tc_expanders<PROJ, KB, NR>(args, G, uring, bars, wring, bring, abort);  // at the launch count
   } else if (warp < 16) {
     regs_inc<kRegEpi>();
-    tc_epilogue<PROJ, KB, NR>(args, G, units, bars, reinterpret_cast<float*>(evec + (warp - 8) * kEvecBytes), tmem, abort);
+    tc_epilogue<PROJ, KB, NR>(args, G, uring, bars, reinterpret_cast<float*>(evec + (warp - 8) * kEvecBytes), tmem, abort);
   } else {
     regs_dec<kRegAux>();
     if (warp == 16)
-      tc_payload_loader<PROJ, KB, NR>(args, G, units, bars, wring, abort);
+      tc_payload_loader<PROJ, KB, NR>(args, G, units, uring, bars, wring, abort);
     else if (warp == 17 && (tid & 31) == 0)
-      tc_act_loader<PROJ, KB, NR>(args, G, units, bars, aring, abort);
+      tc_act_loader<PROJ, KB, NR>(args, G, uring, bars, aring, abort);
     else if (warp == 18 && (tid & 31) == 0)
-      tc_issuer<PROJ, KB, NR>(args, G, units, bars, aring, bring, tmem, abort);
+      tc_issuer<PROJ, KB, NR>(args, G, uring, bars, aring, bring, tmem, abort);
   }
   tc_fence_before();
   __syncthreads();
