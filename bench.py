@@ -244,7 +244,8 @@ def run_ours(args, rank, world):
     pk = peaks()
     if mode == "w4a8" and T <= 64:
         achieved = statistics.mean(fc1_bytes) / (stages_us["fc1"] * 1e-6) / 1e9
-        roof = {"bound": "hbm", "kernel": "k_dec_fc<W4A8,FC1,K=4>" if R <= 1024 and R < 4 * cfg.E else "k_fc<W4A8,FC1>",
+        roof = {"bound": "hbm", "kernel": "k_dec_fc<W4A8,FC1,K=4> (decode rows, split contraction)"
+                if R <= 1024 and R < 4 * cfg.E else "k_tc_fc<FC1,K=4,W4A8> (tcgen05)",
                 "achieved": round(achieved, 1),
                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
                 "traffic": None, "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst)",
@@ -252,7 +253,7 @@ def run_ours(args, rank, world):
     else:
         flops = 2 * R * 2 * cfg.I * cfg.H
         achieved = flops / (stages_us["fc1"] * 1e-6) / 1e12
-        kname = "k_tc_fc<FC1> (tcgen05, doubled-K fp16)" if mode == "w4a16" else "k_fc<W4A8,FC1> (mma.sync)"
+        kname = "k_tc_fc<FC1,%s> (tcgen05)" % ("W4A16" if mode == "w4a16" else "W4A8")
         roof = {"bound": "tensor", "kernel": kname, "achieved": round(achieved, 2),
                 "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4),
                 "traffic": None, "peak_source": pk["source"] + " (bf16 dense burst; fp16 runs at the bf16 rate)",
@@ -281,8 +282,9 @@ def run_ours(args, rank, world):
            "h2d_bytes_per_step": T * cfg.H * 2 + T * cfg.E * 4, "d2h_bytes_per_step": T * cfg.H * 4,
            "steps": e2e_steps, "api": "trellis_moe_forward_host"}
 
-    decode_path = R <= 1024 and R < 4 * cfg.E   # the library's decode-rows path (3 kernels)
-    launches_per_step = 3 if decode_path else 6 + (2 if R > 1024 else 0)  # router, route map (1 or 3), rotate, FC1, FC2, combine
+    decode_path = R <= 1024 and R < 4 * cfg.E   # the library's decode-rows path
+    # decode rows: prologue, FC1, FC2 (with the combine); otherwise router, route map (1 or 3), rotate, FC1, FC2, combine
+    launches_per_step = 3 if decode_path else 6 + (2 if R > 1024 else 0)
     res = {
         "metric": METRIC, "value": round(args.steps * T * world / (total_ms / 1e3), 2), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,

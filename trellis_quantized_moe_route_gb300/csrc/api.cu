@@ -184,9 +184,9 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
   const tm_layer_desc& d = layer->desc;
   const bool w4a8 = (mode == TM_MODE_W4A8) || (mode == TM_MODE_AUTO && T <= d.decode_max_rows);
   const int R = T * d.topk;
-  // W4A16 outside the decode regime runs on the tcgen05 kernels (route blocks
-  // of up to 256 routes); W4A8 there keeps the mma.sync kernels.
-  const bool use_tc = !w4a8 && tmoe::tc_supported(d.H, d.I, layer->bi, d.rot_block_h, d.rot_block_i);
+  // Outside the decode regime FC1 and FC2 run on the tcgen05 kernels (route
+  // blocks of up to 256 routes); the mma.sync kernels cover other geometries.
+  const bool use_tc = tmoe::tc_supported(d.H, d.I, layer->bi, d.rot_block_h, d.rot_block_i);
   const int bn = use_tc ? tmoe::tc_route_block() : choose_bn(d, T);
   cudaError_t e;
   uint32_t* err = at<uint32_t>(ws, L, Layout::ERR);
@@ -252,7 +252,7 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
   t1.sched = err + 1;
   t1.act_rows = (int)(R + (size_t)d.E * (kBlockMax - 1));  // slots
   if (use_tc)
-    e = tmoe::launch_tc_fc(t1, 1, layer->uniform_k, max_blocks, st);
+    e = tmoe::launch_tc_fc(t1, 1, layer->uniform_k, w4a8, max_blocks, st);
   else
     e = tmoe::launch_fc1(a1, w4a8, layer->bi, bn, layer->uniform_k, max_blocks, st);
   if (e != cudaSuccess) return cuda_fail(e, "FC1");
@@ -283,7 +283,7 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
   t2.sched = err + 2;
   t2.act_rows = (int)(R + (size_t)d.E * (kBlockMax - 1));  // slots
   if (use_tc)
-    e = tmoe::launch_tc_fc(t2, 2, layer->uniform_k, max_blocks, st);
+    e = tmoe::launch_tc_fc(t2, 2, layer->uniform_k, w4a8, max_blocks, st);
   else
     e = tmoe::launch_fc2(a2, w4a8, bn, layer->uniform_k, max_blocks, st);
   if (e != cudaSuccess) return cuda_fail(e, "FC2");

@@ -86,8 +86,9 @@ cudaError_t launch_dec_fc(const DecArgs& d, int proj, bool w4a8, int uniform_k, 
 // `units` 128-row CTAs per split exist (also sizes the workspace).
 int dec_ksplit(int kdim, long units);
 
-// Prefill path on tcgen05 (W4A16): x~ [slots][H] and z~ [slots][I] fp16 in
-// slot order, route blocks of tc_route_block() slots.
+// FC1 / FC2 on tcgen05 outside the decode regime: x~ [slots][H] and z~
+// [slots][I] fp16 in slot order (W4A8: the exact dequantized MXFP8 values),
+// route blocks of tc_route_block() slots.
 struct TcArgs {
   FcArgs f;
   int bi;          // FC1 half-row block (64 or 128)
@@ -96,7 +97,7 @@ struct TcArgs {
   int act_rows;    // rows of the activation operand, in slot order: slots
   CUtensorMap amap;  // filled by launch_tc_fc: the activations as [act_rows][K] fp16, box 64 x 128, 128-byte swizzle
 };
-cudaError_t launch_tc_fc(const TcArgs& args, int proj, int uniform_k, int max_blocks, cudaStream_t st);
+cudaError_t launch_tc_fc(const TcArgs& args, int proj, int uniform_k, bool w4a8, int max_blocks, cudaStream_t st);
 int tc_route_block();
 // Geometry the tcgen05 kernels handle (H, I, FC1 half-row block, rotation blocks).
 bool tc_supported(int H, int I, int bi, int rot_h, int rot_i);

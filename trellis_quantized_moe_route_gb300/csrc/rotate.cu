@@ -21,7 +21,7 @@ cudaError_t launch_rotate_quant(const uint16_t* x, const uint16_t* suh, int T, i
   const long warps = (long)T * (H / 128);
   const int blocks = (int)((warps * 32 + 255) / 256);
   if (w4a8)
-    k_rotate_quant<true><<<blocks, 256, 0, st>>>(x, suh, T, H, rot_b, xq, xs, nullptr, 0);
+    k_rotate_quant<true><<<blocks, 256, 0, st>>>(x, suh, T, H, rot_b, xq, xs, slot_of_route, topk);
   else
     k_rotate_quant<false><<<blocks, 256, 0, st>>>(x, suh, T, H, rot_b, xq, xs, slot_of_route, topk);
   return cudaGetLastError();

@@ -7,8 +7,10 @@
 namespace tmoe {
 
 // One warp per (token, 128-wide chunk of H); lane l holds entries 4l..4l+3.
-// With `slot_of_route` (fp16 only) the rotated row is stored once per route of
-// the token, at the route's slot: x~ in slot order, [slots][H].
+// Outputs: fp16 x~ [T][H] (W4A16), E4M3 codes [T][H] + E8M0 scales (W4A8).
+// With `slot_of_route` the row is stored as fp16 once per route of the token,
+// at the route's slot (x~ in slot order, [slots][H]); W4A8 then stores the
+// exact dequantized MXFP8 values code * 2^e.
 template <bool W4A8>
 static __device__ __forceinline__ void rotate_quant_warp(const uint16_t* __restrict__ x,
                                                          const uint16_t* __restrict__ suh, int T, int H, int rot_b,
@@ -35,7 +37,22 @@ static __device__ __forceinline__ void rotate_quant_warp(const uint16_t* __restr
   const float sc = hadamard_scale(rot_b);
 #pragma unroll
   for (int i = 0; i < 4; ++i) v[i] *= sc;
-  if (!W4A8) {
+  if (W4A8 && slot_of_route != nullptr) {
+    // MXFP8 rounding kept as the dequantized values (32-element block = 8 lanes)
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const int e = e8m0_exponent(amax);
+    const float inv = exp2_int(-e), sc = exp2_int(e);
+#pragma unroll
+    for (int i = 0; i < 4; i += 2) {
+      const uint32_t q = e4m3x2_to_f16x2(e4m3x2_from_float2(v[i] * inv, v[i + 1] * inv));
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&q));
+      v[i] = f.x * sc;
+      v[i + 1] = f.y * sc;
+    }
+  }
+  if (!W4A8 || slot_of_route != nullptr) {
     __half2 a = __floats2half2_rn(v[0], v[1]);
     __half2 b = __floats2half2_rn(v[2], v[3]);
     uint2 o;

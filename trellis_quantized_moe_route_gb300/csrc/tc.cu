@@ -1,4 +1,6 @@
-// Prefill contraction on the 5th-generation tensor cores (sm_103a, W4A16).
+// FC1 / FC2 on the 5th-generation tensor cores (sm_103a) outside the decode
+// regime: W4A16, and W4A8 with E4M3-rounded weights and exactly dequantized
+// MXFP8 activations held in fp16.
 //
 // A persistent, warp-specialised kernel; one CTA per SM takes work units
 // (route block rb of up to 256 routes of one expert) x (block mb of N weight
@@ -114,6 +116,13 @@ __device__ __forceinline__ void run_window_smem(const uint16_t* tile, int j0, ui
   lo = (w2 << 16) | w3;
 }
 
+// W4A8 weights: every fp16 codebook value replaced by its E4M3 rounding
+// (nearest even, saturating), held exactly in fp16.
+__device__ __forceinline__ void e4m3_round(uint32_t (&w)[4]) {
+#pragma unroll
+  for (int p = 0; p < 4; ++p) w[p] = e4m3x2_to_f16x2(cvt_e4m3x2(w[p]));
+}
+
 __device__ __forceinline__ void sts128(unsigned char* p, const uint32_t (&w)[4]) {
   *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
@@ -123,7 +132,7 @@ __device__ __forceinline__ void sts128(unsigned char* p, const uint32_t (&w)[4])
 // into the swizzled operand `bsl`. Thread t takes row t % NR and 8 * NR / 256
 // of the row's 8 chunks of 8 columns; chunk c of a row is run (tile c / 2,
 // half c % 2) of the row's trellis tiles.
-template <int NR, int K>
+template <int NR, int K, bool W4A8>
 __device__ __forceinline__ void tc_expand_stage(const unsigned char* wsl, unsigned char* bsl, int tid,
                                                 uint32_t k16, uint32_t nk16) {
   constexpr int CPT = 8 * NR / 256;
@@ -147,9 +156,11 @@ __device__ __forceinline__ void tc_expand_stage(const unsigned char* wsl, unsign
       uint32_t y[8], w[4];
       run_mcg_k4(pw, cw.x, k16, nk16, y);
       raw_to_f16(y, w);
+      if (W4A8) e4m3_round(w);
       sts128(brow + (((uint32_t)(2 * t) ^ sw) << 4), w);
       run_mcg_k4(cw.x, cw.y, k16, nk16, y);
       raw_to_f16(y, w);
+      if (W4A8) e4m3_round(w);
       sts128(brow + (((uint32_t)(2 * t + 1) ^ sw) << 4), w);
     }
   } else {
@@ -164,6 +175,7 @@ __device__ __forceinline__ void tc_expand_stage(const unsigned char* wsl, unsign
 #pragma unroll
       for (int q = 0; q < 8; ++q) y[q] = mcg_raw(s8[q]);
       raw_to_f16(y, w);
+      if (W4A8) e4m3_round(w);
       sts128(brow + (((uint32_t)c ^ sw) << 4), w);
     }
   }
@@ -300,7 +312,7 @@ __device__ __forceinline__ void combine_half(float2 (&w)[HF / 2], uint32_t their
 // partner's, then parks SiLU(gate) in the partner's gate half (which only it
 // reads from then on) and later publishes its final half there too.
 // ev (fp32, HF each): gate scale, hs * gate svh, up scale, hs * up svh * down suh.
-template <int BI>
+template <int BI, bool W4A8>
 __device__ __forceinline__ bool tc_epi_fc1(const FcArgs& a, const float* ev, int mb, int slot, bool valid,
                                            uint32_t tg, int h, PairSync& ps, volatile int* abort) {
   constexpr int HF = BI / 2;
@@ -346,13 +358,34 @@ __device__ __forceinline__ bool tc_epi_fc1(const FcArgs& a, const float* ev, int
   if (valid) {
     const float hs = hadamard_scale(a.rot_b);
     const float2 h2s = make_float2(hs, hs);
+#pragma unroll
+    for (int j = 0; j < HF / 2; ++j) w[j] = __fmul2_rn(w[j], h2s);
+    if (W4A8) {
+      // MXFP8 over each 32 consecutive values (E8M0 exponent from the block's
+      // max |z|, E4M3 nearest even, saturating), stored as the exact
+      // dequantized values
+#pragma unroll
+      for (int b0 = 0; b0 < HF / 2; b0 += 16) {
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fmaxf(fabsf(w[b0 + j].x), fabsf(w[b0 + j].y)));
+        const int ex = e8m0_exponent(amax);
+        const float inv = exp2_int(-ex), sc = exp2_int(ex);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t q = e4m3x2_to_f16x2(e4m3x2_from_float2(w[b0 + j].x * inv, w[b0 + j].y * inv));
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&q));
+          w[b0 + j] = make_float2(f.x * sc, f.y * sc);
+        }
+      }
+    }
     uint16_t* z = reinterpret_cast<uint16_t*>(a.out_act) + (size_t)slot * a.I + mb * BI + h * HF;
 #pragma unroll
     for (int j = 0; j < HF / 2; j += 4) {
       uint32_t pk[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        __half2 h2 = __float22half2_rn(__fmul2_rn(w[j + i], h2s));
+        __half2 h2 = __float22half2_rn(w[j + i]);
         pk[i] = *reinterpret_cast<uint32_t*>(&h2);
       }
       *reinterpret_cast<uint4*>(z + 2 * j) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -455,7 +488,7 @@ struct TcAccPlan {
   __device__ __forceinline__ void advance(int macc) { nb = (macc == 2) ? 0 : (nb ^ 1); }
 };
 
-template <int PROJ, int KB, int NR>
+template <int PROJ, int KB, int NR, bool W4A8>
 __device__ __forceinline__ void tc_expanders(const TcArgs& args, const TcGeom<PROJ, NR>& G, volatile int* uring, TcBars& B,
                                              const unsigned char* wring, unsigned char* bring, volatile int* abort) {
   const FcArgs& a = args.f;
@@ -475,14 +508,14 @@ __device__ __forceinline__ void tc_expanders(const TcArgs& args, const TcGeom<PR
       const unsigned char* wsl = wring + ws * wsz;
       unsigned char* bsl = bring + bs * kBBytes;
       if (KB > 0) {
-        tc_expand_stage<NR, (KB > 0 ? KB : 4)>(wsl, bsl, tid, k16, nk16);
+        tc_expand_stage<NR, (KB > 0 ? KB : 4), W4A8>(wsl, bsl, tid, k16, nk16);
       } else {
         switch (K) {
-          case 2: tc_expand_stage<NR, 2>(wsl, bsl, tid, k16, nk16); break;
-          case 3: tc_expand_stage<NR, 3>(wsl, bsl, tid, k16, nk16); break;
-          case 4: tc_expand_stage<NR, 4>(wsl, bsl, tid, k16, nk16); break;
-          case 5: tc_expand_stage<NR, 5>(wsl, bsl, tid, k16, nk16); break;
-          default: tc_expand_stage<NR, 6>(wsl, bsl, tid, k16, nk16); break;
+          case 2: tc_expand_stage<NR, 2, W4A8>(wsl, bsl, tid, k16, nk16); break;
+          case 3: tc_expand_stage<NR, 3, W4A8>(wsl, bsl, tid, k16, nk16); break;
+          case 4: tc_expand_stage<NR, 4, W4A8>(wsl, bsl, tid, k16, nk16); break;
+          case 5: tc_expand_stage<NR, 5, W4A8>(wsl, bsl, tid, k16, nk16); break;
+          default: tc_expand_stage<NR, 6, W4A8>(wsl, bsl, tid, k16, nk16); break;
         }
       }
       fence_proxy_async();  // generic-proxy stores -> visible to the tensor core
@@ -495,7 +528,7 @@ __device__ __forceinline__ void tc_expanders(const TcArgs& args, const TcGeom<PR
   }
 }
 
-template <int PROJ, int KB, int NR>
+template <int PROJ, int KB, int NR, bool W4A8>
 __device__ __forceinline__ void tc_epilogue(const TcArgs& args, const TcGeom<PROJ, NR>& G, volatile int* uring, TcBars& B,
                                             float* ev, uint32_t tmem, volatile int* abort) {
   const FcArgs& a = args.f;
@@ -548,7 +581,7 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& args, const TcGeom<PRO
       // a lane quarter without valid routes has nothing to store (both warps
       // of the pair see the same lanes, so they skip together)
       if (__any_sync(0xFFFFFFFFu, route >= 0)) {
-        const bool done = (PROJ == 1) ? tc_epi_fc1<NR / 2>(a, ev, mb, slot0 + n, route >= 0, taddr, h, ps, abort)
+        const bool done = (PROJ == 1) ? tc_epi_fc1<NR / 2, W4A8>(a, ev, mb, slot0 + n, route >= 0, taddr, h, ps, abort)
                                       : tc_epi_fc2<NR>(a, ev, mb, slot0 + n, route, route >= 0, taddr, h, ps, abort);
         if (!done) return;
       }
@@ -708,7 +741,7 @@ __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.a
 template <int N>
 __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N)); }
 
-template <int PROJ, int KB, int NR>
+template <int PROJ, int KB, int NR, bool W4A8>
 __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__ TcArgs args) {
   extern __shared__ unsigned char tc_smem_raw[];
   __shared__ __align__(8) TcBars bars;
@@ -757,10 +790,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__
   volatile int* abort = &s_abort;
   volatile int* uring = s_uring;
   if (warp < 8) {
-    tc_expanders<PROJ, KB, NR>(args, G, uring, bars, wring, bring, abort);  // at the launch count
+    tc_expanders<PROJ, KB, NR, W4A8>(args, G, uring, bars, wring, bring, abort);  // at the launch count
   } else if (warp < 16) {
     regs_inc<kRegEpi>();
-    tc_epilogue<PROJ, KB, NR>(args, G, uring, bars, reinterpret_cast<float*>(evec + (warp - 8) * kEvecBytes), tmem, abort);
+    tc_epilogue<PROJ, KB, NR, W4A8>(args, G, uring, bars, reinterpret_cast<float*>(evec + (warp - 8) * kEvecBytes), tmem, abort);
   } else {
     regs_dec<kRegAux>();
     if (warp == 16)
@@ -777,9 +810,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-template <int PROJ, int KB, int NR>
+template <int PROJ, int KB, int NR, bool W4A8>
 static cudaError_t launch_tc_t(const TcArgs& args, int max_blocks, cudaStream_t st) {
-  auto kern = k_tc_fc<PROJ, KB, NR>;
+  auto kern = k_tc_fc<PROJ, KB, NR, W4A8>;
   constexpr int kmax = KB > 0 ? KB : 6;
   static bool attr_done = false;  // first forward call, before any capture
   if (!attr_done) {
@@ -821,7 +854,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-cudaError_t launch_tc_fc(const TcArgs& args_in, int proj, int uniform_k, int max_blocks, cudaStream_t st) {
+cudaError_t launch_tc_fc(const TcArgs& args_in, int proj, int uniform_k, bool w4a8, int max_blocks, cudaStream_t st) {
   TcArgs args = args_in;
   {
     // the activation operand [act_rows][K] fp16 in boxes of 64 columns (128
@@ -839,13 +872,16 @@ cudaError_t launch_tc_fc(const TcArgs& args_in, int proj, int uniform_k, int max
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
   const bool k4 = uniform_k == 4;
+#define TC_DISPATCH(P, N)                                                                                  \
+  return w4a8 ? (k4 ? launch_tc_t<P, 4, N, true>(args, max_blocks, st) : launch_tc_t<P, 0, N, true>(args, max_blocks, st)) \
+              : (k4 ? launch_tc_t<P, 4, N, false>(args, max_blocks, st) : launch_tc_t<P, 0, N, false>(args, max_blocks, st))
   if (proj == 1) {
-    if (args.bi == 128) return k4 ? launch_tc_t<1, 4, 256>(args, max_blocks, st) : launch_tc_t<1, 0, 256>(args, max_blocks, st);
-    return k4 ? launch_tc_t<1, 4, 128>(args, max_blocks, st) : launch_tc_t<1, 0, 128>(args, max_blocks, st);
+    if (args.bi == 128) TC_DISPATCH(1, 256);
+    TC_DISPATCH(1, 128);
   }
-  if (args.f.H % 256 == 0)
-    return k4 ? launch_tc_t<2, 4, 256>(args, max_blocks, st) : launch_tc_t<2, 0, 256>(args, max_blocks, st);
-  return k4 ? launch_tc_t<2, 4, 128>(args, max_blocks, st) : launch_tc_t<2, 0, 128>(args, max_blocks, st);
+  if (args.f.H % 256 == 0) TC_DISPATCH(2, 256);
+  TC_DISPATCH(2, 128);
+#undef TC_DISPATCH
 }
 
 }  // namespace tmoe
