@@ -51,6 +51,21 @@ WORKLOADS = {
 }
 
 
+def job_time_ms(local_ms: float, world: int) -> float:
+    """The job's timed region: the slowest rank's (every rank calls this)."""
+    if world <= 1:
+        return local_ms
+    import torch
+    t = torch.tensor([local_ms], dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(steps: int, tokens_per_step: int, world: int, total_ms: float) -> float:
+    """Whole-job tokens/s: every rank runs its own replica (weak scaling)."""
+    return round(steps * tokens_per_step * world / (total_ms / 1e3), 2)
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -214,11 +229,7 @@ def run_ours(args, rank, world):
     sampler.stop()
     if world > 1:
         torch.distributed.barrier()
-    total_ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([total_ms], dtype=torch.float64)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = job_time_ms(t0.elapsed_time(t1), world)
 
     # stage times of the event graphs replayed at the end of the timed region
     stage = {k: [] for k in ("router", "route_map", "rotate", "fc1", "fc2", "combine", "step")}
@@ -242,13 +253,19 @@ def run_ours(args, rank, world):
         fc1_bytes.append(nb)
         distinct.append(d)
     pk = peaks()
+    # DRAM bytes per launch of the dominant kernel from one ncu capture of this
+    # program (profiles/); None for workloads without a capture
+    ncu_traffic = {"decode": (32.22e6, "profiles/k_dec_fc_fc1_decode_w4a8_T8.md"),
+                   "prefill": (130.83e6, "profiles/k_tc_fc_fc1_prefill_w4a16_T2048.md")}.get(args.workload)
     if mode == "w4a8" and T <= 64:
         achieved = statistics.mean(fc1_bytes) / (stages_us["fc1"] * 1e-6) / 1e9
         roof = {"bound": "hbm", "kernel": "k_dec_fc<W4A8,FC1,K=4> (decode rows, split contraction)"
                 if R <= 1024 and R < 4 * cfg.E else "k_tc_fc<FC1,K=4,W4A8> (tcgen05)",
                 "achieved": round(achieved, 1),
                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
-                "traffic": None, "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst)",
+                "traffic": ncu_traffic[0] if ncu_traffic else None,
+                "traffic_source": ncu_traffic[1] if ncu_traffic else None,
+                "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst)",
                 "bytes_per_launch": int(statistics.mean(fc1_bytes))}
     else:
         flops = 2 * R * 2 * cfg.I * cfg.H
@@ -256,7 +273,9 @@ def run_ours(args, rank, world):
         kname = "k_tc_fc<FC1,%s> (tcgen05)" % ("W4A16" if mode == "w4a16" else "W4A8")
         roof = {"bound": "tensor", "kernel": kname, "achieved": round(achieved, 2),
                 "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4),
-                "traffic": None, "peak_source": pk["source"] + " (bf16 dense burst; fp16 runs at the bf16 rate)",
+                "traffic": ncu_traffic[0] if ncu_traffic else None,
+                "traffic_source": ncu_traffic[1] if ncu_traffic else None,
+                "peak_source": pk["source"] + " (bf16 dense burst; fp16 runs at the bf16 rate)",
                 "flops_per_launch": flops}
 
     # end to end through the host-buffer C-ABI call
@@ -286,7 +305,7 @@ def run_ours(args, rank, world):
     # decode rows: prologue, FC1, FC2 (with the combine); otherwise router, route map (1 or 3), rotate, FC1, FC2, combine
     launches_per_step = 3 if decode_path else 6 + (2 if R > 1024 else 0)
     res = {
-        "metric": METRIC, "value": round(args.steps * T * world / (total_ms / 1e3), 2), "unit": "tokens/s",
+        "metric": METRIC, "value": job_value(args.steps, T, world, total_ms), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3" if mode == "w4a8" else "f16", "data": "synthetic",

@@ -1,0 +1,51 @@
+"""The tensor-core contraction's route-block boundaries against the oracle:
+experts whose route counts sit on both sides of the one / two accumulator
+switch (128 / 129 routes) and of the 256-route block (256 / 257), so that
+blocks of one, two and several accumulators and multi-block experts all
+occur, in both modes."""
+import numpy as np
+import pytest
+
+from oracle import layer as olayer
+from tests.gpu_util import TOL, rel_row_err, small_cfg
+from trellis_quantized_moe_route_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+COUNTS = [257, 256, 129, 128, 1, 37, 60, 4]   # routes per expert (E = 8, top-2)
+
+
+def _ids_with_counts(counts):
+    """Top-2 ids whose per-expert counts are exactly `counts`: the sorted
+    label list paired with itself shifted by half (distinct experts per token
+    since no expert holds more than half of the routes)."""
+    labels = np.repeat(np.arange(len(counts), dtype=np.int32), counts)
+    R = labels.size
+    assert R % 2 == 0 and max(counts) <= R // 2
+    T = R // 2
+    ids = np.stack([labels[:T], labels[T:]], axis=1)
+    assert np.all(ids[:, 0] != ids[:, 1])
+    return ids
+
+
+@pytest.mark.parametrize("mode", ["w4a16", "w4a8"])
+def test_block_boundaries_match_oracle(mode):
+    import torch
+    from trellis_quantized_moe_route_gb300.binding import TrellisMoE
+    ids = _ids_with_counts(COUNTS)
+    T = ids.shape[0]
+    cfg = small_cfg(E=len(COUNTS), topk=2, T=T, seed=77)
+    L = synth.make_layer(cfg)
+    x_bits, _ = synth.make_tokens(cfg, T=T)
+    rng = np.random.default_rng(5)
+    w = rng.uniform(0.1, 1.0, size=ids.shape).astype(np.float32)
+    w /= w.sum(axis=1, keepdims=True)
+    moe = TrellisMoE(L, max_tokens=T)
+    x = torch.from_numpy(x_bits.view(np.int16)).cuda()
+    out = moe.forward(x, torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(), mode=mode)
+    torch.cuda.synchronize()
+    assert moe.poll_error() == 0
+    sel = np.arange(0, T, 3)          # every third token: all experts appear
+    ref = olayer.layer_forward(L, x_bits, ids, w, mode=mode, tokens=sel)
+    err = rel_row_err(out.cpu().numpy()[sel], ref)
+    assert err < TOL[mode], err
