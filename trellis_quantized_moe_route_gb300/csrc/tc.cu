@@ -59,23 +59,28 @@ static_assert(128 * (2 * kRegExp + 2 * kRegEpi + kRegAux) <= kTcThreads * kRegLa
 constexpr int kTcExp = 256;            // expander threads
 constexpr int kTcEpiWarps = 8;         // two per TMEM lane quarter, one per column half
 constexpr int kEvecBytes = 1024;       // per epilogue warp: its half of the unit's folded vectors (fp32)
+constexpr int kStageWords = 20;        // per epilogue warp: 32 rows x 16 words of output staging, stride 20 words
+constexpr int kStageBytes = 32 * kStageWords * 4;
 constexpr int kTcBN = 256;             // routes per route block
 constexpr int kTcKS = 64;              // contraction columns per stage
-constexpr int kSA = 2, kSB = 3, kSW = 4;
+constexpr int kSA = 2, kSW = 4, kSBMax = 3;
+// decoded-operand ring depth: 3 for the 4-bit payload, 2 for the general
+// case, whose larger payload slots leave no room for a third
+__host__ __device__ constexpr int tc_sb(int KB) { return KB > 0 ? 3 : 2; }
 constexpr int kABytes = 256 * 128;     // activation operand: 256 routes x 128 bytes
 constexpr int kBBytes = 256 * 128;     // decoded operand: 256 weight rows x 128 bytes
 constexpr uint64_t kTcWaitNs = 2000000000ull;
 
 // Payload of one stage: 16 tile rows x 4 tiles of 32K bytes.
-__host__ __device__ inline int tc_wslot_bytes(int kmax) { return 16 * 4 * 32 * kmax; }
+__host__ __device__ constexpr int tc_wslot_bytes(int kmax) { return 16 * 4 * 32 * kmax; }
 // Dynamic shared memory: activation ring, decoded ring, payload ring, the
-// epilogue warps' vectors (plus 1024 bytes to align the base).
-__host__ __device__ inline int tc_smem_total(int kmax) {
-  return 1024 + kSA * kABytes + kSB * kBBytes + kSW * tc_wslot_bytes(kmax) + kTcEpiWarps * kEvecBytes;
+// epilogue warps' vectors and output staging (plus 1024 bytes to align the base).
+__host__ __device__ constexpr int tc_smem_total(int kmax, int sb) {
+  return 1024 + kSA * kABytes + sb * kBBytes + kSW * tc_wslot_bytes(kmax) + kTcEpiWarps * (kEvecBytes + kStageBytes);
 }
 
 struct TcBars {
-  uint64_t fullA[kSA], emptyA[kSA], fullB[kSB], emptyB[kSB], fullW[kSW], emptyW[kSW], accFull[2], accEmpty[2];
+  uint64_t fullA[kSA], emptyA[kSA], fullB[kSBMax], emptyB[kSBMax], fullW[kSW], emptyW[kSW], accFull[2], accEmpty[2];
   uint64_t pair[4];  // epilogue warp pairs, one per TMEM lane quarter
   uint64_t fullU[4], emptyU[4];  // unit ring: the scheduler's picks, read by every role in order
 };
@@ -271,6 +276,28 @@ __device__ __forceinline__ float2 silu2(float2 g) {
   return __ffma2_rn(h, make_float2(tanh_fast(h.x), tanh_fast(h.y)), h);
 }
 
+// Coalesced row stores through the warp's staging area: lane l holds 16
+// words of row l (destination base + row_l * stride words, row_l < 0: not
+// stored); each store instruction then writes 64 contiguous bytes of 8 rows.
+// The 20-word row stride keeps the 16-byte writes conflict-free; reading rows
+// r and r + 4 in each group of 8 lanes keeps the reads conflict-free.
+__device__ __forceinline__ void stage_store16(uint32_t* stg, const uint32_t (&v)[16], uint32_t* base, size_t stride,
+                                              int row) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < 16; j += 4)
+    *reinterpret_cast<uint4*>(stg + lane * kStageWords + j) = make_uint4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 8 * i + ((lane >> 2) & 1) * 4 + (lane >> 3), qd = lane & 3;
+    const int rw = __shfl_sync(0xFFFFFFFFu, row, r);
+    const uint4 x = *reinterpret_cast<const uint4*>(stg + r * kStageWords + 4 * qd);
+    if (rw >= 0) *reinterpret_cast<uint4*>(base + (size_t)rw * stride + 4 * qd) = x;
+  }
+  __syncwarp();
+}
+
 // The two epilogue warps of a TMEM lane quarter split every block of columns
 // in halves; a rotation block wider than a half needs its last butterfly
 // level across the pair, exchanged through tensor memory around a bounded
@@ -313,7 +340,7 @@ __device__ __forceinline__ void combine_half(float2 (&w)[HF / 2], uint32_t their
 // reads from then on) and later publishes its final half there too.
 // ev (fp32, HF each): gate scale, hs * gate svh, up scale, hs * up svh * down suh.
 template <int BI, bool W4A8>
-__device__ __forceinline__ bool tc_epi_fc1(const FcArgs& a, const float* ev, int mb, int slot, bool valid,
+__device__ __forceinline__ bool tc_epi_fc1(const FcArgs& a, const float* ev, uint32_t* stg, int mb, int slot, bool valid,
                                            uint32_t tg, int h, PairSync& ps, volatile int* abort) {
   constexpr int HF = BI / 2;
   const bool xch = a.rot_b > HF;
@@ -355,7 +382,7 @@ __device__ __forceinline__ bool tc_epi_fc1(const FcArgs& a, const float* ev, int
     if (!pair_sync(ps, abort)) return false;
     combine_half<HF>(w, tg + mine, h);
   }
-  if (valid) {
+  {
     const float hs = hadamard_scale(a.rot_b);
     const float2 h2s = make_float2(hs, hs);
 #pragma unroll
@@ -379,16 +406,17 @@ __device__ __forceinline__ bool tc_epi_fc1(const FcArgs& a, const float* ev, int
         }
       }
     }
-    uint16_t* z = reinterpret_cast<uint16_t*>(a.out_act) + (size_t)slot * a.I + mb * BI + h * HF;
+    // this half of the z~ row, 32 fp16 (16 words) at a time
+    uint32_t* zb = reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(a.out_act) + mb * BI + h * HF);
 #pragma unroll
-    for (int j = 0; j < HF / 2; j += 4) {
-      uint32_t pk[4];
+    for (int c = 0; c < HF / 2; c += 16) {
+      uint32_t pk[16];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        __half2 h2 = __float22half2_rn(w[j + i]);
+      for (int i = 0; i < 16; ++i) {
+        __half2 h2 = __float22half2_rn(w[c + i]);
         pk[i] = *reinterpret_cast<uint32_t*>(&h2);
       }
-      *reinterpret_cast<uint4*>(z + 2 * j) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      stage_store16(stg, pk, zb + c, (size_t)a.I / 2, valid ? slot : -1);
     }
   }
   return true;
@@ -399,8 +427,8 @@ __device__ __forceinline__ bool tc_epi_fc1(const FcArgs& a, const float* ev, int
 // weighted atomics into the token's output row.
 // ev (fp32): per block, 64 output scales then 64 values hs * down_svh.
 template <int NR>
-__device__ __forceinline__ bool tc_epi_fc2(const FcArgs& a, const float* ev, int mb, int slot, int route, bool valid,
-                                           uint32_t tb, int h, PairSync& ps, volatile int* abort) {
+__device__ __forceinline__ bool tc_epi_fc2(const FcArgs& a, const float* ev, uint32_t* stg, int mb, int slot, int route,
+                                           bool valid, uint32_t tb, int h, PairSync& ps, volatile int* abort) {
   const float wr = (valid && a.atomic) ? a.route_w[route] : 0.0f;
   const uint32_t mine = h * 64, other = (1 - h) * 64;
 #pragma unroll 1
@@ -416,14 +444,21 @@ __device__ __forceinline__ bool tc_epi_fc2(const FcArgs& a, const float* ev, int
       combine_half<64>(w, t0 + other, h);
     }
     scale2<64>(w, ev + blk * 128 + 64);
-    if (!valid) continue;
     const int col0 = mb * NR + blk * 128 + h * 64;
     if (!a.atomic) {
-      float* o = a.out_f32 + (size_t)slot * a.H + col0;
+      // the slot's fp32 row, 16 values at a time through the staging area
+      uint32_t* ob = reinterpret_cast<uint32_t*>(a.out_f32) + col0;
 #pragma unroll
-      for (int j = 0; j < 32; j += 2)
-        *reinterpret_cast<float4*>(o + 2 * j) = make_float4(w[j].x, w[j].y, w[j + 1].x, w[j + 1].y);
-    } else {
+      for (int c = 0; c < 32; c += 8) {
+        uint32_t v16[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          v16[2 * i] = __float_as_uint(w[c + i].x);
+          v16[2 * i + 1] = __float_as_uint(w[c + i].y);
+        }
+        stage_store16(stg, v16, ob + 2 * c, (size_t)a.H, valid ? slot : -1);
+      }
+    } else if (valid) {
       float* o = a.out_f32 + (size_t)(route / a.topk) * a.H + col0;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -501,9 +536,9 @@ __device__ __forceinline__ void tc_expanders(const TcArgs& args, const TcGeom<PR
     const int rb = u / G.mblocks;
     const int K = (KB > 0) ? KB : a.bits[a.block_expert[rb]];
     for (int s = 0; s < G.nst; ++s, ++g) {
-      const int ws = g % kSW, bs = g % kSB;
+      const int ws = g % kSW, bs = g % tc_sb(KB);
       bool ok = mbar_wait_abort(&B.fullW[ws], (g / kSW) & 1, abort, kTcWaitNs);
-      if (ok && g >= kSB) ok = mbar_wait_abort(&B.emptyB[bs], ((g / kSB) - 1) & 1, abort, kTcWaitNs);
+      if (ok && g >= tc_sb(KB)) ok = mbar_wait_abort(&B.emptyB[bs], ((g / tc_sb(KB)) - 1) & 1, abort, kTcWaitNs);
       if (!__all_sync(0xFFFFFFFFu, ok)) return;
       const unsigned char* wsl = wring + ws * wsz;
       unsigned char* bsl = bring + bs * kBBytes;
@@ -530,7 +565,7 @@ __device__ __forceinline__ void tc_expanders(const TcArgs& args, const TcGeom<PR
 
 template <int PROJ, int KB, int NR, bool W4A8>
 __device__ __forceinline__ void tc_epilogue(const TcArgs& args, const TcGeom<PROJ, NR>& G, volatile int* uring, TcBars& B,
-                                            float* ev, uint32_t tmem, volatile int* abort) {
+                                            float* ev, uint32_t* stg, uint32_t tmem, volatile int* abort) {
   const FcArgs& a = args.f;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;           // TMEM lane quarter
@@ -581,8 +616,9 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& args, const TcGeom<PRO
       // a lane quarter without valid routes has nothing to store (both warps
       // of the pair see the same lanes, so they skip together)
       if (__any_sync(0xFFFFFFFFu, route >= 0)) {
-        const bool done = (PROJ == 1) ? tc_epi_fc1<NR / 2, W4A8>(a, ev, mb, slot0 + n, route >= 0, taddr, h, ps, abort)
-                                      : tc_epi_fc2<NR>(a, ev, mb, slot0 + n, route, route >= 0, taddr, h, ps, abort);
+        const bool done = (PROJ == 1)
+                              ? tc_epi_fc1<NR / 2, W4A8>(a, ev, stg, mb, slot0 + n, route >= 0, taddr, h, ps, abort)
+                              : tc_epi_fc2<NR>(a, ev, stg, mb, slot0 + n, route, route >= 0, taddr, h, ps, abort);
         if (!done) return;
       }
       tc_fence_before();
@@ -705,9 +741,9 @@ __device__ __forceinline__ void tc_issuer(const TcArgs& args, const TcGeom<PROJ,
     tc_fence_after();
     const uint32_t d0 = tmem + (uint32_t)(plan.buf(macc, 0) * 256);
     for (int s = 0; s < G.nst; ++s, ++g) {
-      const int as = g % kSA, bs = g % kSB;
+      const int as = g % kSA, bs = g % tc_sb(KB);
       if (!mbar_wait_abort(&B.fullA[as], (g / kSA) & 1, abort, kTcWaitNs) ||
-          !mbar_wait_abort(&B.fullB[bs], (g / kSB) & 1, abort, kTcWaitNs)) {
+          !mbar_wait_abort(&B.fullB[bs], (g / tc_sb(KB)) & 1, abort, kTcWaitNs)) {
         ok = false;
         break;
       }
@@ -733,7 +769,7 @@ __device__ __forceinline__ void tc_issuer(const TcArgs& args, const TcGeom<PROJ,
     }
     plan.advance(macc);
   }
-  if (*abort && glast >= 0) mbar_wait_drain(&B.emptyB[glast % kSB], (glast / kSB) & 1);
+  if (*abort && glast >= 0) mbar_wait_drain(&B.emptyB[glast % tc_sb(KB)], (glast / tc_sb(KB)) & 1);
 }
 
 template <int N>
@@ -749,10 +785,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__
   __shared__ int s_abort;
   __shared__ int s_uring[kUnitRing];
   constexpr int kmax = KB > 0 ? KB : 6;
+  static_assert(tc_smem_total(kmax, tc_sb(KB)) + 1024 <= 232448, "dynamic + static shared memory over the per-block limit");
   unsigned char* smem = tc_smem_raw + ((1024u - (smem_u32(tc_smem_raw) & 1023u)) & 1023u);
   unsigned char* aring = smem;
   unsigned char* bring = aring + kSA * kABytes;
-  unsigned char* wring = bring + kSB * kBBytes;
+  unsigned char* wring = bring + tc_sb(KB) * kBBytes;
   unsigned char* evec = wring + kSW * tc_wslot_bytes(kmax);
   const int tid = threadIdx.x, warp = tid >> 5;
   const TcGeom<PROJ, NR> G(args);
@@ -762,7 +799,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__
       mbar_init(&bars.fullA[i], 1);   // the loader's expect_tx arrival; the gathers complete the bytes
       mbar_init(&bars.emptyA[i], 1);
     }
-    for (int i = 0; i < kSB; ++i) {
+    for (int i = 0; i < tc_sb(KB); ++i) {
       mbar_init(&bars.fullB[i], kTcExp / 32);
       mbar_init(&bars.emptyB[i], 1);
     }
@@ -793,7 +830,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__
     tc_expanders<PROJ, KB, NR, W4A8>(args, G, uring, bars, wring, bring, abort);  // at the launch count
   } else if (warp < 16) {
     regs_inc<kRegEpi>();
-    tc_epilogue<PROJ, KB, NR, W4A8>(args, G, uring, bars, reinterpret_cast<float*>(evec + (warp - 8) * kEvecBytes), tmem, abort);
+    tc_epilogue<PROJ, KB, NR, W4A8>(args, G, uring, bars, reinterpret_cast<float*>(evec + (warp - 8) * kEvecBytes),
+                                    reinterpret_cast<uint32_t*>(evec + kTcEpiWarps * kEvecBytes + (warp - 8) * kStageBytes),
+                                    tmem, abort);
   } else {
     regs_dec<kRegAux>();
     if (warp == 16)
@@ -814,13 +853,14 @@ template <int PROJ, int KB, int NR, bool W4A8>
 static cudaError_t launch_tc_t(const TcArgs& args, int max_blocks, cudaStream_t st) {
   auto kern = k_tc_fc<PROJ, KB, NR, W4A8>;
   constexpr int kmax = KB > 0 ? KB : 6;
+  static_assert(tc_smem_total(kmax, tc_sb(KB)) + 1024 <= 232448, "dynamic + static shared memory over the per-block limit");
   static bool attr_done = false;  // first forward call, before any capture
   if (!attr_done) {
     cudaFuncAttributes fa;
     cudaError_t err = cudaFuncGetAttributes(&fa, kern);
     if (err != cudaSuccess) return err;
     if (fa.numRegs != kRegLaunch) return cudaErrorInvalidConfiguration;  // the register split assumes 128
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_smem_total(kmax));
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_smem_total(kmax, tc_sb(KB)));
     if (err != cudaSuccess) return err;
     attr_done = true;
   }
@@ -831,7 +871,7 @@ static cudaError_t launch_tc_t(const TcArgs& args, int max_blocks, cudaStream_t 
   const int mblocks = (PROJ == 1) ? args.f.I / args.bi : args.f.H / NR;
   const long units = (long)max_blocks * mblocks;
   const int grid = (int)std::max<long>(1, std::min<long>(units, sms));
-  kern<<<grid, kTcThreads, tc_smem_total(kmax), st>>>(args);
+  kern<<<grid, kTcThreads, tc_smem_total(kmax, tc_sb(KB)), st>>>(args);
   return cudaGetLastError();
 }
 
