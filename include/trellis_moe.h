@@ -22,7 +22,8 @@
  *   5. fused epilogue: H -> svh -> SiLU(gate)*up -> suh_down -> H (sparkinfer
  *      PR #90, review of kernel.py: _run_activation);
  *   6. FC2 route-major grouped GEMM with the same decode, then the output
- *      rotation is undone (H, down_svh);
+ *      rotation is undone (output scale, H, down_svh; with the tensor-core
+ *      FC2 these per-route steps run inside the deterministic combine);
  *   7. top-k weighted combine into an FP32 output, in fixed slot order
  *      (deterministic) or by FP32 atomics (opt-in, not bitwise reproducible:
  *      b12x PR #433, conversation: "does not guarantee bitwise summation
@@ -164,7 +165,9 @@ tm_status trellis_moe_decode_tiles(tm_layer* layer, int32_t proj, int32_t expert
 /* Where a forward call of `T` tokens keeps its intermediates inside the
  * workspace (for tests): which = 0 x~ (fp16 or E4M3), 1 x~ E8M0 exponents,
  * 2 FC1 epilogue output z~ (fp16 or E4M3), 3 z~ E8M0 exponents, 4 per-slot
- * FC2 output (fp32 [slots, H]), 5 slot_of_route (int32 [T*topk]),
+ * FC2 output (fp32 [slots, H]: the unrotated route output, or, for the
+ * tensor-core FC2 with the deterministic combine, the bare FC2 accumulator
+ * before output scale, H and down_svh), 5 slot_of_route (int32 [T*topk]),
  * 6 device error word (uint32). Returns TM_EINVAL for an unknown `which`. */
 tm_status trellis_moe_workspace_region(const tm_layer* layer, int32_t T, int32_t which,
                                        size_t* offset, size_t* bytes);

@@ -181,6 +181,8 @@ def test_tiny_config(mode):
     dict(rot_block_h=1, rot_block_i=1),                         # identity rotations
     dict(bits=(5, 6), E=8, topk=3),                             # wider codes
     dict(T=200, E=8, topk=2),                                   # several 64-route blocks per expert
+    dict(H=384),                                                # H % 256 == 128: 128-column FC2 blocks
+    dict(rot_block_h=64),                                       # 64-wide H blocks: no level across halves
 ])
 def test_small_layers(mode, kw):
     cfg = small_cfg(**kw)

@@ -270,6 +270,8 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
   a2.out_scale = nullptr;
   a2.route_w = w;
   a2.atomic = d.deterministic ? 0 : 1;
+  // the tensor-core FC2 leaves the route's output scale, H and down_svh to the combine
+  a2.raw_rows = (use_tc && !a2.atomic && d.topk <= 32) ? 1 : 0;
   if (a2.atomic) {
     if ((e = cudaMemsetAsync(out, 0, (size_t)T * d.H * 4, st)) != cudaSuccess) return cuda_fail(e, "clear output");
     a2.out_f32 = out;
@@ -288,7 +290,11 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
     e = tmoe::launch_fc2(a2, w4a8, bn, layer->uniform_k, max_blocks, st);
   if (e != cudaSuccess) return cuda_fail(e, "FC2");
   if ((e = stage_mark(layer, 5, st)) != cudaSuccess) return cuda_fail(e, "stage event");
-  if (!a2.atomic) {
+  if (a2.raw_rows) {
+    tmoe::CombineUnrotArgs c{a2.out_f32, rm.slot_of_route, rm.block_expert, bn, w, d.out_svh,
+                             d.rot_block_h, T, d.H, d.topk, out};
+    if ((e = tmoe::launch_combine_unrot(c, st)) != cudaSuccess) return cuda_fail(e, "combine");
+  } else if (!a2.atomic) {
     if ((e = tmoe::launch_combine(a2.out_f32, rm.slot_of_route, w, T, d.H, d.topk, out, st)) != cudaSuccess)
       return cuda_fail(e, "combine");
   }

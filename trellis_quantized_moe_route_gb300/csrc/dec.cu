@@ -310,17 +310,30 @@ __device__ __forceinline__ void dec_body(const DecArgs& d, int rb, int mb, int p
   {
     const unsigned char* act = reinterpret_cast<const unsigned char*>(a.act);
     if (W4A8) {
-      // E4M3 codes, widened to fp16 on the way into shared memory
+      // E4M3 codes, widened to fp16 on the way into shared memory; four
+      // loads per thread are in flight before the first is used
       const int vec = ncols >> 2;  // 4 codes per step
-      for (int i = tid; i < kDecBN * vec; i += kDecThreads) {
-        const int rr = i / vec, v = i % vec;
-        const int src = row_src[rr];
-        uint32_t codes = 0;
-        if (src >= 0) codes = __ldg(reinterpret_cast<const uint32_t*>(act + (size_t)src * KDIM + col0) + v);
-        uint2 hv;
-        hv.x = e4m3x2_to_f16x2(codes & 0xFFFFu);
-        hv.y = e4m3x2_to_f16x2(codes >> 16);
-        *reinterpret_cast<uint2*>(act_s + rr * sp.arow + v * 8) = hv;
+      for (int i0 = tid; i0 < kDecBN * vec; i0 += 4 * kDecThreads) {
+        uint32_t codes[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u * kDecThreads;
+          codes[u] = 0;
+          if (i < kDecBN * vec) {
+            const int src = row_src[i / vec];
+            if (src >= 0) codes[u] = __ldg(reinterpret_cast<const uint32_t*>(act + (size_t)src * KDIM + col0) + i % vec);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u * kDecThreads;
+          if (i < kDecBN * vec) {
+            uint2 hv;
+            hv.x = e4m3x2_to_f16x2(codes[u] & 0xFFFFu);
+            hv.y = e4m3x2_to_f16x2(codes[u] >> 16);
+            *reinterpret_cast<uint2*>(act_s + (i / vec) * sp.arow + (i % vec) * 8) = hv;
+          }
+        }
       }
     } else {
       const int vec = (2 * ncols) >> 4;
@@ -445,12 +458,28 @@ __device__ __forceinline__ void dec_body(const DecArgs& d, int rb, int mb, int p
   float* C = reinterpret_cast<float*>(wring);
   constexpr int CS = kDecBN + 1;
   const float* ubase = d.partial + (size_t)unit * d.ksplit * U * kDecBN;
-  for (int i = tid; i < U * kDecBN; i += kDecThreads) {
-    const int r = i / kDecBN, n = i % kDecBN;
-    float v = 0.0f;
-    if (n < nvalid)
-      for (int s2 = 0; s2 < d.ksplit; ++s2) v += __ldcg(ubase + ((size_t)s2 * U + r) * kDecBN + n);
-    C[r * CS + n] = v;
+  // (U * kDecBN / kDecThreads <= 8 values per thread; each split's loads
+  // are all in flight before they are added, in split order)
+  {
+    constexpr int kPer = 2 * 128 * kDecBN / kDecThreads;
+    float v[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) v[j] = 0.0f;
+    for (int s2 = 0; s2 < d.ksplit; ++s2) {
+      float x[kPer];
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int i = tid + j * kDecThreads;
+        x[j] = (i < U * kDecBN && (i % kDecBN) < nvalid) ? __ldcg(ubase + (size_t)s2 * U * kDecBN + i) : 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) v[j] += x[j];
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = tid + j * kDecThreads;
+      if (i < U * kDecBN) C[(i / kDecBN) * CS + (i % kDecBN)] = v[j];
+    }
   }
   __syncthreads();
   if (tid == 0) d.unit_cnt[unit] = 0;

@@ -44,6 +44,7 @@ struct FcArgs {
   float* out_f32;             // FC2: per-slot rows [slots, H], or out [T, H] when atomic
   const float* route_w;       // FC2 atomic: route weights [T*topk]
   int atomic;
+  int raw_rows;               // FC2 (tensor-core kernel, not atomic): rows leave the last Hadamard level and down_svh to the combine
 };
 
 // Decode-rows path (few tokens): one fused prologue, then FC1 and FC2 as
@@ -115,6 +116,17 @@ cudaError_t launch_rotate_quant(const uint16_t* x, const uint16_t* suh, int T, i
 cudaError_t launch_fc1(const FcArgs& a, bool w4a8, int bi, int bn, int uniform_k, int max_blocks, cudaStream_t st);
 cudaError_t launch_fc2(const FcArgs& a, bool w4a8, int bn, int uniform_k, int max_blocks, cudaStream_t st);
 
+struct CombineUnrotArgs {
+  const float* rows;            // [slots, H]: per 128-column block, (I_2 x H_64)(scale * FC2 accumulator)
+  const int32_t* slot_of_route; // [T*k]
+  const int32_t* block_expert;  // expert of each block of bn slots
+  int bn;
+  const float* w;               // route weights [T*k]
+  const uint16_t* svh;          // fp16 down_svh [E, H]
+  int rot_b, T, H, k;
+  float* out;                   // [T, H]
+};
+cudaError_t launch_combine_unrot(const CombineUnrotArgs& a, cudaStream_t st);
 cudaError_t launch_combine(const float* rows, const int32_t* slot_of_route, const float* w, int T, int H, int k,
                            float* out, cudaStream_t st);
 

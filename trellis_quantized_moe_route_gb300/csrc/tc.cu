@@ -423,14 +423,39 @@ __device__ __forceinline__ bool tc_epi_fc1(const FcArgs& a, const float* ev, uin
 }
 
 // FC2, half h of each 128-column block of the route's NR output columns:
-// scale, H, hs * down_svh, then the fp32 row of the slot (deterministic) or
-// weighted atomics into the token's output row.
+// scale and the Hadamard levels within the half into the slot's fp32 row
+// (raw_rows: the combine finishes the route), or scale, H, hs * down_svh,
+// then the fp32 row of the slot or weighted atomics into the token's output row.
 // ev (fp32): per block, 64 output scales then 64 values hs * down_svh.
 template <int NR>
 __device__ __forceinline__ bool tc_epi_fc2(const FcArgs& a, const float* ev, uint32_t* stg, int mb, int slot, int route,
                                            bool valid, uint32_t tb, int h, PairSync& ps, volatile int* abort) {
   const float wr = (valid && a.atomic) ? a.route_w[route] : 0.0f;
   const uint32_t mine = h * 64, other = (1 - h) * 64;
+  if (a.raw_rows) {
+    // this half of each 128-column block: scale, then the Hadamard levels
+    // inside the half (all of them for blocks of 64); the combine applies the
+    // level across halves and hs * down_svh
+#pragma unroll 1
+    for (int blk = 0; blk < NR / 128; ++blk) {
+      float2 w[32];
+      ld_cols2<64>(tb + blk * 128 + mine, w);
+      scale2<64>(w, ev + blk * 128);
+      fwht2<64>(w, a.rot_b > 64 ? 64 : a.rot_b);
+      uint32_t* ob = reinterpret_cast<uint32_t*>(a.out_f32) + mb * NR + blk * 128 + h * 64;
+#pragma unroll
+      for (int c = 0; c < 32; c += 8) {
+        uint32_t v16[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          v16[2 * i] = __float_as_uint(w[c + i].x);
+          v16[2 * i + 1] = __float_as_uint(w[c + i].y);
+        }
+        stage_store16(stg, v16, ob + 2 * c, (size_t)a.H, valid ? slot : -1);
+      }
+    }
+    return true;
+  }
 #pragma unroll 1
   for (int blk = 0; blk < NR / 128; ++blk) {
     const uint32_t t0 = tb + blk * 128;
