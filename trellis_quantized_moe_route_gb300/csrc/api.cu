@@ -68,7 +68,7 @@ int fc1_bi(const tm_layer_desc& d) {
 // 4 routes on average (route blocks of 8).
 struct DecPlan {
   bool use;
-  int max_blocks, bi, units1, parts1, units2, s1, k1, s2, k2;
+  int max_blocks, bi, units1, units2, nseg1, nseg2;
   size_t partial_floats, cnt_ints;
 };
 
@@ -78,19 +78,13 @@ DecPlan dec_plan(const tm_layer_desc& d, int T) {
   p.use = R >= 1 && R <= 1024 && R < 4L * d.E;
   p.bi = fc1_bi(d);
   p.units1 = d.I / p.bi;
-  p.parts1 = 2 * p.bi / 128;
   p.units2 = d.H / 128;
-  p.max_blocks = (int)(R / 8 + std::min<long>(d.E, R) + 1);
-  const long active = std::max<long>(1, std::min<long>(d.E, R));
-  auto split = [](int kdim, int s, int& kc) {
-    kc = ((kdim + s - 1) / s + 63) / 64 * 64;
-    return (kdim + kc - 1) / kc;
-  };
-  p.s1 = split(d.H, tmoe::dec_ksplit(d.H, active * p.units1 * p.parts1), p.k1);
-  p.s2 = split(d.I, tmoe::dec_ksplit(d.I, active * p.units2), p.k2);
-  p.partial_floats = (size_t)p.max_blocks *
-                     std::max<size_t>((size_t)p.units1 * p.s1 * 2 * p.bi, (size_t)p.units2 * p.s2 * 128) * 8;
-  p.cnt_ints = (size_t)p.max_blocks * (p.units1 + p.units2) + (size_t)T * p.units2;
+  p.max_blocks = (int)(R / tmoe::kDecBlock + std::min<long>(d.E, R) + 1);
+  p.nseg1 = (d.H + tmoe::kDecSeg - 1) / tmoe::kDecSeg;
+  p.nseg2 = (d.I + tmoe::kDecSeg - 1) / tmoe::kDecSeg;
+  // per (block, segment, 16-row strip): 8 x 16 partial sums
+  p.partial_floats = (size_t)p.max_blocks * std::max<size_t>((size_t)p.nseg1 * (2 * d.I / 16), (size_t)p.nseg2 * (d.H / 16)) * 128;
+  p.cnt_ints = 0;  // (no counters: every reduction runs in a kernel of its own)
   if (!p.use) p.partial_floats = p.cnt_ints = 0;
   return p;
 }
@@ -100,7 +94,7 @@ struct Layout {
   enum {
     ERR, XQ, XS, ZQ, ZS, ROWS, SLOT_OF_ROUTE,
     IDS, W, RANK, TILE_COUNTS, COUNTS, OFFSETS, BLOCK_EXPERT, NBLOCKS, ROUTE_OF_SLOT,
-    HOST_X, HOST_LOGITS, HOST_OUT, DEC_PARTIAL, DEC_CNT, COUNT
+    HOST_X, HOST_LOGITS, HOST_OUT, DEC_PARTIAL, DEC_CNT, DEC_META, COUNT
   };
   size_t off[COUNT];
   size_t bytes[COUNT];
@@ -134,14 +128,16 @@ Layout make_layout(const tm_layer_desc& d, int T) {
   // The decode path's scratch is not monotonic in T (larger T switches to the
   // general path), so size it for the worst T' <= T: a workspace that fits T
   // then fits every smaller call too.
-  size_t dec_partial = 0, dec_cnt = 0;
+  size_t dec_partial = 0, dec_cnt = 0, dec_blocks = 0;
   for (int t = 1; t <= T && (long)t * d.topk <= 1024; ++t) {
     const DecPlan dp = dec_plan(d, t);
     dec_partial = std::max(dec_partial, dp.partial_floats);
     dec_cnt = std::max(dec_cnt, dp.cnt_ints);
+    if (dp.use) dec_blocks = std::max(dec_blocks, (size_t)dp.max_blocks);
   }
   L.bytes[Layout::DEC_PARTIAL] = dec_partial * 4;
   L.bytes[Layout::DEC_CNT] = dec_cnt * 4;
+  L.bytes[Layout::DEC_META] = dec_blocks * (8 + 8 + 8);  // int64 FC1 and FC2 offsets, then int32 metadata
   size_t o = 0;
   for (int i = 0; i < Layout::COUNT; ++i) {
     L.off[i] = o;
@@ -315,7 +311,7 @@ tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids
   pa.rm.ids = ids;
   pa.rm.R = R;
   pa.rm.E = d.E;
-  pa.rm.block = 8;
+  pa.rm.block = tmoe::kDecBlock;
   pa.rm.rank = at<int32_t>(ws, L, Layout::RANK);
   pa.rm.tile_counts = at<int32_t>(ws, L, Layout::TILE_COUNTS);
   pa.rm.counts = at<int32_t>(ws, L, Layout::COUNTS);
@@ -337,7 +333,14 @@ tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids
   pa.zero_i32 = at<int32_t>(ws, L, Layout::DEC_CNT);
   pa.n_zero_i32 = (int)dp.cnt_ints;
   pa.out = out;
-  pa.out_n = (long)T * d.H;
+  pa.out_n = 0;  // (the FC2 epilogue writes every output row)
+  pa.word_off1 = layer->d_off1;
+  pa.word_off2 = layer->d_off2;
+  pa.bits = layer->d_bits;
+  pa.max_blocks = dp.max_blocks;
+  pa.blk_off1 = at<long long>(ws, L, Layout::DEC_META);
+  pa.blk_off2 = pa.blk_off1 + dp.max_blocks;
+  pa.blk_meta = reinterpret_cast<int32_t*>(pa.blk_off2 + dp.max_blocks);
   if ((e = tmoe::launch_dec_prologue(pa, st)) != cudaSuccess) return cuda_fail(e, "decode prologue");
   for (int i = 1; i <= 3; ++i)
     if ((e = stage_mark(layer, i, st)) != cudaSuccess) return cuda_fail(e, "stage event");
@@ -360,20 +363,24 @@ tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids
   a1.out_scale = at<uint8_t>(ws, L, Layout::ZS);
   a1.route_w = w;
   a1.atomic = d.deterministic ? 0 : 1;
-  d1.ksplit = dp.s1;
-  d1.kchunk = dp.k1;
-  d1.parts = dp.parts1;
+  d1.nseg = dp.nseg1;
   d1.units_m = dp.units1;
   d1.bi = dp.bi;
   d1.partial = at<float>(ws, L, Layout::DEC_PARTIAL);
-  d1.unit_cnt = pa.zero_i32;
-  d1.tok_cnt = nullptr;
+  d1.ids = pa.rm.ids;
+  d1.blk_meta = pa.blk_meta;
+  d1.blk_off = pa.blk_off1;
   d1.slot_of_route = pa.rm.slot_of_route;
   d1.route_w = w;
   d1.out = out;
   d1.T = T;
-  if ((e = tmoe::launch_dec_fc(d1, 1, w4a8, layer->uniform_k, dp.max_blocks, st)) != cudaSuccess)
+  d1.max_blocks = dp.max_blocks;
+  if ((e = tmoe::dec_fc_warps(1, w4a8, layer->uniform_k, &d1.fc_warps)) != cudaSuccess)
+    return cuda_fail(e, "FC1 (decode rows) setup");
+  if ((e = tmoe::launch_dec_fc(d1, 1, w4a8, layer->uniform_k, st)) != cudaSuccess)
     return cuda_fail(e, "FC1 (decode rows)");
+  if ((e = tmoe::launch_dec_epilogue(d1, 1, w4a8, st)) != cudaSuccess)
+    return cuda_fail(e, "FC1 epilogue (decode rows)");
   if ((e = stage_mark(layer, 4, st)) != cudaSuccess) return cuda_fail(e, "stage event");
 
   tmoe::DecArgs d2 = d1;
@@ -388,14 +395,15 @@ tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids
   a2.out_act = nullptr;
   a2.out_scale = nullptr;
   a2.out_f32 = at<float>(ws, L, Layout::ROWS);
-  d2.ksplit = dp.s2;
-  d2.kchunk = dp.k2;
-  d2.parts = 1;
+  d2.nseg = dp.nseg2;
   d2.units_m = dp.units2;
-  d2.unit_cnt = pa.zero_i32 + (size_t)dp.max_blocks * dp.units1;
-  d2.tok_cnt = pa.zero_i32 + (size_t)dp.max_blocks * (dp.units1 + dp.units2);
-  if ((e = tmoe::launch_dec_fc(d2, 2, w4a8, layer->uniform_k, dp.max_blocks, st)) != cudaSuccess)
+  d2.blk_off = pa.blk_off2;
+  if ((e = tmoe::dec_fc_warps(2, w4a8, layer->uniform_k, &d2.fc_warps)) != cudaSuccess)
+    return cuda_fail(e, "FC2 (decode rows) setup");
+  if ((e = tmoe::launch_dec_fc(d2, 2, w4a8, layer->uniform_k, st)) != cudaSuccess)
     return cuda_fail(e, "FC2 (decode rows)");
+  if ((e = tmoe::launch_dec_epilogue(d2, 2, w4a8, st)) != cudaSuccess)
+    return cuda_fail(e, "FC2 epilogue (decode rows)");
   for (int i = 5; i <= 6; ++i)
     if ((e = stage_mark(layer, i, st)) != cudaSuccess) return cuda_fail(e, "stage event");
   return TM_OK;

@@ -1,0 +1,685 @@
+// Decode-rows FC1 / FC2 (sm_103a): persistent, warp-granular kernels for the
+// few-token regime, where every touched expert serves a handful of routes and
+// the layer is bound by expanding the touched trellis payload (b12x PR #129
+// "feat(moe): serve canonical Fruit QSRT atoms", Hot path: W4A8 only for
+// bounded decode rows; the payload is expanded straight into MMA operands).
+//
+// Work item = (route block rb of 8 slots, 16-row strip, 256-column segment).
+// Warp w of the grid takes items w, w + W, w + 2W, ... (W warps in all; items
+// cost the same, so no claiming is needed). It copies each item's 16 payload
+// tiles (one K-bit trellis tile holds 16x16 weights) into a private two-slot
+// shared ring with cp.async -- the copy of the next item overlaps the
+// expansion of this one -- expands the tiles in registers into fp16 mma.sync
+// operands and multiplies them with the block's activation fragments, read
+// straight from L2. W4A8: weights are rounded to E4M3 and activations are
+// E4M3 codes held exactly in fp16, so each 32-column MMA result is exact up
+// to summation order and is scaled by the route's E8M0 block exponent
+// (mma.sync of E4M3 operands is not a native tensor instruction on sm_103).
+// The 16x8 partial sums of an item go to the workspace.
+//
+// The epilogue kernels that follow run one warp per (epilogue unit, slot):
+// the unit's partials summed in segment order (deterministic), then FC1 the
+// activation H -> svh -> SiLU(gate)*up -> suh_down -> H into z~ (sparkinfer
+// PR #90, review of kernel.py: _run_activation), FC2 the unrotation (H,
+// down_svh) and, for the route completing a (token, 128 columns) block, the
+// top-k combine in slot order. No warp waits on another.
+#include <algorithm>
+
+#include "launch.h"
+
+namespace tmoe {
+
+constexpr int kDwThreads = 128;          // four independent warps
+constexpr int kDwWarps = kDwThreads / 32;
+constexpr int kDwSteps = kDecSeg / 32;   // k-steps (two tiles each) per item
+constexpr int kDwTiles = kDecSeg / 16;   // payload tiles per item
+constexpr int kDwRing = 2;
+
+__device__ __forceinline__ void dw_griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void dw_griddep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+// Per-warp metadata of one route block: lanes 0..7 load the slots' routes,
+// lane 8 the block's expert | bits << 16 | valid slots << 24, lane 9 the byte
+// offset of the expert's payload; dw_meta_final broadcasts them. Issued two
+// items ahead of use so that the loads overlap an item's expansion.
+struct DwRaw {
+  int v;
+  long long o;
+};
+struct DwMetaW {
+  int row;  // lane n < 8: activation row of slot n (FC1 token, FC2 slot), -1 if empty
+  int ek;
+  long long off;
+};
+
+__device__ __forceinline__ DwRaw dw_meta_issue(const DecArgs& d, int rb, int lane) {
+  DwRaw r{-1, 0};
+  if (lane < kDecBlock)
+    r.v = d.f.route_of_slot[rb * kDecBlock + lane];
+  else if (lane == kDecBlock)
+    r.v = d.blk_meta[rb];
+  else if (lane == kDecBlock + 1)
+    r.o = d.blk_off[rb];
+  return r;
+}
+
+template <int PROJ>
+__device__ __forceinline__ DwMetaW dw_meta_final(const DwRaw& r, int rb, int lane, int topk) {
+  DwMetaW m;
+  m.ek = __shfl_sync(0xFFFFFFFFu, r.v, kDecBlock);
+  m.off = __shfl_sync(0xFFFFFFFFu, r.o, kDecBlock + 1);
+  m.row = (lane < kDecBlock && r.v >= 0) ? ((PROJ == 1) ? r.v / topk : rb * kDecBlock + lane) : -1;
+  return m;
+}
+
+__host__ __device__ inline int dw_slot_bytes(int kmax) { return kDwTiles * 32 * kmax; }
+__host__ __device__ inline int dw_smem_bytes(int kmax) { return kDwWarps * kDwRing * dw_slot_bytes(kmax); }
+
+// Window of a run for any K, read from shared memory: the 64 stream bits
+// starting at the word holding bit q0 = (j0+1)K-16 (mod 256K), and the bit
+// offset of state j0 inside them.
+template <int K>
+__device__ __forceinline__ void dw_window(const uint16_t* tile, int j0, uint32_t& hi, uint32_t& lo, int& off) {
+  constexpr int NB = 256 * K;
+  constexpr int NW = 16 * K;
+  int q0 = (j0 + 1) * K - 16;
+  if (q0 < 0) q0 += NB;
+  const int w = q0 >> 4;
+  off = q0 & 15;
+  const uint32_t w0 = tile[w], w1 = tile[(w + 1) % NW], w2 = tile[(w + 2) % NW], w3 = tile[(w + 3) % NW];
+  hi = (w0 << 16) | w1;
+  lo = (w2 << 16) | w3;
+}
+
+// An item's payload tiles (32K bytes each) into a ring slot, one cp.async
+// group per item. K = 4: the 64-byte halves of odd tiles are swapped so that
+// the two tiles a warp reads in one k-step fall on different banks.
+template <int K>
+__device__ __forceinline__ void dw_copy(unsigned char* dst, const unsigned char* src, int ntiles, int lane) {
+  const int chunks = ntiles * 2 * K;
+  for (int c = lane; c < chunks; c += 32) {
+    int off = c * 16;
+    if (K == 4) {
+      const int t = c >> 3, cc = c & 7;
+      off = t * 128 + ((cc ^ ((t & 1) << 2)) << 4);
+    }
+    cp_async16(dst + off, src + (size_t)c * 16, 16);
+  }
+}
+
+__device__ __forceinline__ void dw_copy_any(int k, unsigned char* dst, const unsigned char* src, int ntiles, int lane) {
+  switch (k) {
+    case 2: dw_copy<2>(dst, src, ntiles, lane); break;
+    case 3: dw_copy<3>(dst, src, ntiles, lane); break;
+    case 4: dw_copy<4>(dst, src, ntiles, lane); break;
+    case 5: dw_copy<5>(dst, src, ntiles, lane); break;
+    default: dw_copy<6>(dst, src, ntiles, lane); break;
+  }
+}
+
+// Item geometry shared by the copy and the compute.
+struct DwItem {
+  int rb, sg, strip;
+  int e, k, nvalid;
+  int ncols;  // columns of this segment (a multiple of 32)
+};
+
+__device__ __forceinline__ DwItem dw_item(const DecArgs& d, uint32_t id, uint32_t nstrips, int kdim) {
+  DwItem it;
+  const uint32_t t = id / nstrips;
+  it.strip = (int)(id - t * nstrips);
+  const uint32_t rb = t / (uint32_t)d.nseg;
+  it.sg = (int)(t - rb * (uint32_t)d.nseg);
+  it.rb = (int)rb;
+  it.ncols = min(kDecSeg, kdim - it.sg * kDecSeg);
+  return it;
+}
+
+__device__ __forceinline__ void dw_item_meta(DwItem& it, const DwMetaW& m) {
+  it.e = m.ek & 0xFFFF;
+  it.k = (m.ek >> 16) & 0xFF;
+  it.nvalid = m.ek >> 24;
+}
+
+__device__ __forceinline__ const unsigned char* dw_src(const DecArgs& d, const DwMetaW& m, const DwItem& it, int kdim) {
+  const int tiles_k = kdim >> 4;
+  return reinterpret_cast<const unsigned char*>(d.f.payload) + m.off +
+         ((size_t)it.strip * tiles_k + (size_t)it.sg * kDwTiles) * 32 * it.k;
+}
+
+// Expansion and MMAs of one item: acc (this lane's D fragment, rows g, g+8 of
+// the strip, slots 2q, 2q+1) over the item's k-steps.
+template <bool W4A8, int K>
+__device__ __forceinline__ void dw_compute(const DecArgs& d, const DwItem& it, int row,
+                                           const unsigned char* wt, int kdim, float (&acc)[4]) {
+  const FcArgs& a = d.f;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, q = lane & 3, h = q & 1, tsel = q >> 1;
+  const int steps = it.ncols >> 5;
+  const int col0 = it.sg * kDecSeg;
+  // activation fragment source: slot g's row, columns 32 ks + 16 tsel + 8 h
+  const int arow = __shfl_sync(0xFFFFFFFFu, row, g);
+  const uint16_t* ap = reinterpret_cast<const uint16_t*>(a.act) + (size_t)(arow < 0 ? 0 : arow) * kdim + col0 +
+                       16 * tsel + 8 * h;
+  // W4A8: E8M0 block exponents of slots 2q and 2q+1 for this segment
+  const int r0 = W4A8 ? __shfl_sync(0xFFFFFFFFu, row, 2 * q) : -1;
+  const int r1 = W4A8 ? __shfl_sync(0xFFFFFFFFu, row, 2 * q + 1) : -1;
+  const uint8_t* sp0 = a.act_scale + (size_t)(r0 < 0 ? 0 : r0) * (kdim >> 5) + (col0 >> 5);
+  const uint8_t* sp1 = a.act_scale + (size_t)(r1 < 0 ? 0 : r1) * (kdim >> 5) + (col0 >> 5);
+  const uint32_t k16 = 0x10000u + (uint32_t)(d.T >> 30);  // 65536, opaque to the compiler
+  const uint32_t nk16 = 0u - k16;
+  const int swz = 64 * tsel;
+  const int oc0 = (4 * (2 * g + h)) ^ swz, op0 = (4 * ((2 * g + h + 31) & 31)) ^ swz;
+  const int oc1 = (4 * (2 * g + 16 + h)) ^ swz, op1 = (4 * (2 * g + 15 + h)) ^ swz;
+#pragma unroll
+  for (int ks = 0; ks < kDwSteps; ++ks) {
+    if (ks < steps) {
+      const uint4 bv = (arow >= 0) ? __ldg(reinterpret_cast<const uint4*>(ap + 32 * ks)) : make_uint4(0u, 0u, 0u, 0u);
+      const unsigned char* tile = wt + (2 * ks + tsel) * 32 * K;
+      uint32_t y0[8], y1[8];
+      if (K == 4) {
+        const uint32_t c0w = *reinterpret_cast<const uint32_t*>(tile + oc0);
+        const uint32_t p0w = *reinterpret_cast<const uint32_t*>(tile + op0);
+        const uint32_t c1w = *reinterpret_cast<const uint32_t*>(tile + oc1);
+        const uint32_t p1w = *reinterpret_cast<const uint32_t*>(tile + op1);
+        run_mcg_k4(p0w, c0w, k16, nk16, y0);
+        run_mcg_k4(p1w, c1w, k16, nk16, y1);
+      } else {
+        uint32_t hi, lo, s8[8];
+        int off;
+        dw_window<K>(reinterpret_cast<const uint16_t*>(tile), 16 * g + 8 * h, hi, lo, off);
+        run_states_generic<K>(hi, lo, off, s8);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y0[i] = mcg_raw(s8[i]);
+        dw_window<K>(reinterpret_cast<const uint16_t*>(tile), 16 * (g + 8) + 8 * h, hi, lo, off);
+        run_states_generic<K>(hi, lo, off, s8);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y1[i] = mcg_raw(s8[i]);
+      }
+      uint32_t wa[4], wb[4];
+      if (W4A8) {
+        raw_to_e4m3_f16(y0, wa);
+        raw_to_e4m3_f16(y1, wb);
+      } else {
+        raw_to_f16(y0, wa);
+        raw_to_f16(y1, wb);
+      }
+      const uint32_t a0[4] = {wa[0], wb[0], wa[1], wb[1]};
+      const uint32_t a1[4] = {wa[2], wb[2], wa[3], wb[3]};
+      if (W4A8) {
+        const float s0 = (r0 >= 0) ? exp2_int((int)__ldg(sp0 + ks) - 127) : 0.0f;
+        const float s1 = (r1 >= 0) ? exp2_int((int)__ldg(sp1 + ks) - 127) : 0.0f;
+        float dd[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f16_16816(dd, a0, bv.x, bv.y);
+        mma_f16_16816(dd, a1, bv.z, bv.w);
+        acc[0] = fmaf(dd[0], s0, acc[0]);
+        acc[1] = fmaf(dd[1], s1, acc[1]);
+        acc[2] = fmaf(dd[2], s0, acc[2]);
+        acc[3] = fmaf(dd[3], s1, acc[3]);
+      } else {
+        mma_f16_16816(acc, a0, bv.x, bv.y);
+        mma_f16_16816(acc, a1, bv.z, bv.w);
+      }
+    }
+  }
+}
+
+template <bool W4A8, int KB>
+__device__ __forceinline__ void dw_compute_any(const DecArgs& d, const DwItem& it, int row,
+                                               const unsigned char* wt, int kdim, float (&acc)[4]) {
+  if (KB > 0) {
+    dw_compute<W4A8, (KB > 0 ? KB : 4)>(d, it, row, wt, kdim, acc);
+    return;
+  }
+  switch (it.k) {
+    case 2: dw_compute<W4A8, 2>(d, it, row, wt, kdim, acc); break;
+    case 3: dw_compute<W4A8, 3>(d, it, row, wt, kdim, acc); break;
+    case 4: dw_compute<W4A8, 4>(d, it, row, wt, kdim, acc); break;
+    case 5: dw_compute<W4A8, 5>(d, it, row, wt, kdim, acc); break;
+    default: dw_compute<W4A8, 6>(d, it, row, wt, kdim, acc); break;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Epilogues, one warp for one slot n of one unit of route block rb. Partial
+// sums of an item sit at partial[item * 128 + slot * 16 + row16], item = (rb *
+// nseg + sg) * nstrips + strip. dw_sum_parts adds those of one strip in
+// segment order, four loads in flight at a time.
+// ---------------------------------------------------------------------------
+template <int V>
+__device__ __forceinline__ void dw_sum_parts(const DecArgs& d, int rb, int strip, int nstrips, int n, int r16,
+                                             float (&v)[V]) {
+#pragma unroll
+  for (int i = 0; i < V; ++i) v[i] = 0.0f;
+  for (int s0 = 0; s0 < d.nseg; s0 += 4) {
+    float x[4][V];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const bool ok = s0 + u < d.nseg;
+      const float* p = d.partial + ((size_t)(rb * d.nseg + (ok ? s0 + u : 0)) * nstrips + strip) * 128 + n * 16 + r16;
+      if (V == 4) {
+        const float4 q = ok ? __ldcg(reinterpret_cast<const float4*>(p)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        x[u][0] = q.x; x[u][1] = q.y; x[u][V > 2 ? 2 : 0] = q.z; x[u][V > 3 ? 3 : 0] = q.w;
+      } else {
+        const float2 q = ok ? __ldcg(reinterpret_cast<const float2*>(p)) : make_float2(0.f, 0.f);
+        x[u][0] = q.x; x[u][1] = q.y;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (s0 + u < d.nseg) {
+#pragma unroll
+        for (int i = 0; i < V; ++i) v[i] += x[u][i];
+      }
+  }
+}
+
+// The same for two strips at once (gate and up), all loads of four segments
+// in flight together.
+template <int V>
+__device__ __forceinline__ void dw_sum_parts2(const DecArgs& d, int rb, int strip_a, int strip_b, int nstrips, int n,
+                                              int r16, float (&va)[V], float (&vb)[V]) {
+#pragma unroll
+  for (int i = 0; i < V; ++i) va[i] = vb[i] = 0.0f;
+  for (int s0 = 0; s0 < d.nseg; s0 += 4) {
+    float xa[4][V], xb[4][V];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const bool ok = s0 + u < d.nseg;
+      const size_t base = (size_t)(rb * d.nseg + (ok ? s0 + u : 0)) * nstrips;
+      const float* pa = d.partial + (base + strip_a) * 128 + n * 16 + r16;
+      const float* pb = d.partial + (base + strip_b) * 128 + n * 16 + r16;
+      if (V == 4) {
+        const float4 qa = ok ? __ldcg(reinterpret_cast<const float4*>(pa)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 qb = ok ? __ldcg(reinterpret_cast<const float4*>(pb)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        xa[u][0] = qa.x; xa[u][1] = qa.y; xa[u][V > 2 ? 2 : 0] = qa.z; xa[u][V > 3 ? 3 : 0] = qa.w;
+        xb[u][0] = qb.x; xb[u][1] = qb.y; xb[u][V > 2 ? 2 : 0] = qb.z; xb[u][V > 3 ? 3 : 0] = qb.w;
+      } else {
+        const float2 qa = ok ? __ldcg(reinterpret_cast<const float2*>(pa)) : make_float2(0.f, 0.f);
+        const float2 qb = ok ? __ldcg(reinterpret_cast<const float2*>(pb)) : make_float2(0.f, 0.f);
+        xa[u][0] = qa.x; xa[u][1] = qa.y;
+        xb[u][0] = qb.x; xb[u][1] = qb.y;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (s0 + u < d.nseg) {
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+          va[i] += xa[u][i];
+          vb[i] += xb[u][i];
+        }
+      }
+  }
+}
+
+// PER consecutive fp16 values as floats (PER = 2 or 4, 4- or 8-byte aligned).
+template <int PER>
+__device__ __forceinline__ void dw_ld_h(const uint16_t* p, float (&v)[PER]) {
+  if (PER == 4) {
+    const uint2 q = __ldg(reinterpret_cast<const uint2*>(p));
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&q.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&q.y));
+    v[0] = a.x; v[1] = a.y; v[PER > 2 ? 2 : 0] = b.x; v[PER > 3 ? 3 : 0] = b.y;
+  } else {
+    const uint32_t q = __ldg(reinterpret_cast<const uint32_t*>(p));
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&q));
+    v[0] = a.x; v[1] = a.y;
+  }
+}
+
+// FC1 unit mb: gate channels mb*BI .. +BI-1 and the matching up channels.
+template <int PER, bool W4A8>
+__device__ __forceinline__ void dw_epilogue_fc1(const DecArgs& d, int rb, int mb, int e, int n, int nstrips) {
+  constexpr int BI = 32 * PER;
+  const FcArgs& a = d.f;
+  const int lane = threadIdx.x & 31;
+  const uint16_t* s1 = a.scale + (size_t)e * 2 * a.I;
+  const uint16_t* rt = a.rot_tab + (size_t)e * 3 * a.I;
+  const int c0 = mb * BI + lane * PER;  // this lane's first channel (PER consecutive, one strip)
+  const int strip_g = c0 >> 4, strip_u = (a.I + c0) >> 4, r16 = c0 & 15;
+  const float hs = hadamard_scale(a.rot_b);
+  {
+    const int slot = rb * kDecBlock + n;
+    float gv[PER], uv[PER], av[PER];
+    // the channel vectors first, then the partial sums: both in flight together
+    float sg_[PER], su_[PER], vg_[PER], vu_[PER], vd_[PER];
+    dw_ld_h<PER>(s1 + c0, sg_);
+    dw_ld_h<PER>(s1 + a.I + c0, su_);
+    dw_ld_h<PER>(rt + c0, vg_);
+    dw_ld_h<PER>(rt + a.I + c0, vu_);
+    dw_ld_h<PER>(rt + 2 * a.I + c0, vd_);
+    dw_sum_parts2<PER>(d, rb, strip_g, strip_u, nstrips, n, r16, gv, uv);
+#pragma unroll
+    for (int p = 0; p < PER; ++p) {
+      gv[p] *= sg_[p];
+      uv[p] *= su_[p];
+    }
+    warp_fwht<PER>(gv, a.rot_b);
+    warp_fwht<PER>(uv, a.rot_b);
+#pragma unroll
+    for (int p = 0; p < PER; ++p) {
+      const float gg = gv[p] * hs * vg_[p];
+      const float uu = uv[p] * hs * vu_[p];
+      av[p] = (gg / (1.0f + __expf(-gg))) * uu * vd_[p];
+    }
+    warp_fwht<PER>(av, a.rot_b);
+#pragma unroll
+    for (int p = 0; p < PER; ++p) av[p] *= hs;
+    uint16_t* z = reinterpret_cast<uint16_t*>(a.out_act) + (size_t)slot * a.I + c0;
+    if (!W4A8) {
+#pragma unroll
+      for (int p = 0; p < PER; p += 2) {
+        __half2 v2 = __floats2half2_rn(av[p], av[p + 1]);
+        *reinterpret_cast<__half2*>(z + p) = v2;
+      }
+    } else {
+      // MXFP8 of z~ per 32 channels: E4M3 codes kept as fp16, E8M0 exponent apart
+      constexpr int LPB = 32 / PER;  // lanes per 32-channel block
+      float amax = 0.0f;
+#pragma unroll
+      for (int p = 0; p < PER; ++p) amax = fmaxf(amax, fabsf(av[p]));
+#pragma unroll
+      for (int o = 1; o < LPB; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+      const int ex = e8m0_exponent(amax);
+      const float inv = exp2_int(-ex);
+#pragma unroll
+      for (int p = 0; p < PER; p += 2)
+        *reinterpret_cast<uint32_t*>(z + p) = e4m3x2_to_f16x2(e4m3x2_from_float2(av[p] * inv, av[p + 1] * inv));
+      if ((lane % LPB) == 0) a.out_scale[(size_t)slot * (a.I >> 5) + (c0 >> 5)] = (uint8_t)(ex + 127);
+    }
+  }
+}
+
+// FC2, token t, output channels mb*128 .. +127: for each of the token's routes
+// j = 0..k-1 in order, the route's summed partials, output scale, H, hs *
+// down_svh, and w_j times that into the FP32 sum (the deterministic top-k
+// combine); routes are taken four at a time with all their loads in flight.
+__device__ __forceinline__ void dw_epilogue_fc2(const DecArgs& d, int t, int mb, int nstrips) {
+  const FcArgs& a = d.f;
+  const int lane = threadIdx.x & 31;
+  const int h0 = mb * 128 + lane * 4;
+  const int strip = h0 >> 4, r16 = h0 & 15;
+  const float hs = hadamard_scale(a.rot_b);
+  const int k = a.topk;
+  // the token's slots, weights and experts, one route per lane
+  int my_slot = -1, my_e = 0;
+  float my_w = 0.0f;
+  if (lane < k) {
+    my_slot = d.slot_of_route[t * k + lane];
+    my_w = d.route_w[t * k + lane];
+    my_e = d.ids[t * k + lane];
+  }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j0 = 0; j0 < k; j0 += 4) {
+    int sl[4], ex[4];
+    float wj[4], v[4][4], sc[4][4], sv[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u;
+      sl[u] = __shfl_sync(0xFFFFFFFFu, my_slot, j & 31);
+      wj[u] = __shfl_sync(0xFFFFFFFFu, my_w, j & 31);
+      ex[u] = __shfl_sync(0xFFFFFFFFu, my_e, j & 31);
+      if (j >= k) sl[u] = -1;
+      const bool ok = sl[u] >= 0;  // (a dropped, out-of-range expert id has no slot)
+      dw_ld_h<4>(a.scale + (size_t)(ok ? ex[u] : 0) * a.H + h0, sc[u]);
+      dw_ld_h<4>(a.rot_tab + (size_t)(ok ? ex[u] : 0) * a.H + h0, sv[u]);
+    }
+    // partial sums of the four routes, two segments at a time
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int p = 0; p < 4; ++p) v[u][p] = 0.0f;
+    for (int s0 = 0; s0 < d.nseg; s0 += 2) {
+      float4 x[4][2];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const bool ok = sl[u] >= 0 && s0 + q < d.nseg;
+          const int rb = ok ? sl[u] / kDecBlock : 0, n = ok ? sl[u] % kDecBlock : 0;
+          const float* pp = d.partial + ((size_t)(rb * d.nseg + (ok ? s0 + q : 0)) * nstrips + strip) * 128 + n * 16 + r16;
+          x[u][q] = ok ? __ldcg(reinterpret_cast<const float4*>(pp)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          if (s0 + q < d.nseg) {
+            v[u][0] += x[u][q].x;
+            v[u][1] += x[u][q].y;
+            v[u][2] += x[u][q].z;
+            v[u][3] += x[u][q].w;
+          }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (sl[u] < 0) continue;  // warp-uniform
+      float y[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) y[p] = v[u][p] * sc[u][p];
+      warp_fwht<4>(y, a.rot_b);
+#pragma unroll
+      for (int p = 0; p < 4; ++p) y[p] = y[p] * hs * sv[u][p];
+      acc.x = fmaf(wj[u], y[0], acc.x);
+      acc.y = fmaf(wj[u], y[1], acc.y);
+      acc.z = fmaf(wj[u], y[2], acc.z);
+      acc.w = fmaf(wj[u], y[3], acc.w);
+    }
+  }
+  *reinterpret_cast<float4*>(d.out + (size_t)t * a.H + h0) = acc;
+}
+
+// ---------------------------------------------------------------------------
+// The kernel. Warp w of W takes items w, w + W, ..., so that the warps work
+// through the payload together, one window of W consecutive items at a time
+// (measured faster than giving each warp a contiguous range, which balances
+// the last window better but scatters the concurrent reads). The metadata of
+// an item's route block is loaded two items ahead, its payload one item
+// ahead. FC2 reads only prologue outputs (route map, block table) and
+// constant weights before it waits for its predecessor, so its first payload
+// copy overlaps the FC1 epilogue. Partial sums: per item, [slot][16 rows] fp32.
+// ---------------------------------------------------------------------------
+template <bool W4A8, int PROJ, int KB>
+__global__ void __launch_bounds__(kDwThreads, KB > 0 ? 6 : 4) k_dec_warp(const DecArgs d) {
+  extern __shared__ __align__(128) unsigned char dw_smem[];
+  const FcArgs& a = d.f;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int KMAX = KB > 0 ? KB : 6;
+  const int slot_bytes = dw_slot_bytes(KMAX);
+  unsigned char* ring = dw_smem + warp * kDwRing * slot_bytes;
+  const int kdim = PROJ == 1 ? a.H : a.I;
+  const uint32_t nstrips = (uint32_t)((PROJ == 1 ? 2 * a.I : a.H) >> 4);
+  const uint32_t per_block = (uint32_t)d.nseg * nstrips;
+  const uint32_t nwarps = gridDim.x * kDwWarps;
+
+  if (PROJ == 1) dw_griddep_wait();  // the route map and x~ come from the prologue
+  const int nb = min(*a.nblocks, d.max_blocks);
+  const uint32_t h1 = (uint32_t)nb * per_block;  // items
+  uint32_t h = blockIdx.x * kDwWarps + warp;     // next item of this warp
+  const bool any = h < h1;
+  uint32_t pc = 0, pn = 0, pn2 = 0;
+  DwItem it{}, nit{};
+  DwMetaW m{}, nm{};
+  DwRaw raw1{-1, 0}, raw2{-1, 0};
+  bool has1 = false, has2 = false;
+  if (any) {
+    pc = h;
+    h += nwarps;
+    const DwRaw raw0 = dw_meta_issue(d, (int)(pc / per_block), lane);
+    has1 = h < h1;
+    if (has1) {
+      pn = h;
+      h += nwarps;
+      raw1 = dw_meta_issue(d, (int)(pn / per_block), lane);
+    }
+    it = dw_item(d, pc, nstrips, kdim);
+    m = dw_meta_final<PROJ>(raw0, it.rb, lane, a.topk);
+    dw_item_meta(it, m);
+    dw_copy_any(KB > 0 ? KB : it.k, ring, dw_src(d, m, it, kdim), it.ncols >> 4, lane);
+  }
+  cp_async_commit();
+  if (PROJ == 2) dw_griddep_wait();  // z~ and the partial buffer belong to the predecessors until now
+  dw_griddep_launch();
+  if (!any) return;
+  if (has1) {
+    nit = dw_item(d, pn, nstrips, kdim);
+    nm = dw_meta_final<PROJ>(raw1, nit.rb, lane, a.topk);
+    dw_item_meta(nit, nm);
+    has2 = h < h1;
+    if (has2) {
+      pn2 = h;
+      h += nwarps;
+      raw2 = dw_meta_issue(d, (int)(pn2 / per_block), lane);
+    }
+  }
+  for (int n = 0;; ++n) {
+    if (has1)
+      dw_copy_any(KB > 0 ? KB : nit.k, ring + ((n + 1) & 1) * slot_bytes, dw_src(d, nm, nit, kdim), nit.ncols >> 4, lane);
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncwarp();
+
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    dw_compute_any<W4A8, KB>(d, it, m.row, ring + (n & 1) * slot_bytes, kdim, acc);
+
+    // partial sums of the valid slots, [slot][16 rows]
+    const int g = lane >> 2, c = 2 * (lane & 3);
+    float* pb = d.partial + (size_t)pc * 128;
+    if (c < it.nvalid) {
+      pb[c * 16 + g] = acc[0];
+      pb[c * 16 + g + 8] = acc[2];
+    }
+    if (c + 1 < it.nvalid) {
+      pb[(c + 1) * 16 + g] = acc[1];
+      pb[(c + 1) * 16 + g + 8] = acc[3];
+    }
+    __syncwarp();  // this ring slot is refilled two pieces on
+    if (!has1) break;
+    pc = pn;
+    it = nit;
+    m = nm;
+    has1 = has2;
+    if (has1) {
+      pn = pn2;
+      nit = dw_item(d, pn, nstrips, kdim);
+      nm = dw_meta_final<PROJ>(raw2, nit.rb, lane, a.topk);
+      dw_item_meta(nit, nm);
+      has2 = h < h1;
+      if (has2) {
+        pn2 = h;
+      h += nwarps;
+        raw2 = dw_meta_issue(d, (int)(pn2 / per_block), lane);
+      }
+    }
+  }
+  cp_async_wait<0>();
+}
+
+// The epilogue kernels: FC1 one warp per (route block, unit of BI
+// intermediate channels, slot), FC2 one warp per (token, 128 output channels).
+template <bool W4A8, int PROJ>
+__global__ void __launch_bounds__(256) k_dec_epi(const DecArgs d) {
+  dw_griddep_wait();  // the partial sums come from the predecessor
+  dw_griddep_launch();
+  const FcArgs& a = d.f;
+  const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  if (PROJ == 1) {
+    const int n = gw % kDecBlock;
+    const int um = gw / kDecBlock;
+    const int mb = um % d.units_m;
+    const int rb = um / d.units_m;
+    if (rb >= d.max_blocks) return;
+    const int meta = d.blk_meta[rb];  // (0 past the last block)
+    if (n >= (meta >> 24)) return;    // padding slot
+    const int e = meta & 0xFFFF;
+    const int nstrips = (2 * a.I) >> 4;
+    if (d.bi == 128)
+      dw_epilogue_fc1<4, W4A8>(d, rb, mb, e, n, nstrips);
+    else
+      dw_epilogue_fc1<2, W4A8>(d, rb, mb, e, n, nstrips);
+  } else {
+    const int mb = gw % d.units_m;
+    const int t = gw / d.units_m;
+    if (t >= d.T) return;
+    dw_epilogue_fc2(d, t, mb, a.H >> 4);
+  }
+}
+
+template <bool W4A8, int PROJ, int KB>
+static cudaError_t dw_warps_t(int* warps) {
+  // attributes and the resident-CTA count are fixed on the first call (before any capture)
+  static int resident = 0;
+  if (resident == 0) {
+    auto kern = k_dec_warp<W4A8, PROJ, KB>;
+    const int smem = dw_smem_bytes(KB > 0 ? KB : 6);
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    int per_sm = 0;
+    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDwThreads, smem)) != cudaSuccess) return err;
+    int dev = 0, sms = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+    resident = std::max(1, per_sm) * sms;
+  }
+  *warps = resident * kDwWarps;
+  return cudaSuccess;
+}
+
+template <bool W4A8, int PROJ, int KB>
+static cudaError_t launch_dw_t(const DecArgs& d, cudaStream_t st) {
+  if (d.fc_warps <= 0 || d.fc_warps % kDwWarps) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(d.fc_warps / kDwWarps);
+  cfg.blockDim = dim3(kDwThreads);
+  cfg.dynamicSmemBytes = dw_smem_bytes(KB > 0 ? KB : 6);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_dec_warp<W4A8, PROJ, KB>, d);
+}
+
+template <bool W4A8, int PROJ>
+static cudaError_t launch_epi_t(const DecArgs& d, cudaStream_t st) {
+  const long warps = (PROJ == 1) ? (long)d.max_blocks * d.units_m * kDecBlock : (long)d.T * d.units_m;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((warps + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_dec_epi<W4A8, PROJ>, d);
+}
+
+cudaError_t dec_fc_warps(int proj, bool w4a8, int uniform_k, int* warps) {
+  const bool k4 = uniform_k == 4;
+  if (proj == 1) {
+    if (w4a8) return k4 ? dw_warps_t<true, 1, 4>(warps) : dw_warps_t<true, 1, 0>(warps);
+    return k4 ? dw_warps_t<false, 1, 4>(warps) : dw_warps_t<false, 1, 0>(warps);
+  }
+  if (w4a8) return k4 ? dw_warps_t<true, 2, 4>(warps) : dw_warps_t<true, 2, 0>(warps);
+  return k4 ? dw_warps_t<false, 2, 4>(warps) : dw_warps_t<false, 2, 0>(warps);
+}
+
+cudaError_t launch_dec_epilogue(const DecArgs& d, int proj, bool w4a8, cudaStream_t st) {
+  if (proj == 1) return w4a8 ? launch_epi_t<true, 1>(d, st) : launch_epi_t<false, 1>(d, st);
+  return w4a8 ? launch_epi_t<true, 2>(d, st) : launch_epi_t<false, 2>(d, st);
+}
+
+cudaError_t launch_dec_fc(const DecArgs& d, int proj, bool w4a8, int uniform_k, cudaStream_t st) {
+  const bool k4 = uniform_k == 4;
+  if (proj == 1) {
+    if (w4a8) return k4 ? launch_dw_t<true, 1, 4>(d, st) : launch_dw_t<true, 1, 0>(d, st);
+    return k4 ? launch_dw_t<false, 1, 4>(d, st) : launch_dw_t<false, 1, 0>(d, st);
+  }
+  if (w4a8) return k4 ? launch_dw_t<true, 2, 4>(d, st) : launch_dw_t<true, 2, 0>(d, st);
+  return k4 ? launch_dw_t<false, 2, 4>(d, st) : launch_dw_t<false, 2, 0>(d, st);
+}
+
+}  // namespace tmoe

@@ -48,7 +48,10 @@ struct FcArgs {
 };
 
 // Decode-rows path (few tokens): one fused prologue, then FC1 and FC2 as
-// split-K kernels whose last-arriving CTA per unit finishes the epilogue.
+// persistent warp-granular kernels over items of 16 weight rows x 256
+// contraction columns of one route block of 8 slots, each followed by an
+// epilogue kernel (one warp per epilogue unit and slot) that sums the unit's
+// partial sums in fixed order.
 struct DecPrologueArgs {
   const float* logits;      // router logits [T, E], or nullptr when ids are given
   int32_t* ids_out;         // router outputs (when logits != nullptr)
@@ -57,24 +60,38 @@ struct DecPrologueArgs {
   const uint16_t* x;        // bf16 [T, H]
   const uint16_t* suh;      // fp16 [H]
   int T, H, topk, rot_b, w4a8;
-  void* xq;                 // fp16 or E4M3 [T, H]
+  void* xq;                 // fp16 [T, H] (W4A8: the E4M3 codes, as fp16)
   uint8_t* xs;              // E8M0 [T, H/32]
   int32_t* zero_i32;        // counters to clear
   int n_zero_i32;
   float* out;               // [T, H], cleared here (tokens without a valid route stay 0)
   long out_n;
+  // per route block b < max_blocks, written after the route map: expert |
+  // bits << 16 | valid slots << 24 (0 past the last block), and the byte
+  // offsets of the expert's FC1 and FC2 payload
+  const int64_t* word_off1;
+  const int64_t* word_off2;
+  const uint8_t* bits;
+  int max_blocks;
+  int32_t* blk_meta;
+  long long* blk_off1;
+  long long* blk_off2;
 };
 
+constexpr int kDecSeg = 256;  // contraction columns of one decode-rows item
+constexpr int kDecBlock = 8;  // slots per route block
+
 struct DecArgs {
-  FcArgs f;
-  int ksplit;               // S: CTAs along the contraction axis per unit part
-  int kchunk;               // columns per split (multiple of 64)
-  int parts;                // 128-row CTAs per epilogue unit (FC1: 2*BI/128, FC2: 1)
+  FcArgs f;                 // act: fp16 rows (W4A8: E4M3 codes as fp16, E8M0 scales in act_scale)
+  const int32_t* blk_meta;  // per route block: expert | bits << 16 | valid slots << 24
+  const long long* blk_off; // per route block: byte offset of the expert's payload (this projection)
+  int nseg;                 // contraction segments of kDecSeg columns
   int units_m;              // epilogue units per route block (FC1: I/BI, FC2: H/128)
   int bi;                   // FC1 half-row block (64 or 128)
-  float* partial;           // [max_blocks*units_m][S][unit_rows][8] fp32
-  int32_t* unit_cnt;        // [max_blocks*units_m] arrival counters
-  int32_t* tok_cnt;         // FC2: [T][units_m] completion counters
+  int max_blocks;           // route blocks the route map can produce
+  int fc_warps;             // warps of the FC kernel's grid (dec_fc_warps)
+  float* partial;           // [blocks][nseg][rows/16][8 slots][16 rows] fp32 partial sums
+  const int32_t* ids;       // [T*topk] expert ids (FC2 epilogue)
   const int32_t* slot_of_route;
   const float* route_w;     // [T*topk]
   float* out;               // FC2: final output [T, H]
@@ -82,10 +99,11 @@ struct DecArgs {
 };
 
 cudaError_t launch_dec_prologue(const DecPrologueArgs& a, cudaStream_t st);
-cudaError_t launch_dec_fc(const DecArgs& d, int proj, bool w4a8, int uniform_k, int max_blocks, cudaStream_t st);
-// Split-K factor the decode path uses for a contraction of `kdim` columns when
-// `units` 128-row CTAs per split exist (also sizes the workspace).
-int dec_ksplit(int kdim, long units);
+// Warps of the decode-rows FC kernel's grid (all resident: CTAs per SM x SMs);
+// fixed on the first call, which also sets the kernel's attributes.
+cudaError_t dec_fc_warps(int proj, bool w4a8, int uniform_k, int* warps);
+cudaError_t launch_dec_fc(const DecArgs& d, int proj, bool w4a8, int uniform_k, cudaStream_t st);
+cudaError_t launch_dec_epilogue(const DecArgs& d, int proj, bool w4a8, cudaStream_t st);
 
 // FC1 / FC2 on tcgen05 outside the decode regime: x~ [slots][H] and z~
 // [slots][I] fp16 in slot order (W4A8: the exact dequantized MXFP8 values),
