@@ -255,11 +255,10 @@ def run_ours(args, rank, world):
     pk = peaks()
     # DRAM bytes per launch of the dominant kernel from one ncu capture of this
     # program (profiles/); None for workloads without a capture
-    ncu_traffic = {"decode": (32.22e6, "profiles/k_dec_fc_fc1_decode_w4a8_T8.md"),
-                   "prefill": (130.83e6, "profiles/k_tc_fc_fc1_prefill_w4a16_T2048.md")}.get(args.workload)
+    ncu_traffic = {"prefill": (130.83e6, "profiles/k_tc_fc_fc1_prefill_w4a16_T2048.md")}.get(args.workload)
     if mode == "w4a8" and T <= 64:
         achieved = statistics.mean(fc1_bytes) / (stages_us["fc1"] * 1e-6) / 1e9
-        roof = {"bound": "hbm", "kernel": "k_dec_fc<W4A8,FC1,K=4> (decode rows, split contraction)"
+        roof = {"bound": "hbm", "kernel": "k_dec_warp<W4A8,FC1,K=4> (decode rows, persistent warp items)"
                 if R <= 1024 and R < 4 * cfg.E else "k_tc_fc<FC1,K=4,W4A8> (tcgen05)",
                 "achieved": round(achieved, 1),
                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
@@ -303,7 +302,7 @@ def run_ours(args, rank, world):
 
     decode_path = R <= 1024 and R < 4 * cfg.E   # the library's decode-rows path
     # decode rows: prologue, FC1, FC2 (with the combine); otherwise router, route map (1 or 3), rotate, FC1, FC2, combine
-    launches_per_step = 3 if decode_path else 6 + (2 if R > 1024 else 0)
+    launches_per_step = 5 if decode_path else 6 + (2 if R > 1024 else 0)
     res = {
         "metric": METRIC, "value": job_value(args.steps, T, world, total_ms), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,

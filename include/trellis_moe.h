@@ -163,11 +163,16 @@ tm_status trellis_moe_decode_tiles(tm_layer* layer, int32_t proj, int32_t expert
                                    int32_t ntiles, int32_t mode, void* dst, void* stream);
 
 /* Where a forward call of `T` tokens keeps its intermediates inside the
- * workspace (for tests): which = 0 x~ (fp16 or E4M3), 1 x~ E8M0 exponents,
- * 2 FC1 epilogue output z~ (fp16 or E4M3), 3 z~ E8M0 exponents, 4 per-slot
+ * workspace (for tests): which = 0 x~, 1 x~ E8M0 exponents, 2 FC1 epilogue
+ * output z~, 3 z~ E8M0 exponents (x~ and z~: fp16 for W4A16; for W4A8 the
+ * E4M3 codes on the mma.sync path, the codes held as fp16 on the decode-rows
+ * path, the dequantized values as fp16 in slot order on the tensor-core
+ * path), 4 per-slot
  * FC2 output (fp32 [slots, H]: the unrotated route output, or, for the
- * tensor-core FC2 with the deterministic combine, the bare FC2 accumulator
- * before output scale, H and down_svh), 5 slot_of_route (int32 [T*topk]),
+ * tensor-core FC2 with the deterministic combine, the scaled FC2 accumulator
+ * after the Hadamard levels within each 64-column half; not written by the
+ * decode-rows path, whose combine is part of the FC2 epilogue), 5
+ * slot_of_route (int32 [T*topk]),
  * 6 device error word (uint32). Returns TM_EINVAL for an unknown `which`. */
 tm_status trellis_moe_workspace_region(const tm_layer* layer, int32_t T, int32_t which,
                                        size_t* offset, size_t* bytes);
@@ -178,8 +183,12 @@ tm_status trellis_moe_workspace_region(const tm_layer* layer, int32_t T, int32_t
  * cudaEventRecordExternal so that the records also become nodes of a captured
  * CUDA graph, at these boundaries: 0 start, 1 after the router (forward_logits
  * and forward_host only), 2 after the route map, 3 after rotate+quantize,
- * 4 after FC1, 5 after FC2, 6 after the combine. events = NULL or n = 0 turns
- * recording off. The handles are copied; the caller keeps ownership. */
+ * 4 after FC1, 5 after FC2, 6 after the combine. In the decode-rows path the
+ * router, route map and rotation are one kernel (1..3 follow it together),
+ * 4 follows the FC1 GEMM kernel (FC1's epilogue kernel counts with FC2) and
+ * the combine is part of the FC2 epilogue (5 and 6 follow it together).
+ * events = NULL or n = 0 turns recording off. The handles are copied; the
+ * caller keeps ownership. */
 tm_status trellis_moe_set_stage_events(tm_layer* layer, void* const* events, int32_t n);
 
 /* Read and clear the device error word of `workspace` (synchronises `stream`).

@@ -379,9 +379,10 @@ tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids
     return cuda_fail(e, "FC1 (decode rows) setup");
   if ((e = tmoe::launch_dec_fc(d1, 1, w4a8, layer->uniform_k, st)) != cudaSuccess)
     return cuda_fail(e, "FC1 (decode rows)");
+  // (stage 4 marks the FC1 GEMM kernel; its epilogue kernel counts with FC2)
+  if ((e = stage_mark(layer, 4, st)) != cudaSuccess) return cuda_fail(e, "stage event");
   if ((e = tmoe::launch_dec_epilogue(d1, 1, w4a8, st)) != cudaSuccess)
     return cuda_fail(e, "FC1 epilogue (decode rows)");
-  if ((e = stage_mark(layer, 4, st)) != cudaSuccess) return cuda_fail(e, "stage event");
 
   tmoe::DecArgs d2 = d1;
   tmoe::FcArgs& a2 = d2.f;
