@@ -354,6 +354,32 @@ def test_decode_path_layers(mode, kw):
     assert err < TOL[mode], err
 
 
+def _scale_bf16(bits, k):
+    """bf16 bit patterns times 2^k (exact: only the exponent changes)."""
+    f = (bits.astype(np.uint32) << 16).view(np.float32) * np.float32(2.0 ** k)
+    return (f.view(np.uint32) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("scales", [(0, -24, 16, 0), (-24, -24, -24, -24), (16, 16, 16, 16)])
+def test_decode_path_w4a8_block_exponent_ranges(scales):
+    """W4A8 decode rows keep the activations both as E4M3 codes and as
+    code * 2^e; blocks whose exponent falls outside [-15, 7] must take the
+    scaled path. Tokens scaled by 2^-24 and 2^16 push x~ (and z~) out of that
+    range, alone or mixed with ordinary tokens in one route block."""
+    cfg = small_cfg(T=4, E=16, topk=4, H=256, I=128)
+    assert cfg.T * cfg.topk < 4 * cfg.E
+    L = synth.make_layer(cfg)
+    moe = _moe(L, cfg.T)
+    x_bits, logits = synth.make_tokens(cfg)
+    x_bits = np.stack([_scale_bf16(x_bits[t], k) for t, k in enumerate(scales)])
+    ids, w = oracle_routes(logits, cfg.topk)
+    x, lg = upload_tokens(x_bits, logits)
+    out = moe.forward_logits(x, lg, mode="w4a8")
+    torch.cuda.synchronize()
+    ref = olayer.layer_forward(L, x_bits, ids, w.astype(np.float32), mode="w4a8")
+    assert rel_row_err(out.cpu().numpy(), ref) < TOL["w4a8"]
+
+
 def test_decode_path_deterministic_poisoned_and_atomic():
     cfg = small_cfg(T=6, E=32, topk=4)
     L = synth.make_layer(cfg)

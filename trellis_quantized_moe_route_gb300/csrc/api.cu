@@ -329,6 +329,8 @@ tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids
   pa.rot_b = d.rot_block_h;
   pa.w4a8 = w4a8 ? 1 : 0;
   pa.xq = at<void>(ws, L, Layout::XQ);
+  // W4A8: the pre-multiplied copy of x~ after the codes (the region holds slots >= 2T rows)
+  pa.xq_scaled = at<uint16_t>(ws, L, Layout::XQ) + (size_t)T * d.H;
   pa.xs = at<uint8_t>(ws, L, Layout::XS);
   pa.zero_i32 = at<int32_t>(ws, L, Layout::DEC_CNT);
   pa.n_zero_i32 = (int)dp.cnt_ints;
@@ -368,6 +370,10 @@ tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids
   d1.bi = dp.bi;
   d1.partial = at<float>(ws, L, Layout::DEC_PARTIAL);
   d1.ids = pa.rm.ids;
+  d1.act_scaled = pa.xq_scaled;
+  // z~ rows are slots < max_blocks * 8; the pre-multiplied copy follows them
+  // (the region holds T*topk + 255E >= 2 * max_blocks * 8 rows in this regime)
+  d1.out_act_scaled = at<uint16_t>(ws, L, Layout::ZQ) + (size_t)dp.max_blocks * tmoe::kDecBlock * d.I;
   d1.blk_meta = pa.blk_meta;
   d1.blk_off = pa.blk_off1;
   d1.slot_of_route = pa.rm.slot_of_route;
@@ -397,6 +403,7 @@ tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids
   a2.out_scale = nullptr;
   a2.out_f32 = at<float>(ws, L, Layout::ROWS);
   d2.nseg = dp.nseg2;
+  d2.act_scaled = d1.out_act_scaled;
   d2.units_m = dp.units2;
   d2.blk_off = pa.blk_off2;
   if ((e = tmoe::dec_fc_warps(2, w4a8, layer->uniform_k, &d2.fc_warps)) != cudaSuccess)

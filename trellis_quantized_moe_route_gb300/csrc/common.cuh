@@ -264,11 +264,33 @@ __device__ __forceinline__ int e8m0_exponent(float amax) {
   return max(-127, min(127, e));
 }
 
+// MXFP8 blocks whose E8M0 exponent e lies in [-15, 7] can be held as fp16
+// values code * 2^e exactly (448 * 2^7 < 65504; the smallest code step
+// 2^-9 * 2^-15 is the fp16 subnormal step).
+constexpr int kE8m0PreLo = 127 - 15, kE8m0PreHi = 127 + 7;
+
 // 2^e as a float, exact for e in [-149, 127].
 __device__ __forceinline__ float exp2_int(int e) {
   if (e >= -126) return __uint_as_float((uint32_t)(e + 127) << 23);
   return __uint_as_float(1u << (e + 149));
 }
+
+// Four fp16 values (two half2 words) times 2^e, rounded to fp16 (exact when
+// the result is representable).
+__device__ __forceinline__ uint32_t f16x2_times_exp2(uint32_t c, int e) {
+  const float sc = exp2_int(max(-149, min(127, e)));
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&c));
+  __half2 r = __floats2half2_rn(a.x * sc, a.y * sc);
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint2 f16x4_times_exp2(uint2 c, int e) {
+  const float sc = exp2_int(max(-149, min(127, e)));
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&c.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&c.y));
+  __half2 ra = __floats2half2_rn(a.x * sc, a.y * sc), rb = __floats2half2_rn(b.x * sc, b.y * sc);
+  return make_uint2(*reinterpret_cast<uint32_t*>(&ra), *reinterpret_cast<uint32_t*>(&rb));
+}
+
 
 // ---------------------------------------------------------------------------
 // Warp-level MMA (legacy mma.sync) wrappers.

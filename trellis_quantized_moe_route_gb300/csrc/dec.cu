@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(1024) k_dec_prologue(const DecPrologueArgs a) 
   const int cta = blockIdx.x - 1;
   const int gw = cta * 32 + warp;
   if (a.w4a8)
-    rotate_quant_warp<true>(a.x, a.suh, a.T, a.H, a.rot_b, a.xq, a.xs, gw, nullptr, 0, true);
+    rotate_quant_warp<true>(a.x, a.suh, a.T, a.H, a.rot_b, a.xq, a.xs, gw, nullptr, 0, true, a.xq_scaled);
   else
     rotate_quant_warp<false>(a.x, a.suh, a.T, a.H, a.rot_b, a.xq, a.xs, gw);
   const long gtid = (long)cta * blockDim.x + tid, gstride = (long)nrot * blockDim.x;

@@ -149,7 +149,10 @@ __device__ __forceinline__ const unsigned char* dw_src(const DecArgs& d, const D
 
 // Expansion and MMAs of one item: acc (this lane's D fragment, rows g, g+8 of
 // the strip, slots 2q, 2q+1) over the item's k-steps.
-template <bool W4A8, int K>
+// PRE (W4A8): the activations are read as code * 2^e, so the MMAs accumulate
+// straight into acc with no per-block scaling (every block of the item has
+// its exponent in [-15, 7]; see dw_pre_issue).
+template <bool W4A8, bool PRE, int K>
 __device__ __forceinline__ void dw_compute(const DecArgs& d, const DwItem& it, int row,
                                            const unsigned char* wt, int kdim, float (&acc)[4]) {
   const FcArgs& a = d.f;
@@ -159,11 +162,11 @@ __device__ __forceinline__ void dw_compute(const DecArgs& d, const DwItem& it, i
   const int col0 = it.sg * kDecSeg;
   // activation fragment source: slot g's row, columns 32 ks + 16 tsel + 8 h
   const int arow = __shfl_sync(0xFFFFFFFFu, row, g);
-  const uint16_t* ap = reinterpret_cast<const uint16_t*>(a.act) + (size_t)(arow < 0 ? 0 : arow) * kdim + col0 +
+  const uint16_t* ap = (PRE ? d.act_scaled : reinterpret_cast<const uint16_t*>(a.act)) + (size_t)(arow < 0 ? 0 : arow) * kdim + col0 +
                        16 * tsel + 8 * h;
   // W4A8: E8M0 block exponents of slots 2q and 2q+1 for this segment
-  const int r0 = W4A8 ? __shfl_sync(0xFFFFFFFFu, row, 2 * q) : -1;
-  const int r1 = W4A8 ? __shfl_sync(0xFFFFFFFFu, row, 2 * q + 1) : -1;
+  const int r0 = (W4A8 && !PRE) ? __shfl_sync(0xFFFFFFFFu, row, 2 * q) : -1;
+  const int r1 = (W4A8 && !PRE) ? __shfl_sync(0xFFFFFFFFu, row, 2 * q + 1) : -1;
   const uint8_t* sp0 = a.act_scale + (size_t)(r0 < 0 ? 0 : r0) * (kdim >> 5) + (col0 >> 5);
   const uint8_t* sp1 = a.act_scale + (size_t)(r1 < 0 ? 0 : r1) * (kdim >> 5) + (col0 >> 5);
   const uint32_t k16 = 0x10000u + (uint32_t)(d.T >> 30);  // 65536, opaque to the compiler
@@ -206,7 +209,7 @@ __device__ __forceinline__ void dw_compute(const DecArgs& d, const DwItem& it, i
       }
       const uint32_t a0[4] = {wa[0], wb[0], wa[1], wb[1]};
       const uint32_t a1[4] = {wa[2], wb[2], wa[3], wb[3]};
-      if (W4A8) {
+      if (W4A8 && !PRE) {
         const float s0 = (r0 >= 0) ? exp2_int((int)__ldg(sp0 + ks) - 127) : 0.0f;
         const float s1 = (r1 >= 0) ? exp2_int((int)__ldg(sp1 + ks) - 127) : 0.0f;
         float dd[4] = {0.f, 0.f, 0.f, 0.f};
@@ -224,20 +227,51 @@ __device__ __forceinline__ void dw_compute(const DecArgs& d, const DwItem& it, i
   }
 }
 
-template <bool W4A8, int KB>
-__device__ __forceinline__ void dw_compute_any(const DecArgs& d, const DwItem& it, int row,
-                                               const unsigned char* wt, int kdim, float (&acc)[4]) {
+template <bool W4A8, bool PRE, int KB>
+__device__ __forceinline__ void dw_compute_k(const DecArgs& d, const DwItem& it, int row,
+                                             const unsigned char* wt, int kdim, float (&acc)[4]) {
   if (KB > 0) {
-    dw_compute<W4A8, (KB > 0 ? KB : 4)>(d, it, row, wt, kdim, acc);
+    dw_compute<W4A8, PRE, (KB > 0 ? KB : 4)>(d, it, row, wt, kdim, acc);
     return;
   }
   switch (it.k) {
-    case 2: dw_compute<W4A8, 2>(d, it, row, wt, kdim, acc); break;
-    case 3: dw_compute<W4A8, 3>(d, it, row, wt, kdim, acc); break;
-    case 4: dw_compute<W4A8, 4>(d, it, row, wt, kdim, acc); break;
-    case 5: dw_compute<W4A8, 5>(d, it, row, wt, kdim, acc); break;
-    default: dw_compute<W4A8, 6>(d, it, row, wt, kdim, acc); break;
+    case 2: dw_compute<W4A8, PRE, 2>(d, it, row, wt, kdim, acc); break;
+    case 3: dw_compute<W4A8, PRE, 3>(d, it, row, wt, kdim, acc); break;
+    case 4: dw_compute<W4A8, PRE, 4>(d, it, row, wt, kdim, acc); break;
+    case 5: dw_compute<W4A8, PRE, 5>(d, it, row, wt, kdim, acc); break;
+    default: dw_compute<W4A8, PRE, 6>(d, it, row, wt, kdim, acc); break;
   }
+}
+
+template <bool W4A8, int KB>
+__device__ __forceinline__ void dw_compute_any(const DecArgs& d, const DwItem& it, bool pre, int row,
+                                               const unsigned char* wt, int kdim, float (&acc)[4]) {
+  if (W4A8 && pre)
+    dw_compute_k<W4A8, true, KB>(d, it, row, wt, kdim, acc);
+  else
+    dw_compute_k<W4A8, false, KB>(d, it, row, wt, kdim, acc);
+}
+
+// W4A8: the E8M0 exponents an item reads (its valid slots x its 32-column
+// blocks), two per lane (lane l: slot l/4, blocks 2(l%4) and 2(l%4)+1),
+// loaded one item ahead; dw_pre_final says whether all lie in [-15, 7].
+__device__ __forceinline__ uint32_t dw_pre_issue(const DecArgs& d, const DwItem& it, int row, int kdim, int lane) {
+  const int n = lane >> 2, b0 = 2 * (lane & 3);
+  const int r = __shfl_sync(0xFFFFFFFFu, row, n);
+  const int nb = it.ncols >> 5;
+  uint32_t lo = 127u, hi = 127u;
+  if (r >= 0) {
+    const uint8_t* sp = d.f.act_scale + (size_t)r * (kdim >> 5) + it.sg * kDwSteps + b0;
+    if (b0 < nb) lo = __ldg(sp);
+    if (b0 + 1 < nb) hi = __ldg(sp + 1);
+  }
+  return lo | (hi << 8);
+}
+__device__ __forceinline__ bool dw_pre_final(uint32_t v) {
+  const uint32_t lo = v & 0xFFu, hi = v >> 8;
+  const bool ok = lo >= (uint32_t)kE8m0PreLo && lo <= (uint32_t)kE8m0PreHi && hi >= (uint32_t)kE8m0PreLo &&
+                  hi <= (uint32_t)kE8m0PreHi;
+  return __all_sync(0xFFFFFFFFu, ok);
 }
 
 // ---------------------------------------------------------------------------
@@ -383,9 +417,13 @@ __device__ __forceinline__ void dw_epilogue_fc1(const DecArgs& d, int rb, int mb
       for (int o = 1; o < LPB; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
       const int ex = e8m0_exponent(amax);
       const float inv = exp2_int(-ex);
+      uint16_t* zs = d.out_act_scaled + (size_t)slot * a.I + c0;
 #pragma unroll
-      for (int p = 0; p < PER; p += 2)
-        *reinterpret_cast<uint32_t*>(z + p) = e4m3x2_to_f16x2(e4m3x2_from_float2(av[p] * inv, av[p + 1] * inv));
+      for (int p = 0; p < PER; p += 2) {
+        const uint32_t c = e4m3x2_to_f16x2(e4m3x2_from_float2(av[p] * inv, av[p + 1] * inv));
+        *reinterpret_cast<uint32_t*>(z + p) = c;
+        *reinterpret_cast<uint32_t*>(zs + p) = f16x2_times_exp2(c, ex);
+      }
       if ((lane % LPB) == 0) a.out_scale[(size_t)slot * (a.I >> 5) + (c0 >> 5)] = (uint8_t)(ex + 127);
     }
   }
@@ -503,6 +541,7 @@ __global__ void __launch_bounds__(kDwThreads, KB > 0 ? 6 : 4) k_dec_warp(const D
   DwMetaW m{}, nm{};
   DwRaw raw1{-1, 0}, raw2{-1, 0};
   bool has1 = false, has2 = false;
+  uint32_t pre_cur = 0, pre_next = 0;
   if (any) {
     pc = h;
     h += nwarps;
@@ -519,13 +558,15 @@ __global__ void __launch_bounds__(kDwThreads, KB > 0 ? 6 : 4) k_dec_warp(const D
     dw_copy_any(KB > 0 ? KB : it.k, ring, dw_src(d, m, it, kdim), it.ncols >> 4, lane);
   }
   cp_async_commit();
-  if (PROJ == 2) dw_griddep_wait();  // z~ and the partial buffer belong to the predecessors until now
+  if (PROJ == 2) dw_griddep_wait();  // z~, its exponents and the partial buffer belong to the predecessors until now
   dw_griddep_launch();
   if (!any) return;
+  if (W4A8) pre_cur = dw_pre_issue(d, it, m.row, kdim, lane);
   if (has1) {
     nit = dw_item(d, pn, nstrips, kdim);
     nm = dw_meta_final<PROJ>(raw1, nit.rb, lane, a.topk);
     dw_item_meta(nit, nm);
+    if (W4A8) pre_next = dw_pre_issue(d, nit, nm.row, kdim, lane);
     has2 = h < h1;
     if (has2) {
       pn2 = h;
@@ -541,7 +582,8 @@ __global__ void __launch_bounds__(kDwThreads, KB > 0 ? 6 : 4) k_dec_warp(const D
     __syncwarp();
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    dw_compute_any<W4A8, KB>(d, it, m.row, ring + (n & 1) * slot_bytes, kdim, acc);
+    const bool pre = W4A8 && dw_pre_final(pre_cur);
+    dw_compute_any<W4A8, KB>(d, it, pre, m.row, ring + (n & 1) * slot_bytes, kdim, acc);
 
     // partial sums of the valid slots, [slot][16 rows]
     const int g = lane >> 2, c = 2 * (lane & 3);
@@ -559,12 +601,14 @@ __global__ void __launch_bounds__(kDwThreads, KB > 0 ? 6 : 4) k_dec_warp(const D
     pc = pn;
     it = nit;
     m = nm;
+    pre_cur = pre_next;
     has1 = has2;
     if (has1) {
       pn = pn2;
       nit = dw_item(d, pn, nstrips, kdim);
       nm = dw_meta_final<PROJ>(raw2, nit.rb, lane, a.topk);
       dw_item_meta(nit, nm);
+      if (W4A8) pre_next = dw_pre_issue(d, nit, nm.row, kdim, lane);
       has2 = h < h1;
       if (has2) {
         pn2 = h;

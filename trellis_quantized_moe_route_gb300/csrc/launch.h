@@ -61,6 +61,7 @@ struct DecPrologueArgs {
   const uint16_t* suh;      // fp16 [H]
   int T, H, topk, rot_b, w4a8;
   void* xq;                 // fp16 [T, H] (W4A8: the E4M3 codes, as fp16)
+  uint16_t* xq_scaled;      // W4A8: fp16 [T, H] code * 2^e (exact where e in [-15, 7])
   uint8_t* xs;              // E8M0 [T, H/32]
   int32_t* zero_i32;        // counters to clear
   int n_zero_i32;
@@ -83,6 +84,8 @@ constexpr int kDecBlock = 8;  // slots per route block
 
 struct DecArgs {
   FcArgs f;                 // act: fp16 rows (W4A8: E4M3 codes as fp16, E8M0 scales in act_scale)
+  const uint16_t* act_scaled;  // W4A8: the same rows as code * 2^e (used where every e is in [-15, 7])
+  uint16_t* out_act_scaled;    // FC1 W4A8: z~ as code * 2^e
   const int32_t* blk_meta;  // per route block: expert | bits << 16 | valid slots << 24
   const long long* blk_off; // per route block: byte offset of the expert's payload (this projection)
   int nseg;                 // contraction segments of kDecSeg columns

@@ -8,7 +8,8 @@ namespace tmoe {
 
 // One warp per (token, 128-wide chunk of H); lane l holds entries 4l..4l+3.
 // Outputs: fp16 x~ [T][H] (W4A16), E4M3 codes [T][H] + E8M0 scales (W4A8;
-// with `f16_codes` each code is stored as the fp16 number it encodes).
+// with `f16_codes` each code is stored as the fp16 number it encodes, and
+// `xq_scaled`, if given, receives code * 2^e as fp16, exact for e in [-15, 7]).
 // With `slot_of_route` the row is stored as fp16 once per route of the token,
 // at the route's slot (x~ in slot order, [slots][H]); W4A8 then stores the
 // exact dequantized MXFP8 values code * 2^e.
@@ -17,7 +18,8 @@ static __device__ __forceinline__ void rotate_quant_warp(const uint16_t* __restr
                                                          const uint16_t* __restrict__ suh, int T, int H, int rot_b,
                                                          void* __restrict__ xq, uint8_t* __restrict__ xs, int gw,
                                                          const int32_t* __restrict__ slot_of_route = nullptr,
-                                                         int topk = 0, bool f16_codes = false) {
+                                                         int topk = 0, bool f16_codes = false,
+                                                         uint16_t* __restrict__ xq_scaled = nullptr) {
   const int lane = threadIdx.x & 31;
   const int chunks = H >> 7;
   if (gw >= T * chunks) return;
@@ -76,10 +78,11 @@ static __device__ __forceinline__ void rotate_quant_warp(const uint16_t* __restr
     const int e = e8m0_exponent(amax);
     const float inv = exp2_int(-e);
     const uint32_t q0 = e4m3x2_from_float2(v[0] * inv, v[1] * inv), q1 = e4m3x2_from_float2(v[2] * inv, v[3] * inv);
-    if (f16_codes)  // the E4M3 codes held exactly as fp16
-      *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(xq) + base) =
-          make_uint2(e4m3x2_to_f16x2(q0), e4m3x2_to_f16x2(q1));
-    else
+    if (f16_codes) {  // the E4M3 codes held exactly as fp16
+      const uint2 c = make_uint2(e4m3x2_to_f16x2(q0), e4m3x2_to_f16x2(q1));
+      *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(xq) + base) = c;
+      if (xq_scaled) *reinterpret_cast<uint2*>(xq_scaled + base) = f16x4_times_exp2(c, e);
+    } else
       *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(xq) + base) = q0 | (q1 << 16);
     if ((lane & 7) == 0) xs[(size_t)t * (H >> 5) + (size_t)c * 4 + (lane >> 3)] = (uint8_t)(e + 127);
   }
