@@ -34,58 +34,6 @@ struct DecRouteSmem {
   int ids[1024];
 };
 
-// Orderable key of a finite float (larger float, larger key; -0 as +0) and back.
-__device__ __forceinline__ uint32_t dec_key(float f) {
-  const uint32_t b = __float_as_uint(f + 0.0f);
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-__device__ __forceinline__ float dec_unkey(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-
-// Top-k softmax of one token's logits by one warp: k rounds of a warp-wide
-// max of the remaining keys, ties to the lowest expert id; weights
-// exp(l - l_max) / sum over the selected, summed in selection order.
-__device__ __forceinline__ void dec_route_token(const float* __restrict__ row, int E, int k, int t,
-                                                int32_t* __restrict__ ids, float* __restrict__ w, int* s_ids) {
-  const int lane = threadIdx.x & 31;
-  uint32_t key[kMaxExperts / 32];
-#pragma unroll
-  for (int i = 0; i < kMaxExperts / 32; ++i) {
-    const int e = lane + 32 * i;
-    key[i] = (e < E) ? dec_key(__ldg(row + e)) : 0u;  // 0: absent or taken
-  }
-  float best0 = 0.0f, wsum = 0.0f, my_w = 0.0f;
-  int my_id = 0;
-  for (int j = 0; j < k; ++j) {
-    uint32_t lm = 0;
-#pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i) lm = max(lm, key[i]);
-    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, lm);
-    uint32_t lid = 0xFFFFFFFFu;
-#pragma unroll
-    for (int i = kMaxExperts / 32 - 1; i >= 0; --i)
-      if (key[i] == m) lid = lane + 32 * i;
-    const uint32_t id = __reduce_min_sync(0xFFFFFFFFu, lid);
-#pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i)
-      if (lane + 32 * i == (int)id) key[i] = 0u;
-    const float bv = dec_unkey(m);
-    if (j == 0) best0 = bv;
-    const float ex = __expf(bv - best0);
-    wsum += ex;
-    if (lane == j) {
-      my_id = (int)id;
-      my_w = ex;
-    }
-  }
-  if (lane < k) {
-    ids[(size_t)t * k + lane] = my_id;
-    w[(size_t)t * k + lane] = my_w / wsum;
-    s_ids[t * k + lane] = my_id;
-  }
-}
-
 __device__ __forceinline__ void dec_route_map(const DecPrologueArgs& a, DecRouteSmem& sm) {
   const RouteMapArgs& r = a.rm;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -99,7 +47,7 @@ __device__ __forceinline__ void dec_route_map(const DecPrologueArgs& a, DecRoute
   const int nw = (R + 31) / 32;  // warps holding routes
   for (int i = tid; i < nw * E; i += blockDim.x) sm.cnt[i / E][i % E] = 0;
   if (a.logits) {
-    for (int t = warp; t < a.T; t += 32) dec_route_token(a.logits + (size_t)t * E, E, a.topk, t, a.ids_out, a.w_out, sm.ids);
+    for (int t = warp; t < a.T; t += 32) route_token_redux(a.logits + (size_t)t * E, E, a.topk, t, a.ids_out, a.w_out, sm.ids);
   } else {
     for (int i = tid; i < R; i += blockDim.x) sm.ids[i] = r.ids[i];
   }

@@ -21,7 +21,7 @@ __global__ void __launch_bounds__(256) k_route_topk(const float* __restrict__ lo
                                                     int32_t* __restrict__ ids, float* __restrict__ w) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (warp >= T) return;
-  route_token_warp(logits, warp, E, k, ids, w);
+  route_token_redux(logits + (size_t)warp * E, E, k, warp, ids, w);
 }
 
 

@@ -6,61 +6,58 @@
 
 namespace tmoe {
 
-// ---------------------------------------------------------------------------
-// Router: one warp per token.
-// ---------------------------------------------------------------------------
-// Top-k of token t's logits (E <= 256) by the calling warp; writes ids and
-// weights of row t.
-static __device__ __forceinline__ void route_token_warp(const float* __restrict__ logits, int t, int E, int k,
-                                                        int32_t* __restrict__ ids, float* __restrict__ w) {
-  const int warp = t;
+// Orderable key of a finite float (larger float, larger key; -0 as +0) and back.
+static __device__ __forceinline__ uint32_t route_key(float f) {
+  const uint32_t b = __float_as_uint(f + 0.0f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+static __device__ __forceinline__ float route_unkey(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Top-k softmax of one token's logits by one warp: k rounds of a warp-wide
+// max of the remaining keys, ties to the lowest expert id; weights
+// exp(l - l_max) / sum over the selected, summed in selection order.
+static __device__ __forceinline__ void route_token_redux(const float* __restrict__ row, int E, int k, int t,
+                                                int32_t* __restrict__ ids, float* __restrict__ w, int* s_ids = nullptr) {
   const int lane = threadIdx.x & 31;
-  const float* row = logits + (size_t)warp * E;
-  float v[8];
-  uint32_t taken = 0;
+  uint32_t key[kMaxExperts / 32];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < kMaxExperts / 32; ++i) {
     const int e = lane + 32 * i;
-    v[i] = (e < E) ? row[e] : 0.0f;
-    if (e >= E) taken |= 1u << i;
+    key[i] = (e < E) ? route_key(__ldg(row + e)) : 0u;  // 0: absent or taken
   }
   float best0 = 0.0f, wsum = 0.0f, my_w = 0.0f;
   int my_id = 0;
   for (int j = 0; j < k; ++j) {
-    // lane-local best: larger value, then lower id
-    float bv = -INFINITY;
-    int bid = 0x7FFFFFFF;
+    uint32_t lm = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      if (!(taken & (1u << i)) && (v[i] > bv || (v[i] == bv && e < bid) || bid == 0x7FFFFFFF)) {
-        bv = v[i];
-        bid = e;
-      }
-    }
+    for (int i = 0; i < kMaxExperts / 32; ++i) lm = max(lm, key[i]);
+    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, lm);
+    uint32_t lid = 0xFFFFFFFFu;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-      const int oid = __shfl_xor_sync(0xFFFFFFFFu, bid, o);
-      if (oid != 0x7FFFFFFF && (bid == 0x7FFFFFFF || ov > bv || (ov == bv && oid < bid))) {
-        bv = ov;
-        bid = oid;
-      }
-    }
-    if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
+    for (int i = kMaxExperts / 32 - 1; i >= 0; --i)
+      if (key[i] == m) lid = lane + 32 * i;
+    const uint32_t id = __reduce_min_sync(0xFFFFFFFFu, lid);
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i)
+      if (lane + 32 * i == (int)id) key[i] = 0u;
+    const float bv = route_unkey(m);
     if (j == 0) best0 = bv;
     const float ex = __expf(bv - best0);
     wsum += ex;
     if (lane == j) {
-      my_id = bid;
+      my_id = (int)id;
       my_w = ex;
     }
   }
   if (lane < k) {
-    ids[(size_t)warp * k + lane] = my_id;
-    w[(size_t)warp * k + lane] = my_w / wsum;
+    ids[(size_t)t * k + lane] = my_id;
+    w[(size_t)t * k + lane] = my_w / wsum;
+    if (s_ids) s_ids[t * k + lane] = my_id;
   }
 }
+
 
 // ---------------------------------------------------------------------------
 // Route map. A "tile" is 1024 consecutive routes, one per thread.
@@ -119,10 +116,18 @@ static __device__ __forceinline__ void scan_experts(int E, int ntiles, int block
   const int tid = threadIdx.x;
   for (int e = tid; e < E; e += blockDim.x) {
     int run = 0;
-    for (int t = 0; t < ntiles; ++t) {
-      const int c = tile_counts[(size_t)t * E + e];
-      tile_counts[(size_t)t * E + e] = run;  // becomes the tile's base within the expert
-      run += c;
+    // sixteen tiles' counts in flight at a time, then their bases written
+    for (int t0 = 0; t0 < ntiles; t0 += 16) {
+      int c[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) c[u] = (t0 + u < ntiles) ? tile_counts[(size_t)(t0 + u) * E + e] : 0;
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        if (t0 + u < ntiles) {
+          tile_counts[(size_t)(t0 + u) * E + e] = run;  // becomes the tile's base within the expert
+          run += c[u];
+        }
+      }
     }
     counts[e] = run;
     s_pad[e] = (run + block - 1) / block;  // route blocks of this expert
