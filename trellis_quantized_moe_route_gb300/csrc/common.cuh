@@ -132,10 +132,20 @@ __device__ __forceinline__ void run_mcg_k4(uint32_t prev_raw, uint32_t cur_raw, 
   }
 }
 
-// Weights from raw codebook words: fp16 pairs (w0,w1) .. (w6,w7).
+// Weights from raw codebook words: fp16 pairs (w0,w1) .. (w6,w7). Each
+// word's halves are summed by one fp16x2 add of its low and high halves
+// (both lanes hold the sum), and one byte permute joins two such sums; on
+// sm_103 this costs fewer integer-pipe instructions than permuting the
+// words' halves first (measured).
 __device__ __forceinline__ void raw_to_f16(const uint32_t (&y)[8], uint32_t (&w)[4]) {
 #pragma unroll
-  for (int p = 0; p < 4; ++p) w[p] = cb_pair_from_raw(y[2 * p], y[2 * p + 1]);
+  for (int p = 0; p < 4; ++p) {
+    const __half2 va = *reinterpret_cast<const __half2*>(&y[2 * p]);
+    const __half2 vb = *reinterpret_cast<const __half2*>(&y[2 * p + 1]);
+    __half2 da = __hadd2(__low2half2(va), __high2half2(va));
+    __half2 db = __hadd2(__low2half2(vb), __high2half2(vb));
+    w[p] = __byte_perm(*reinterpret_cast<uint32_t*>(&da), *reinterpret_cast<uint32_t*>(&db), 0x5410);
+  }
 }
 
 // fp16x2 -> two E4M3 bytes with the native conversion instruction.
