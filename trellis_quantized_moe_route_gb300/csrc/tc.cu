@@ -49,13 +49,20 @@
 namespace tmoe {
 
 constexpr int kTcThreads = 640;        // warpgroups: 2 expander, 2 epilogue, 1 loader/issuer
-// Registers per thread after the split: expanders keep the launch count, the
-// loader/issuer warpgroup gives registers up, the epilogue warpgroups take
-// them (sum x 128 threads <= 640 x 96, the launch budget: the kernel must be
-// compiled at 96 registers, which the launcher checks, or setmaxnreg.inc
-// could wait for registers never freed).
-constexpr int kRegExp = 96, kRegEpi = 128, kRegAux = 32, kRegLaunch = 96;
-static_assert(128 * (2 * kRegExp + 2 * kRegEpi + kRegAux) <= kTcThreads * kRegLaunch, "register split over budget");
+// Registers per thread after the split: the expander and loader/issuer
+// warpgroups give registers up, the epilogue warpgroups take them (sum x 128
+// threads <= 640 x 96, the launch budget: the kernel must be compiled at 96
+// registers, which the launcher checks, or setmaxnreg.inc could wait for
+// registers never freed). With the K=4 expansion the expanders fit in 56 and
+// the FC1 epilogue needs 168 to run without spilling; the general-K
+// expanders keep the launch count.
+constexpr int kRegAux = 32, kRegLaunch = 96;
+template <int KB>
+struct TcRegs {
+  static constexpr int exp = KB > 0 ? 56 : 96;
+  static constexpr int epi = KB > 0 ? 168 : 128;
+  static_assert(128 * (2 * exp + 2 * epi + kRegAux) <= kTcThreads * kRegLaunch, "register split over budget");
+};
 constexpr int kTcExp = 256;            // expander threads
 constexpr int kTcEpiWarps = 8;         // two per TMEM lane quarter, one per column half
 constexpr int kEvecBytes = 1024;       // per epilogue warp: its half of the unit's folded vectors (fp32)
@@ -852,9 +859,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__
   volatile int* abort = &s_abort;
   volatile int* uring = s_uring;
   if (warp < 8) {
-    tc_expanders<PROJ, KB, NR, W4A8>(args, G, uring, bars, wring, bring, abort);  // at the launch count
+    if (TcRegs<KB>::exp < kRegLaunch) regs_dec<TcRegs<KB>::exp>();
+    tc_expanders<PROJ, KB, NR, W4A8>(args, G, uring, bars, wring, bring, abort);
   } else if (warp < 16) {
-    regs_inc<kRegEpi>();
+    regs_inc<TcRegs<KB>::epi>();
     tc_epilogue<PROJ, KB, NR, W4A8>(args, G, uring, bars, reinterpret_cast<float*>(evec + (warp - 8) * kEvecBytes),
                                     reinterpret_cast<uint32_t*>(evec + kTcEpiWarps * kEvecBytes + (warp - 8) * kStageBytes),
                                     tmem, abort);
