@@ -383,6 +383,7 @@ __device__ __forceinline__ void dw_epilogue_fc1(const DecArgs& d, int rb, int mb
     dw_ld_h<PER>(rt + c0, vg_);
     dw_ld_h<PER>(rt + a.I + c0, vu_);
     dw_ld_h<PER>(rt + 2 * a.I + c0, vd_);
+    dw_griddep_wait();  // the partial sums come from the predecessor
     dw_sum_parts2<PER>(d, rb, strip_g, strip_u, nstrips, n, r16, gv, uv);
 #pragma unroll
     for (int p = 0; p < PER; ++p) {
@@ -463,6 +464,7 @@ __device__ __forceinline__ void dw_epilogue_fc2(const DecArgs& d, int t, int mb,
       dw_ld_h<4>(a.scale + (size_t)(ok ? ex[u] : 0) * a.H + h0, sc[u]);
       dw_ld_h<4>(a.rot_tab + (size_t)(ok ? ex[u] : 0) * a.H + h0, sv[u]);
     }
+    if (j0 == 0) dw_griddep_wait();  // the partial sums come from the predecessor
     // partial sums of the four routes, two segments at a time
 #pragma unroll
     for (int u = 0; u < 4; ++u)
@@ -624,7 +626,9 @@ __global__ void __launch_bounds__(kDwThreads, KB > 0 ? 6 : 4) k_dec_warp(const D
 // intermediate channels, slot), FC2 one warp per (token, 128 output channels).
 template <bool W4A8, int PROJ>
 __global__ void __launch_bounds__(256) k_dec_epi(const DecArgs d) {
-  dw_griddep_wait();  // the partial sums come from the predecessor
+  // (the route map and block table come from the prologue, complete before
+  // this grid could start; each epilogue waits for its predecessor only
+  // before it reads the partial sums)
   dw_griddep_launch();
   const FcArgs& a = d.f;
   const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
