@@ -44,7 +44,7 @@ __device__ __forceinline__ float4 h4_to_f4(uint2 p) {
 
 constexpr int kCombineMaxK = 32;
 
-__global__ void __launch_bounds__(256) k_combine_unrot(CombineUnrotArgs a) {
+__global__ void __launch_bounds__(256, 3) k_combine_unrot(CombineUnrotArgs a) {
   const int lane = threadIdx.x & 31;
   const int chunks = (a.H + 255) >> 8;
   const long wid = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -65,7 +65,8 @@ __global__ void __launch_bounds__(256) k_combine_unrot(CombineUnrotArgs a) {
   float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
   // four routes at a time: their loads are issued before any is used
   for (int j0 = 0; j0 < a.k; j0 += 4) {
-    float4 va[4], vb[4], ga[4], gb[4];
+    float4 va[4], vb[4];
+    uint2 ga[4], gb[4];
     int slot[4];
     float wj[4];
 #pragma unroll
@@ -75,26 +76,28 @@ __global__ void __launch_bounds__(256) k_combine_unrot(CombineUnrotArgs a) {
       wj[u] = __shfl_sync(0xFFFFFFFFu, my_w, j & 31);
       const int e = __shfl_sync(0xFFFFFFFFu, my_e, j & 31);
       if (j >= a.k) slot[u] = -1;
-      va[u] = vb[u] = ga[u] = gb[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      va[u] = vb[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      ga[u] = gb[u] = make_uint2(0u, 0u);
       if (slot[u] >= 0 && live) {  // (a dropped, out-of-range expert id has no slot)
         const float* r = a.rows + (size_t)slot[u] * a.H + c0;
         const uint16_t* g = a.svh + (size_t)e * a.H + c0;
         va[u] = __ldcs(reinterpret_cast<const float4*>(r));
         vb[u] = __ldcs(reinterpret_cast<const float4*>(r + 64));
-        ga[u] = h4_to_f4(__ldg(reinterpret_cast<const uint2*>(g)));
-        gb[u] = h4_to_f4(__ldg(reinterpret_cast<const uint2*>(g + 64)));
+        ga[u] = __ldg(reinterpret_cast<const uint2*>(g));
+        gb[u] = __ldg(reinterpret_cast<const uint2*>(g + 64));
       }
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       if (slot[u] < 0) continue;  // warp-uniform
+      const float4 fa = h4_to_f4(ga[u]), fb = h4_to_f4(gb[u]);
       float4 x = va[u], y = vb[u];
       if (across) {
         x = make_float4(va[u].x + vb[u].x, va[u].y + vb[u].y, va[u].z + vb[u].z, va[u].w + vb[u].w);
         y = make_float4(va[u].x - vb[u].x, va[u].y - vb[u].y, va[u].z - vb[u].z, va[u].w - vb[u].w);
       }
-      x = make_float4(x.x * (hs * ga[u].x), x.y * (hs * ga[u].y), x.z * (hs * ga[u].z), x.w * (hs * ga[u].w));
-      y = make_float4(y.x * (hs * gb[u].x), y.y * (hs * gb[u].y), y.z * (hs * gb[u].z), y.w * (hs * gb[u].w));
+      x = make_float4(x.x * (hs * fa.x), x.y * (hs * fa.y), x.z * (hs * fa.z), x.w * (hs * fa.w));
+      y = make_float4(y.x * (hs * fb.x), y.y * (hs * fb.y), y.z * (hs * fb.z), y.w * (hs * fb.w));
       lo = make_float4(fmaf(wj[u], x.x, lo.x), fmaf(wj[u], x.y, lo.y), fmaf(wj[u], x.z, lo.z), fmaf(wj[u], x.w, lo.w));
       hi = make_float4(fmaf(wj[u], y.x, hi.x), fmaf(wj[u], y.y, hi.y), fmaf(wj[u], y.z, hi.z), fmaf(wj[u], y.w, hi.w));
     }

@@ -27,6 +27,8 @@ static __device__ __forceinline__ void rotate_quant_warp(const uint16_t* __restr
   const size_t base = (size_t)t * H + (size_t)c * 128 + 4 * lane;
   const uint2 xr = __ldg(reinterpret_cast<const uint2*>(x + base));
   const uint2 sr = __ldg(reinterpret_cast<const uint2*>(suh + (size_t)c * 128 + 4 * lane));
+  // the token's slots (topk <= 32), one per lane, fetched with x
+  const int my_slot = (slot_of_route != nullptr && lane < topk) ? slot_of_route[(size_t)t * topk + lane] : -1;
   float v[4];
   const uint32_t xw[2] = {xr.x, xr.y};
   const uint32_t sw[2] = {sr.x, sr.y};
@@ -65,7 +67,7 @@ static __device__ __forceinline__ void rotate_quant_warp(const uint16_t* __restr
       *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(xq) + base) = o;
     } else {
       for (int k = 0; k < topk; ++k) {
-        const int slot = slot_of_route[(size_t)t * topk + k];
+        const int slot = __shfl_sync(0xFFFFFFFFu, my_slot, k);
         if (slot >= 0)
           *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(xq) + (size_t)slot * H + (size_t)c * 128 + 4 * lane) = o;
       }

@@ -825,7 +825,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__
   unsigned char* evec = wring + kSW * tc_wslot_bytes(kmax);
   const int tid = threadIdx.x, warp = tid >> 5;
   const TcGeom<PROJ, NR> G(args);
-  const int units = *args.f.nblocks * G.mblocks;
   if (tid == 0) {
     for (int i = 0; i < kSA; ++i) {
       mbar_init(&bars.fullA[i], 1);   // the loader's expect_tx arrival; the gathers complete the bytes
@@ -855,6 +854,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  const int units = *args.f.nblocks * G.mblocks;
   const uint32_t tmem = tmem_slot;
   volatile int* abort = &s_abort;
   volatile int* uring = s_uring;
