@@ -340,6 +340,7 @@ DECODE_SHAPES = [
     dict(T=8, E=64, topk=8, bits=(5,), H=512, I=256),                        # generic K=5 decode
     dict(T=2, E=16, topk=3, rot_block_h=1, rot_block_i=1),                   # identity rotations
     dict(T=1, E=8, topk=8, H=1024, I=512),                                   # every expert, one token
+    dict(T=120, E=256, topk=8, H=256, I=128),                                # 960 routes: the regime's largest block table
 ]
 
 
