@@ -150,13 +150,13 @@ __device__ __forceinline__ uint64_t global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// One potentially blocking test: the thread sleeps until the phase completes
-// or about `kSuspendNs` pass, instead of spinning.
-constexpr uint32_t kSuspendNs = 20000;
+// One potentially blocking test of the phase (the hardware's own time limit;
+// an explicit suspend hint of 20 us made the pipeline's hand-offs measurably
+// slower to wake up).
 __device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
   uint32_t done;
-  asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, p;\n}\n"
-               : "=r"(done) : "r"(a), "r"(parity), "n"(kSuspendNs) : "memory");
+  asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+               : "=r"(done) : "r"(a), "r"(parity) : "memory");
   return done != 0;
 }
 // Wait for the phase with the given parity. Gives up when `*abort` is set or
