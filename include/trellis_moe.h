@@ -127,7 +127,19 @@ tm_status trellis_moe_forward_logits(tm_layer* layer, const uint16_t* x, const f
 /* As forward_logits, but x_host, logits_host and out_host are HOST buffers
  * (pinned memory recommended). Copies the inputs into the workspace, runs the
  * layer and copies the result back, all on `stream`, then synchronises the
- * stream. Workspace: trellis_moe_workspace_size(layer, T) bytes. */
+ * stream. Workspace: trellis_moe_workspace_size(layer, T) bytes.
+ * When all three buffers are page-locked and mapped into the device's address
+ * space (pinned memory under unified addressing; x_host 8-byte and out_host
+ * 16-byte aligned) and the layer is deterministic, no staging copies are made:
+ * the kernels read x and the logits and write the result over the host link
+ * (NVLink-C2C on Grace systems) themselves, the same bytes in each direction.
+ * The handle then also remembers the buffer set (x_host, logits_host,
+ * out_host, workspace, T, mode): its second call captures the layer as a CUDA
+ * graph on a private stream and later calls launch that graph on `stream`.
+ * Each call reads the buffers' contents at that call. Up to 16 sets are kept,
+ * least recently used evicted; set_stage_events and destroy free them; the
+ * cache is guarded by a mutex. Otherwise the inputs are copied into the
+ * workspace and the result out of it on `stream`. */
 tm_status trellis_moe_forward_host(tm_layer* layer, const uint16_t* x_host,
                                    const float* logits_host, int32_t T, int32_t mode,
                                    float* out_host, void* workspace, size_t workspace_bytes,
@@ -179,9 +191,9 @@ tm_status trellis_moe_workspace_region(const tm_layer* layer, int32_t T, int32_t
 
 /* Stage timing for benchmarks and profilers. With `events` non-NULL (n = 7
  * cudaEvent_t handles created by the caller, NULL entries skipped), every later
- * forward call on this handle records events[i] on its stream, with
- * cudaEventRecordExternal so that the records also become nodes of a captured
- * CUDA graph, at these boundaries: 0 start, 1 after the router (forward_logits
+ * forward call on this handle records events[i] on its stream (inside a stream
+ * capture with cudaEventRecordExternal, so that the records become nodes of the
+ * captured CUDA graph; otherwise as a plain record), at these boundaries: 0 start, 1 after the router (forward_logits
  * and forward_host only), 2 after the route map, 3 after rotate+quantize,
  * 4 after FC1, 5 after FC2, 6 after the combine. In the decode-rows path the
  * router, route map and rotation are one kernel (1..3 follow it together),

@@ -242,6 +242,52 @@ def test_forward_host_matches_device_call():
     assert torch.equal(dev, oh)
 
 
+@pytest.mark.parametrize("T,mode", [(8, "w4a8"), (20, "w4a16")])
+def test_forward_host_graph_replay_reads_current_buffers(T, mode):
+    """The host-buffer call runs directly on the first use of a buffer set,
+    captures a graph on the second and replays it afterwards: every call must
+    read the pinned inputs as they are at that call, and a change of the stage
+    events (which the captured graph records) must not leave a stale graph."""
+    cfg = small_cfg(T=T)
+    L = synth.make_layer(cfg)
+    moe = _moe(L, cfg.T)
+    xh = torch.empty((T, cfg.H), dtype=torch.int16).pin_memory()
+    lh = torch.empty((T, cfg.E), dtype=torch.float32).pin_memory()
+    oh = torch.empty((T, cfg.H), dtype=torch.float32).pin_memory()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+    for call, seed in enumerate((5, 6, 7, 6, 8, 9)):
+        x_bits, logits = synth.make_tokens(cfg, seed=seed)
+        x, lg = upload_tokens(x_bits, logits)
+        want = moe.forward_logits(x, lg, mode=mode).cpu()
+        xh.copy_(torch.from_numpy(x_bits.view(np.int16).copy()))
+        lh.copy_(torch.from_numpy(logits.copy()))
+        if call == 4:
+            moe.set_stage_events(ev)
+        oh.fill_(float("nan"))
+        moe.forward_host(xh, lh, oh, mode=mode)
+        assert torch.equal(want, oh), call
+        if call == 4:
+            assert ev[6].query() and ev[0].elapsed_time(ev[6]) > 0
+            moe.set_stage_events(None)
+    # pageable buffers take the direct path
+    x_bits, logits = synth.make_tokens(cfg, seed=10)
+    x, lg = upload_tokens(x_bits, logits)
+    want = moe.forward_logits(x, lg, mode=mode).cpu()
+    xp = torch.from_numpy(x_bits.view(np.int16).copy())
+    lp = torch.from_numpy(logits.copy())
+    op = torch.empty((T, cfg.H), dtype=torch.float32)
+    moe.forward_host(xp, lp, op, mode=mode)
+    assert torch.equal(want, op)
+    # the atomic combine keeps the staged copies on pinned buffers too
+    moa = _moe(L, cfg.T, deterministic=False)
+    xh.copy_(xp)
+    lh.copy_(lp)
+    for _ in range(3):
+        oh.fill_(float("nan"))
+        moa.forward_host(xh, lh, oh, mode=mode)
+        assert torch.allclose(want, oh, rtol=1e-5, atol=1e-5)
+
+
 def test_auto_mode_switches_at_decode_rows():
     cfg = small_cfg(T=16)
     L = synth.make_layer(cfg)

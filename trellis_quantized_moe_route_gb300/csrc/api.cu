@@ -11,6 +11,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
 #include <vector>
 
 #include "../../include/trellis_moe.h"
@@ -26,6 +27,25 @@ struct tm_layer {
   uint8_t* d_bits;     // [E]
   int device;
   cudaEvent_t stage_ev[7];  // optional stage-boundary events (NULL = off)
+  // Host-buffer calls on mapped page-locked buffers replay a captured graph of
+  // the layer once the same buffers come back; one entry per buffer set, least
+  // recently used evicted. exec == NULL: seen once, not captured yet (or the
+  // capture failed).
+  struct HostGraph {
+    const void* x;
+    const void* logits;
+    void* out;
+    void* ws;
+    int T;
+    int mode;
+    bool failed;
+    uint64_t used;
+    cudaGraphExec_t exec;
+  };
+  std::mutex graph_mu;
+  std::vector<HostGraph> graphs;
+  uint64_t graph_clock = 0;
+  cudaStream_t capture_stream = nullptr;  // private stream the graphs are captured on
 };
 
 namespace {
@@ -44,10 +64,23 @@ tm_status cuda_fail(cudaError_t e, const char* what) {
   return fail(TM_ECUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-// Records stage-boundary event i if the caller asked for it.
+// Records stage-boundary event i if the caller asked for it: inside a stream
+// capture as an external event node (so that replays record it), else as a
+// plain record (the external flag is invalid outside a capture).
 cudaError_t stage_mark(const tm_layer* layer, int i, cudaStream_t st) {
   if (!layer->stage_ev[i]) return cudaSuccess;
-  return cudaEventRecordWithFlags(layer->stage_ev[i], st, cudaEventRecordExternal);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const cudaError_t e = cudaStreamIsCapturing(st, &cs);
+  if (e != cudaSuccess) return e;
+  return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(layer->stage_ev[i], st, cudaEventRecordExternal)
+                                             : cudaEventRecord(layer->stage_ev[i], st);
+}
+
+// Frees the captured host-call graphs. Caller holds graph_mu.
+void drop_host_graphs(tm_layer* layer) {
+  for (auto& g : layer->graphs)
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+  layer->graphs.clear();
 }
 
 constexpr size_t kAlign = 256;
@@ -509,6 +542,11 @@ size_t trellis_moe_workspace_size(const tm_layer* layer, int32_t max_tokens) {
 
 void trellis_moe_destroy(tm_layer* layer) {
   if (!layer) return;
+  {
+    std::lock_guard<std::mutex> lock(layer->graph_mu);
+    drop_host_graphs(layer);
+  }
+  if (layer->capture_stream) cudaStreamDestroy(layer->capture_stream);
   cudaFree(layer->d_off1);
   cudaFree(layer->d_off2);
   cudaFree(layer->d_bits);
@@ -558,6 +596,107 @@ tm_status trellis_moe_forward_logits(tm_layer* layer, const uint16_t* x, const f
   return run_layer(layer, x, nullptr, nullptr, logits, T, mode, out, workspace, L, st);
 }
 
+namespace {
+
+// Copy-in, layer and copy-out of one host-buffer call, enqueued on `st`.
+tm_status enqueue_host(tm_layer* layer, const uint16_t* x_host, const float* logits_host, int32_t T, int32_t mode,
+                       float* out_host, void* workspace, const Layout& L, cudaStream_t st) {
+  const tm_layer_desc& d = layer->desc;
+  uint16_t* dx = at<uint16_t>(workspace, L, Layout::HOST_X);
+  float* dl = at<float>(workspace, L, Layout::HOST_LOGITS);
+  float* dout = at<float>(workspace, L, Layout::HOST_OUT);
+  cudaError_t e;
+  if ((e = cudaMemcpyAsync(dx, x_host, (size_t)T * d.H * 2, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+    return cuda_fail(e, "copy x to device");
+  if ((e = cudaMemcpyAsync(dl, logits_host, (size_t)T * d.E * 4, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+    return cuda_fail(e, "copy logits to device");
+  if ((e = stage_mark(layer, 0, st)) != cudaSuccess) return cuda_fail(e, "stage event");
+  tm_status s = run_layer(layer, dx, nullptr, nullptr, dl, T, mode, dout, workspace, L, st);
+  if (s != TM_OK) return s;
+  if ((e = cudaMemcpyAsync(out_host, dout, (size_t)T * d.H * 4, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+    return cuda_fail(e, "copy out to host");
+  return TM_OK;
+}
+
+// The device address of page-locked host memory mapped into the device's
+// address space (with unified addressing, the host address itself); NULL for
+// pageable or unmapped memory.
+const void* mapped_ptr(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+// The layer on mapped host buffers: the kernels read x and the logits and
+// write the result across the host link themselves, no staging copies.
+tm_status enqueue_mapped(tm_layer* layer, const uint16_t* x_dev, const float* logits_dev, int32_t T, int32_t mode,
+                         float* out_dev, void* workspace, const Layout& L, cudaStream_t st) {
+  cudaError_t e;
+  if ((e = stage_mark(layer, 0, st)) != cudaSuccess) return cuda_fail(e, "stage event");
+  return run_layer(layer, x_dev, nullptr, nullptr, logits_dev, T, mode, out_dev, workspace, L, st);
+}
+
+constexpr size_t kMaxHostGraphs = 16;
+
+// Captures enqueue_mapped on the layer's private stream and instantiates it.
+// Returns NULL if any step fails; the caller then runs the call directly, which
+// reports a real argument or launch error itself.
+cudaGraphExec_t capture_host(tm_layer* layer, const uint16_t* x_dev, const float* logits_dev, int32_t T,
+                             int32_t mode, float* out_dev, void* workspace, const Layout& L) {
+  if (!layer->capture_stream &&
+      cudaStreamCreateWithFlags(&layer->capture_stream, cudaStreamNonBlocking) != cudaSuccess) {
+    layer->capture_stream = nullptr;
+    cudaGetLastError();
+    return nullptr;
+  }
+  cudaStream_t cs = layer->capture_stream;
+  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  const tm_status s = enqueue_mapped(layer, x_dev, logits_dev, T, mode, out_dev, workspace, L, cs);
+  cudaGraph_t graph = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(cs, &graph);
+  cudaGraphExec_t exec = nullptr;
+  if (s == TM_OK && e == cudaSuccess && graph && cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess)
+    exec = nullptr;
+  if (graph) cudaGraphDestroy(graph);
+  cudaGetLastError();
+  g_err[0] = 0;
+  return exec;
+}
+
+// The graph for this buffer set, capturing it on its second use; NULL on the
+// first use or after a failed capture (run directly). Caller holds graph_mu.
+cudaGraphExec_t host_graph(tm_layer* layer, const uint16_t* x_dev, const float* logits_dev, int32_t T,
+                           int32_t mode, float* out_dev, void* workspace, const Layout& L) {
+  auto& v = layer->graphs;
+  const uint64_t now = ++layer->graph_clock;
+  for (auto& g : v) {
+    if (g.x != x_dev || g.logits != logits_dev || g.out != out_dev || g.ws != workspace || g.T != T || g.mode != mode)
+      continue;
+    g.used = now;
+    if (!g.exec && !g.failed) {
+      g.exec = capture_host(layer, x_dev, logits_dev, T, mode, out_dev, workspace, L);
+      g.failed = g.exec == nullptr;
+    }
+    return g.exec;
+  }
+  if (v.size() >= kMaxHostGraphs) {
+    auto lru = std::min_element(v.begin(), v.end(),
+                                [](const tm_layer::HostGraph& a, const tm_layer::HostGraph& b) { return a.used < b.used; });
+    if (lru->exec) cudaGraphExecDestroy(lru->exec);
+    v.erase(lru);
+  }
+  v.push_back({x_dev, logits_dev, out_dev, workspace, T, mode, false, now, nullptr});
+  return nullptr;
+}
+
+}  // namespace
+
 tm_status trellis_moe_forward_host(tm_layer* layer, const uint16_t* x_host, const float* logits_host, int32_t T,
                                    int32_t mode, float* out_host, void* workspace, size_t workspace_bytes,
                                    void* stream) {
@@ -571,20 +710,23 @@ tm_status trellis_moe_forward_host(tm_layer* layer, const uint16_t* x_host, cons
   tm_status s = check_ws(layer, T, workspace, workspace_bytes, &L);
   if (s != TM_OK) return s;
   cudaStream_t st = (cudaStream_t)stream;
-  const tm_layer_desc& d = layer->desc;
-  uint16_t* dx = at<uint16_t>(workspace, L, Layout::HOST_X);
-  float* dl = at<float>(workspace, L, Layout::HOST_LOGITS);
-  float* dout = at<float>(workspace, L, Layout::HOST_OUT);
   cudaError_t e;
-  if ((e = cudaMemcpyAsync(dx, x_host, (size_t)T * d.H * 2, cudaMemcpyHostToDevice, st)) != cudaSuccess)
-    return cuda_fail(e, "copy x to device");
-  if ((e = cudaMemcpyAsync(dl, logits_host, (size_t)T * d.E * 4, cudaMemcpyHostToDevice, st)) != cudaSuccess)
-    return cuda_fail(e, "copy logits to device");
-  if ((e = stage_mark(layer, 0, st)) != cudaSuccess) return cuda_fail(e, "stage event");
-  s = run_layer(layer, dx, nullptr, nullptr, dl, T, mode, dout, workspace, L, st);
-  if (s != TM_OK) return s;
-  if ((e = cudaMemcpyAsync(out_host, dout, (size_t)T * d.H * 4, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
-    return cuda_fail(e, "copy out to host");
+  const auto* xd = static_cast<const uint16_t*>(mapped_ptr(x_host));
+  const auto* ld = static_cast<const float*>(mapped_ptr(logits_host));
+  auto* od = static_cast<float*>(const_cast<void*>(mapped_ptr(out_host)));
+  // (the opt-in atomic combine clears and accumulates into the output: it
+  // keeps the staged copies)
+  if (layer->desc.deterministic && xd && ld && od && ((uintptr_t)xd) % 8 == 0 && ((uintptr_t)od) % 16 == 0) {
+    std::lock_guard<std::mutex> lock(layer->graph_mu);
+    cudaGraphExec_t exec = host_graph(layer, xd, ld, T, mode, od, workspace, L);
+    if (exec) {
+      if ((e = cudaGraphLaunch(exec, st)) != cudaSuccess) return cuda_fail(e, "graph launch");
+    } else if ((s = enqueue_mapped(layer, xd, ld, T, mode, od, workspace, L, st)) != TM_OK) {
+      return s;
+    }
+  } else if ((s = enqueue_host(layer, x_host, logits_host, T, mode, out_host, workspace, L, st)) != TM_OK) {
+    return s;
+  }
   if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "synchronize");
   return TM_OK;
 }
@@ -693,6 +835,11 @@ tm_status trellis_moe_workspace_region(const tm_layer* layer, int32_t T, int32_t
 tm_status trellis_moe_set_stage_events(tm_layer* layer, void* const* events, int32_t n) {
   g_err[0] = 0;
   if (!layer) return fail(TM_EINVAL, "layer is NULL");
+  {
+    // Captured host-call graphs record the old events: drop them.
+    std::lock_guard<std::mutex> lock(layer->graph_mu);
+    drop_host_graphs(layer);
+  }
   if (events == nullptr || n == 0) {
     for (int i = 0; i < 7; ++i) layer->stage_ev[i] = nullptr;
     return TM_OK;
