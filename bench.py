@@ -259,7 +259,7 @@ def run_ours(args, rank, world):
     # DRAM bytes per launch of the dominant kernel from one ncu capture of this
     # program (profiles/); None for workloads without a capture
     ncu_traffic = {"decode": (28.39e6, "profiles/k_dec_warp_fc1_decode_w4a8_T8.md"),
-                   "prefill": (127.95e6, "profiles/k_tc_fc_fc1_prefill_w4a16_T2048.md")}.get(args.workload)
+                   "prefill": (127.79e6, "profiles/k_tc_fc_fc1_prefill_w4a16_T2048.md")}.get(args.workload)
     if mode == "w4a8" and T <= 64:
         achieved = statistics.mean(fc1_bytes) / (stages_us["fc1"] * 1e-6) / 1e9
         roof = {"bound": "hbm", "kernel": "k_dec_warp<W4A8,FC1,K=4> (decode rows, persistent warp items)"
@@ -302,7 +302,10 @@ def run_ours(args, rank, world):
     e2e_ms = h0.elapsed_time(h1)
     e2e = {"value": round(e2e_steps * T * world / (e2e_ms / 1e3), 2), "unit": "tokens/s",
            "h2d_bytes_per_step": T * cfg.H * 2 + T * cfg.E * 4, "d2h_bytes_per_step": T * cfg.H * 4,
-           "steps": e2e_steps, "api": "trellis_moe_forward_host"}
+           "steps": e2e_steps, "api": "trellis_moe_forward_host",
+           "transfer": "pinned host buffers mapped into the device address space: the kernels read x and the "
+                       "logits and write the fp32 result over NVLink-C2C each call (no staging copies); the call "
+                       "replays a graph cached for the buffer set and synchronises the stream"}
 
     decode_path = R <= 1024 and R < 4 * cfg.E   # the library's decode-rows path
     # decode rows: prologue, FC1, FC2 (with the combine); otherwise router, route map (1 or 3), rotate, FC1, FC2, combine
