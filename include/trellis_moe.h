@@ -203,6 +203,21 @@ tm_status trellis_moe_workspace_region(const tm_layer* layer, int32_t T, int32_t
  * caller keeps ownership. */
 tm_status trellis_moe_set_stage_events(tm_layer* layer, void* const* events, int32_t n);
 
+/* How the decode-rows path (T*topk <= 1024 and < 4E routes) expands trellis
+ * states into weights. on = 0 (the default): by the codebook hash in
+ * registers (several CTAs per SM); on = 1: by lookup in a table of the
+ * codebook value of every 16-bit state (65,536 fp16 entries; in W4A8 mode the
+ * value of its E4M3 rounding), built on the device when the layer is prepared
+ * and copied into each FC CTA's shared memory (one CTA per SM). On sm_103 the
+ * lookups' random bank conflicts make the table the slower variant; it is
+ * kept as the measured alternative. Both give the same
+ * weights bit for bit: the table is the full-codeword shared lookup table
+ * that b12x PR #129 "feat(moe): serve canonical Fruit QSRT atoms" (its commit
+ * notes) splits out of that change for separate review, here filled from the
+ * same expansion functions as the hash path. Drops the handle's captured
+ * host-call graphs. Errors: TM_EINVAL. */
+tm_status trellis_moe_set_decode_lut(tm_layer* layer, int32_t on);
+
 /* Read and clear the device error word of `workspace` (synchronises `stream`).
  * *flags: bit 0 = an expert id was out of range. Returns TM_EDEVICE if any flag
  * was set, else TM_OK. */

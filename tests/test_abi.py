@@ -63,5 +63,6 @@ def test_host_validation_without_gpu(lib):
     # forward on a NULL handle
     assert lib.trellis_moe_forward(None, P(8), P(8), P(8), 1, 0, P(8), P(256), 1 << 20, None) == -1
     assert lib.trellis_moe_set_stage_events(None, None, 0) == -1
+    assert lib.trellis_moe_set_decode_lut(None, 1) == -1
     lib.trellis_moe_destroy(None)
 

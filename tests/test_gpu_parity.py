@@ -401,6 +401,28 @@ def test_decode_path_layers(mode, kw):
     assert err < TOL[mode], err
 
 
+@pytest.mark.parametrize("mode", ["w4a8", "w4a16"])
+@pytest.mark.parametrize("kw", DECODE_SHAPES + [dict(name="decode", E=128, H=1024, I=512, topk=8, T=8)])
+def test_decode_path_table_and_hash_agree_bitwise(mode, kw):
+    """The decode rows expand weights either by the codebook hash (default) or
+    by table lookup; the table holds the hash's own values, so the two must
+    agree bit for bit (and the table path must meet the oracle too)."""
+    cfg = small_cfg(**kw)
+    L = synth.make_layer(cfg)
+    moe = _moe(L, cfg.T)
+    x_bits, logits = synth.make_tokens(cfg)
+    x, lg = upload_tokens(x_bits, logits)
+    hashed = moe.forward_logits(x, lg, mode=mode).clone()
+    moe.set_decode_lut(True)
+    lut = moe.forward_logits(x, lg, mode=mode).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(lut, hashed)
+    err, _, _ = run_and_compare(moe, L, cfg, cfg.T, mode)
+    assert err < TOL[mode], err
+    moe.set_decode_lut(False)
+    assert torch.equal(moe.forward_logits(x, lg, mode=mode), hashed)
+
+
 def _scale_bf16(bits, k):
     """bf16 bit patterns times 2^k (exact: only the exponent changes)."""
     f = (bits.astype(np.uint32) << 16).view(np.float32) * np.float32(2.0 ** k)

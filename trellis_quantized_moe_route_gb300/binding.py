@@ -29,7 +29,8 @@ EXPORTED = [
     "trellis_moe_prepare", "trellis_moe_workspace_size", "trellis_moe_forward",
     "trellis_moe_forward_logits", "trellis_moe_forward_host", "trellis_moe_route",
     "trellis_moe_route_map", "trellis_moe_rotate_quant", "trellis_moe_decode_tiles",
-    "trellis_moe_workspace_region", "trellis_moe_set_stage_events", "trellis_moe_poll_error",
+    "trellis_moe_workspace_region", "trellis_moe_set_stage_events", "trellis_moe_set_decode_lut",
+    "trellis_moe_poll_error",
     "trellis_moe_last_error", "trellis_moe_destroy", "trellis_moe_route_map_static",
 ]
 
@@ -76,6 +77,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "trellis_moe_decode_tiles": (I32, [P, I32, I32, I32, I32, I32, P, P]),
         "trellis_moe_workspace_region": (I32, [P, I32, I32, ctypes.POINTER(SZ), ctypes.POINTER(SZ)]),
         "trellis_moe_set_stage_events": (I32, [P, ctypes.POINTER(P), I32]),
+        "trellis_moe_set_decode_lut": (I32, [P, I32]),
         "trellis_moe_poll_error": (I32, [P, P, ctypes.POINTER(ctypes.c_uint32), P]),
         "trellis_moe_last_error": (ctypes.c_char_p, []),
         "trellis_moe_destroy": (None, [P]),
@@ -270,6 +272,11 @@ class TrellisMoE:
         off, nb = ctypes.c_size_t(), ctypes.c_size_t()
         _check(self.lib.trellis_moe_workspace_region(self.handle, T, which, ctypes.byref(off), ctypes.byref(nb)))
         return self.workspace[off.value:off.value + nb.value]
+
+    def set_decode_lut(self, on: bool):
+        """Decode-rows expansion by codebook table lookup (True) or by the
+        hash (False, the default); see the C header."""
+        _check(self.lib.trellis_moe_set_decode_lut(self.handle, 1 if on else 0))
 
     def set_stage_events(self, events):
         """events: None, or 7 torch.cuda.Event (or None) recorded at the stage

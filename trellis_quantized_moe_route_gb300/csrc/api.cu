@@ -25,6 +25,8 @@ struct tm_layer {
   int64_t* d_off1;     // [E] word offsets of each expert's FC1 block
   int64_t* d_off2;     // [E]
   uint8_t* d_bits;     // [E]
+  uint16_t* d_lut;     // codebook tables for the decode-rows lookup variant (fp16 | E4M3 as fp16)
+  int use_lut;         // decode rows expand by table lookup (1) or by the hash (0)
   int device;
   cudaEvent_t stage_ev[7];  // optional stage-boundary events (NULL = off)
   // Host-buffer calls on mapped page-locked buffers replay a captured graph of
@@ -414,7 +416,8 @@ tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids
   d1.out = out;
   d1.T = T;
   d1.max_blocks = dp.max_blocks;
-  if ((e = tmoe::dec_fc_warps(1, w4a8, layer->uniform_k, &d1.fc_warps)) != cudaSuccess)
+  d1.lut = layer->use_lut ? layer->d_lut + (w4a8 ? 65536 : 0) : nullptr;
+  if ((e = tmoe::dec_fc_warps(1, w4a8, layer->uniform_k, d1.lut != nullptr, &d1.fc_warps)) != cudaSuccess)
     return cuda_fail(e, "FC1 (decode rows) setup");
   if ((e = tmoe::launch_dec_fc(d1, 1, w4a8, layer->uniform_k, st)) != cudaSuccess)
     return cuda_fail(e, "FC1 (decode rows)");
@@ -439,7 +442,7 @@ tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids
   d2.act_scaled = d1.out_act_scaled;
   d2.units_m = dp.units2;
   d2.blk_off = pa.blk_off2;
-  if ((e = tmoe::dec_fc_warps(2, w4a8, layer->uniform_k, &d2.fc_warps)) != cudaSuccess)
+  if ((e = tmoe::dec_fc_warps(2, w4a8, layer->uniform_k, d2.lut != nullptr, &d2.fc_warps)) != cudaSuccess)
     return cuda_fail(e, "FC2 (decode rows) setup");
   if ((e = tmoe::launch_dec_fc(d2, 2, w4a8, layer->uniform_k, st)) != cudaSuccess)
     return cuda_fail(e, "FC2 (decode rows)");
@@ -518,15 +521,21 @@ tm_status trellis_moe_prepare(const tm_layer_desc* desc, tm_layer** out, size_t*
   if ((e = cudaGetDevice(&L->device)) != cudaSuccess) { delete L; return cuda_fail(e, "cudaGetDevice"); }
   L->d_off1 = L->d_off2 = nullptr;
   L->d_bits = nullptr;
+  L->d_lut = nullptr;
+  L->use_lut = 0;
   if ((e = cudaMalloc(&L->d_off1, d.E * 8)) != cudaSuccess ||
       (e = cudaMalloc(&L->d_off2, d.E * 8)) != cudaSuccess ||
       (e = cudaMalloc(&L->d_bits, d.E)) != cudaSuccess ||
+      (e = cudaMalloc(&L->d_lut, tmoe::decode_lut_bytes())) != cudaSuccess ||
       (e = cudaMemcpy(L->d_off1, off1.data(), d.E * 8, cudaMemcpyHostToDevice)) != cudaSuccess ||
       (e = cudaMemcpy(L->d_off2, off2.data(), d.E * 8, cudaMemcpyHostToDevice)) != cudaSuccess ||
-      (e = cudaMemcpy(L->d_bits, L->bits.data(), d.E, cudaMemcpyHostToDevice)) != cudaSuccess) {
+      (e = cudaMemcpy(L->d_bits, L->bits.data(), d.E, cudaMemcpyHostToDevice)) != cudaSuccess ||
+      (e = tmoe::build_decode_lut(L->d_lut, nullptr)) != cudaSuccess ||
+      (e = cudaStreamSynchronize(nullptr)) != cudaSuccess) {
     cudaFree(L->d_off1);
     cudaFree(L->d_off2);
     cudaFree(L->d_bits);
+    cudaFree(L->d_lut);
     delete L;
     return cuda_fail(e, "upload descriptor tables");
   }
@@ -550,6 +559,7 @@ void trellis_moe_destroy(tm_layer* layer) {
   cudaFree(layer->d_off1);
   cudaFree(layer->d_off2);
   cudaFree(layer->d_bits);
+  cudaFree(layer->d_lut);
   delete layer;
 }
 
@@ -846,6 +856,19 @@ tm_status trellis_moe_set_stage_events(tm_layer* layer, void* const* events, int
   }
   if (n != 7) return fail(TM_EINVAL, "n=%d: pass 7 events (NULL entries allowed) or none", n);
   for (int i = 0; i < 7; ++i) layer->stage_ev[i] = (cudaEvent_t)events[i];
+  return TM_OK;
+}
+
+tm_status trellis_moe_set_decode_lut(tm_layer* layer, int32_t on) {
+  g_err[0] = 0;
+  if (!layer) return fail(TM_EINVAL, "layer is NULL");
+  if (on != 0 && on != 1) return fail(TM_EINVAL, "on=%d must be 0 or 1", on);
+  {
+    // captured host-call graphs hold the other variant's kernels: drop them
+    std::lock_guard<std::mutex> lock(layer->graph_mu);
+    drop_host_graphs(layer);
+  }
+  layer->use_lut = on;
   return TM_OK;
 }
 

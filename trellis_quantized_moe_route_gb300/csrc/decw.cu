@@ -23,6 +23,14 @@
 // PR #90, review of kernel.py: _run_activation), FC2 the unrotation (H,
 // down_svh) and, for the route completing a (token, 128 columns) block, the
 // top-k combine in slot order. No warp waits on another.
+//
+// Two expansion variants: the codebook hash in registers (several four-warp
+// CTAs per SM; the default), or one shared-memory table lookup per weight
+// (the full-codeword lookup table that b12x PR #129's commit notes split out
+// for separate review; one CTA per SM whose warps share the 128 KB table,
+// copied from the layer's device copy at kernel start). The table trades the
+// hash's integer, fp16-add and E4M3-conversion instructions for one shared
+// load, whose random bank conflicts make it the slower of the two here.
 #include <algorithm>
 
 #include "launch.h"
@@ -73,7 +81,17 @@ __device__ __forceinline__ DwMetaW dw_meta_final(const DwRaw& r, int rb, int lan
 }
 
 __host__ __device__ inline int dw_slot_bytes(int kmax) { return kDwTiles * 32 * kmax; }
-__host__ __device__ inline int dw_smem_bytes(int kmax) { return kDwWarps * kDwRing * dw_slot_bytes(kmax); }
+
+// Codebook lookup table: the fp16 weight of each of the 65,536 trellis states
+// (W4A8: of its E4M3 rounding), 128 KB. The lookup variant runs one CTA per
+// SM whose warps share the table in shared memory; the procedural variant
+// runs several four-warp CTAs per SM.
+constexpr int kDwLutEntries = 65536;
+constexpr int kDwLutBytes = kDwLutEntries * 2;
+__host__ __device__ constexpr int dw_cta_warps(int kb, bool lut) { return lut ? (kb > 0 ? 24 : 16) : kDwWarps; }
+__host__ __device__ inline int dw_smem_bytes(int kmax, bool lut, int warps) {
+  return (lut ? kDwLutBytes : 0) + warps * kDwRing * dw_slot_bytes(kmax);
+}
 
 // Window of a run for any K, read from shared memory: the 64 stream bits
 // starting at the word holding bit q0 = (j0+1)K-16 (mod 256K), and the bit
@@ -147,14 +165,61 @@ __device__ __forceinline__ const unsigned char* dw_src(const DecArgs& d, const D
          ((size_t)it.strip * tiles_k + (size_t)it.sg * kDwTiles) * 32 * it.k;
 }
 
+// One 8-weight run of a tile (tile row r, half h; K = 4: the 32-bit words at
+// byte offsets oc and op of the row's run and of the word before it) as fp16
+// pairs, either by the codebook hash (W4A8: rounded to E4M3) ...
+template <bool W4A8, int K>
+__device__ __forceinline__ void dw_run_hash(const unsigned char* tile, int r, int h, int oc, int op, uint32_t k16,
+                                            uint32_t nk16, uint32_t (&w)[4]) {
+  uint32_t y[8];
+  if (K == 4) {
+    run_mcg_k4(*reinterpret_cast<const uint32_t*>(tile + op), *reinterpret_cast<const uint32_t*>(tile + oc), k16, nk16, y);
+  } else {
+    uint32_t hi, lo, s8[8];
+    int off;
+    dw_window<K>(reinterpret_cast<const uint16_t*>(tile), 16 * r + 8 * h, hi, lo, off);
+    run_states_generic<K>(hi, lo, off, s8);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = mcg_raw(s8[i]);
+  }
+  if (W4A8)
+    raw_to_e4m3_f16(y, w);
+  else
+    raw_to_f16(y, w);
+}
+
+// ... or by one lookup per weight in the shared-memory codebook table.
+template <int K>
+__device__ __forceinline__ void dw_run_lut(const unsigned char* tile, const uint16_t* lut, int r, int h, int oc, int op,
+                                           uint32_t (&w)[4]) {
+  uint32_t s[8];
+  if (K == 4) {
+    run_states_k4(*reinterpret_cast<const uint32_t*>(tile + op), *reinterpret_cast<const uint32_t*>(tile + oc), s);
+  } else {
+    uint32_t hi, lo;
+    int off;
+    dw_window<K>(reinterpret_cast<const uint16_t*>(tile), 16 * r + 8 * h, hi, lo, off);
+    run_states_generic<K>(hi, lo, off, s);
+  }
+#pragma unroll
+  for (int p = 0; p < 4; ++p) w[p] = __byte_perm((uint32_t)lut[s[2 * p]], (uint32_t)lut[s[2 * p + 1]], 0x5410);
+}
+
+// With the table, how many of a lane's two runs per tile take it (the other
+// takes the hash, so that the shared-memory pipe and the integer / fp16 pipes
+// could share the work). Lookups of random states meet bank conflicts: on
+// sm_103 both the full table and the one-run split are slower than the hash
+// alone, which is why the hash is the default.
+constexpr int kDwLutRuns = 2;
+
 // Expansion and MMAs of one item: acc (this lane's D fragment, rows g, g+8 of
 // the strip, slots 2q, 2q+1) over the item's k-steps.
 // PRE (W4A8): the activations are read as code * 2^e, so the MMAs accumulate
 // straight into acc with no per-block scaling (every block of the item has
 // its exponent in [-15, 7]; see dw_pre_issue).
-template <bool W4A8, bool PRE, int K>
+template <bool W4A8, bool PRE, int K, bool LUT>
 __device__ __forceinline__ void dw_compute(const DecArgs& d, const DwItem& it, int row,
-                                           const unsigned char* wt, int kdim, float (&acc)[4]) {
+                                           const unsigned char* wt, const uint16_t* lut, int kdim, float (&acc)[4]) {
   const FcArgs& a = d.f;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3, h = q & 1, tsel = q >> 1;
@@ -179,34 +244,15 @@ __device__ __forceinline__ void dw_compute(const DecArgs& d, const DwItem& it, i
     if (ks < steps) {
       const uint4 bv = (arow >= 0) ? __ldg(reinterpret_cast<const uint4*>(ap + 32 * ks)) : make_uint4(0u, 0u, 0u, 0u);
       const unsigned char* tile = wt + (2 * ks + tsel) * 32 * K;
-      uint32_t y0[8], y1[8];
-      if (K == 4) {
-        const uint32_t c0w = *reinterpret_cast<const uint32_t*>(tile + oc0);
-        const uint32_t p0w = *reinterpret_cast<const uint32_t*>(tile + op0);
-        const uint32_t c1w = *reinterpret_cast<const uint32_t*>(tile + oc1);
-        const uint32_t p1w = *reinterpret_cast<const uint32_t*>(tile + op1);
-        run_mcg_k4(p0w, c0w, k16, nk16, y0);
-        run_mcg_k4(p1w, c1w, k16, nk16, y1);
-      } else {
-        uint32_t hi, lo, s8[8];
-        int off;
-        dw_window<K>(reinterpret_cast<const uint16_t*>(tile), 16 * g + 8 * h, hi, lo, off);
-        run_states_generic<K>(hi, lo, off, s8);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) y0[i] = mcg_raw(s8[i]);
-        dw_window<K>(reinterpret_cast<const uint16_t*>(tile), 16 * (g + 8) + 8 * h, hi, lo, off);
-        run_states_generic<K>(hi, lo, off, s8);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) y1[i] = mcg_raw(s8[i]);
-      }
       uint32_t wa[4], wb[4];
-      if (W4A8) {
-        raw_to_e4m3_f16(y0, wa);
-        raw_to_e4m3_f16(y1, wb);
-      } else {
-        raw_to_f16(y0, wa);
-        raw_to_f16(y1, wb);
-      }
+      if (LUT)
+        dw_run_lut<K>(tile, lut, g, h, oc0, op0, wa);
+      else
+        dw_run_hash<W4A8, K>(tile, g, h, oc0, op0, k16, nk16, wa);
+      if (LUT && kDwLutRuns == 2)
+        dw_run_lut<K>(tile, lut, g + 8, h, oc1, op1, wb);
+      else
+        dw_run_hash<W4A8, K>(tile, g + 8, h, oc1, op1, k16, nk16, wb);
       const uint32_t a0[4] = {wa[0], wb[0], wa[1], wb[1]};
       const uint32_t a1[4] = {wa[2], wb[2], wa[3], wb[3]};
       if (W4A8 && !PRE) {
@@ -227,29 +273,30 @@ __device__ __forceinline__ void dw_compute(const DecArgs& d, const DwItem& it, i
   }
 }
 
-template <bool W4A8, bool PRE, int KB>
-__device__ __forceinline__ void dw_compute_k(const DecArgs& d, const DwItem& it, int row,
-                                             const unsigned char* wt, int kdim, float (&acc)[4]) {
+template <bool W4A8, bool PRE, int KB, bool LUT>
+__device__ __forceinline__ void dw_compute_k(const DecArgs& d, const DwItem& it, int row, const unsigned char* wt,
+                                             const uint16_t* lut, int kdim, float (&acc)[4]) {
   if (KB > 0) {
-    dw_compute<W4A8, PRE, (KB > 0 ? KB : 4)>(d, it, row, wt, kdim, acc);
+    dw_compute<W4A8, PRE, (KB > 0 ? KB : 4), LUT>(d, it, row, wt, lut, kdim, acc);
     return;
   }
   switch (it.k) {
-    case 2: dw_compute<W4A8, PRE, 2>(d, it, row, wt, kdim, acc); break;
-    case 3: dw_compute<W4A8, PRE, 3>(d, it, row, wt, kdim, acc); break;
-    case 4: dw_compute<W4A8, PRE, 4>(d, it, row, wt, kdim, acc); break;
-    case 5: dw_compute<W4A8, PRE, 5>(d, it, row, wt, kdim, acc); break;
-    default: dw_compute<W4A8, PRE, 6>(d, it, row, wt, kdim, acc); break;
+    case 2: dw_compute<W4A8, PRE, 2, LUT>(d, it, row, wt, lut, kdim, acc); break;
+    case 3: dw_compute<W4A8, PRE, 3, LUT>(d, it, row, wt, lut, kdim, acc); break;
+    case 4: dw_compute<W4A8, PRE, 4, LUT>(d, it, row, wt, lut, kdim, acc); break;
+    case 5: dw_compute<W4A8, PRE, 5, LUT>(d, it, row, wt, lut, kdim, acc); break;
+    default: dw_compute<W4A8, PRE, 6, LUT>(d, it, row, wt, lut, kdim, acc); break;
   }
 }
 
-template <bool W4A8, int KB>
+template <bool W4A8, int KB, bool LUT>
 __device__ __forceinline__ void dw_compute_any(const DecArgs& d, const DwItem& it, bool pre, int row,
-                                               const unsigned char* wt, int kdim, float (&acc)[4]) {
+                                               const unsigned char* wt, const uint16_t* lut, int kdim,
+                                               float (&acc)[4]) {
   if (W4A8 && pre)
-    dw_compute_k<W4A8, true, KB>(d, it, row, wt, kdim, acc);
+    dw_compute_k<W4A8, true, KB, LUT>(d, it, row, wt, lut, kdim, acc);
   else
-    dw_compute_k<W4A8, false, KB>(d, it, row, wt, kdim, acc);
+    dw_compute_k<W4A8, false, KB, LUT>(d, it, row, wt, lut, kdim, acc);
 }
 
 // W4A8: the E8M0 exponents an item reads (its valid slots x its 32-column
@@ -520,23 +567,33 @@ __device__ __forceinline__ void dw_epilogue_fc2(const DecArgs& d, int t, int mb,
 // constant weights before it waits for its predecessor, so its first payload
 // copy overlaps the FC1 epilogue. Partial sums: per item, [slot][16 rows] fp32.
 // ---------------------------------------------------------------------------
-template <bool W4A8, int PROJ, int KB>
-__global__ void __launch_bounds__(kDwThreads, KB > 0 ? 6 : 4) k_dec_warp(const DecArgs d) {
+template <bool W4A8, int PROJ, int KB, bool LUT>
+__global__ void __launch_bounds__(dw_cta_warps(KB, LUT) * 32, LUT ? 1 : (KB > 0 ? 6 : 4)) k_dec_warp(const DecArgs d) {
   extern __shared__ __align__(128) unsigned char dw_smem[];
+  constexpr int NW = dw_cta_warps(KB, LUT);
   const FcArgs& a = d.f;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int KMAX = KB > 0 ? KB : 6;
   const int slot_bytes = dw_slot_bytes(KMAX);
-  unsigned char* ring = dw_smem + warp * kDwRing * slot_bytes;
+  unsigned char* ring = dw_smem + (LUT ? kDwLutBytes : 0) + warp * kDwRing * slot_bytes;
+  const uint16_t* lut = reinterpret_cast<const uint16_t*>(dw_smem);
   const int kdim = PROJ == 1 ? a.H : a.I;
   const uint32_t nstrips = (uint32_t)((PROJ == 1 ? 2 * a.I : a.H) >> 4);
   const uint32_t per_block = (uint32_t)d.nseg * nstrips;
-  const uint32_t nwarps = gridDim.x * kDwWarps;
+  const uint32_t nwarps = gridDim.x * NW;
 
+  if (LUT) {
+    // the codebook table (fixed since the layer was prepared) into shared
+    // memory, overlapping the predecessor's tail
+    const uint4* src = reinterpret_cast<const uint4*>(d.lut);
+    uint4* dst = reinterpret_cast<uint4*>(dw_smem);
+    for (int i = threadIdx.x; i < kDwLutBytes / 16; i += NW * 32) dst[i] = __ldg(src + i);
+    __syncthreads();
+  }
   if (PROJ == 1) dw_griddep_wait();  // the route map and x~ come from the prologue
   const int nb = min(*a.nblocks, d.max_blocks);
   const uint32_t h1 = (uint32_t)nb * per_block;  // items
-  uint32_t h = blockIdx.x * kDwWarps + warp;     // next item of this warp
+  uint32_t h = blockIdx.x * NW + warp;           // next item of this warp
   const bool any = h < h1;
   uint32_t pc = 0, pn = 0, pn2 = 0;
   DwItem it{}, nit{};
@@ -585,7 +642,7 @@ __global__ void __launch_bounds__(kDwThreads, KB > 0 ? 6 : 4) k_dec_warp(const D
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     const bool pre = W4A8 && dw_pre_final(pre_cur);
-    dw_compute_any<W4A8, KB>(d, it, pre, m.row, ring + (n & 1) * slot_bytes, kdim, acc);
+    dw_compute_any<W4A8, KB, LUT>(d, it, pre, m.row, ring + (n & 1) * slot_bytes, lut, kdim, acc);
 
     // partial sums of the valid slots, [slot][16 rows]
     const int g = lane >> 2, c = 2 * (lane & 3);
@@ -654,40 +711,44 @@ __global__ void __launch_bounds__(256) k_dec_epi(const DecArgs d) {
   }
 }
 
-template <bool W4A8, int PROJ, int KB>
+template <bool W4A8, int PROJ, int KB, bool LUT>
 static cudaError_t dw_warps_t(int* warps) {
   // attributes and the resident-CTA count are fixed on the first call (before any capture)
+  constexpr int NW = dw_cta_warps(KB, LUT);
   static int resident = 0;
   if (resident == 0) {
-    auto kern = k_dec_warp<W4A8, PROJ, KB>;
-    const int smem = dw_smem_bytes(KB > 0 ? KB : 6);
+    auto kern = k_dec_warp<W4A8, PROJ, KB, LUT>;
+    const int smem = dw_smem_bytes(KB > 0 ? KB : 6, LUT, NW);
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     int per_sm = 0;
-    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDwThreads, smem)) != cudaSuccess) return err;
+    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NW * 32, smem)) != cudaSuccess) return err;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
     int dev = 0, sms = 0;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
     if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
-    resident = std::max(1, per_sm) * sms;
+    resident = per_sm * sms;
   }
-  *warps = resident * kDwWarps;
+  *warps = resident * NW;
   return cudaSuccess;
 }
 
-template <bool W4A8, int PROJ, int KB>
+template <bool W4A8, int PROJ, int KB, bool LUT>
 static cudaError_t launch_dw_t(const DecArgs& d, cudaStream_t st) {
-  if (d.fc_warps <= 0 || d.fc_warps % kDwWarps) return cudaErrorInvalidValue;
+  constexpr int NW = dw_cta_warps(KB, LUT);
+  if (d.fc_warps <= 0 || d.fc_warps % NW) return cudaErrorInvalidValue;
+  if (LUT && (!d.lut || ((uintptr_t)d.lut) % 16)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(d.fc_warps / kDwWarps);
-  cfg.blockDim = dim3(kDwThreads);
-  cfg.dynamicSmemBytes = dw_smem_bytes(KB > 0 ? KB : 6);
+  cfg.gridDim = dim3(d.fc_warps / NW);
+  cfg.blockDim = dim3(NW * 32);
+  cfg.dynamicSmemBytes = dw_smem_bytes(KB > 0 ? KB : 6, LUT, NW);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_dec_warp<W4A8, PROJ, KB>, d);
+  return cudaLaunchKernelEx(&cfg, k_dec_warp<W4A8, PROJ, KB, LUT>, d);
 }
 
 template <bool W4A8, int PROJ>
@@ -705,14 +766,19 @@ static cudaError_t launch_epi_t(const DecArgs& d, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, k_dec_epi<W4A8, PROJ>, d);
 }
 
-cudaError_t dec_fc_warps(int proj, bool w4a8, int uniform_k, int* warps) {
+template <bool LUT>
+static cudaError_t dec_fc_warps_t(int proj, bool w4a8, int uniform_k, int* warps) {
   const bool k4 = uniform_k == 4;
   if (proj == 1) {
-    if (w4a8) return k4 ? dw_warps_t<true, 1, 4>(warps) : dw_warps_t<true, 1, 0>(warps);
-    return k4 ? dw_warps_t<false, 1, 4>(warps) : dw_warps_t<false, 1, 0>(warps);
+    if (w4a8) return k4 ? dw_warps_t<true, 1, 4, LUT>(warps) : dw_warps_t<true, 1, 0, LUT>(warps);
+    return k4 ? dw_warps_t<false, 1, 4, LUT>(warps) : dw_warps_t<false, 1, 0, LUT>(warps);
   }
-  if (w4a8) return k4 ? dw_warps_t<true, 2, 4>(warps) : dw_warps_t<true, 2, 0>(warps);
-  return k4 ? dw_warps_t<false, 2, 4>(warps) : dw_warps_t<false, 2, 0>(warps);
+  if (w4a8) return k4 ? dw_warps_t<true, 2, 4, LUT>(warps) : dw_warps_t<true, 2, 0, LUT>(warps);
+  return k4 ? dw_warps_t<false, 2, 4, LUT>(warps) : dw_warps_t<false, 2, 0, LUT>(warps);
+}
+
+cudaError_t dec_fc_warps(int proj, bool w4a8, int uniform_k, bool lut, int* warps) {
+  return lut ? dec_fc_warps_t<true>(proj, w4a8, uniform_k, warps) : dec_fc_warps_t<false>(proj, w4a8, uniform_k, warps);
 }
 
 cudaError_t launch_dec_epilogue(const DecArgs& d, int proj, bool w4a8, cudaStream_t st) {
@@ -720,14 +786,41 @@ cudaError_t launch_dec_epilogue(const DecArgs& d, int proj, bool w4a8, cudaStrea
   return w4a8 ? launch_epi_t<true, 2>(d, st) : launch_epi_t<false, 2>(d, st);
 }
 
-cudaError_t launch_dec_fc(const DecArgs& d, int proj, bool w4a8, int uniform_k, cudaStream_t st) {
+template <bool LUT>
+static cudaError_t launch_dec_fc_t(const DecArgs& d, int proj, bool w4a8, int uniform_k, cudaStream_t st) {
   const bool k4 = uniform_k == 4;
   if (proj == 1) {
-    if (w4a8) return k4 ? launch_dw_t<true, 1, 4>(d, st) : launch_dw_t<true, 1, 0>(d, st);
-    return k4 ? launch_dw_t<false, 1, 4>(d, st) : launch_dw_t<false, 1, 0>(d, st);
+    if (w4a8) return k4 ? launch_dw_t<true, 1, 4, LUT>(d, st) : launch_dw_t<true, 1, 0, LUT>(d, st);
+    return k4 ? launch_dw_t<false, 1, 4, LUT>(d, st) : launch_dw_t<false, 1, 0, LUT>(d, st);
   }
-  if (w4a8) return k4 ? launch_dw_t<true, 2, 4>(d, st) : launch_dw_t<true, 2, 0>(d, st);
-  return k4 ? launch_dw_t<false, 2, 4>(d, st) : launch_dw_t<false, 2, 0>(d, st);
+  if (w4a8) return k4 ? launch_dw_t<true, 2, 4, LUT>(d, st) : launch_dw_t<true, 2, 0, LUT>(d, st);
+  return k4 ? launch_dw_t<false, 2, 4, LUT>(d, st) : launch_dw_t<false, 2, 0, LUT>(d, st);
+}
+
+cudaError_t launch_dec_fc(const DecArgs& d, int proj, bool w4a8, int uniform_k, cudaStream_t st) {
+  return d.lut ? launch_dec_fc_t<true>(d, proj, w4a8, uniform_k, st) : launch_dec_fc_t<false>(d, proj, w4a8, uniform_k, st);
+}
+
+// The codebook tables of a layer: [0, 65536) the fp16 weight of each state,
+// [65536, 131072) the fp16 value of its E4M3 rounding, computed by the same
+// expansion functions as the procedural path (8 states per thread).
+__global__ void k_build_decode_lut(uint16_t* lut) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= kDwLutEntries / 8) return;
+  uint32_t y[8], w[4], we[4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) y[i] = mcg_raw((uint32_t)(8 * t + i));
+  raw_to_f16(y, w);
+  raw_to_e4m3_f16(y, we);
+  reinterpret_cast<uint4*>(lut)[t] = make_uint4(w[0], w[1], w[2], w[3]);
+  reinterpret_cast<uint4*>(lut + kDwLutEntries)[t] = make_uint4(we[0], we[1], we[2], we[3]);
+}
+
+size_t decode_lut_bytes() { return 2 * (size_t)kDwLutBytes; }
+
+cudaError_t build_decode_lut(uint16_t* lut, cudaStream_t st) {
+  k_build_decode_lut<<<kDwLutEntries / 8 / 256, 256, 0, st>>>(lut);
+  return cudaGetLastError();
 }
 
 }  // namespace tmoe

@@ -99,12 +99,16 @@ struct DecArgs {
   const float* route_w;     // [T*topk]
   float* out;               // FC2: final output [T, H]
   int T;
+  const uint16_t* lut;      // codebook table of the mode (65,536 fp16), or NULL: expand by the hash
 };
 
 cudaError_t launch_dec_prologue(const DecPrologueArgs& a, cudaStream_t st);
 // Warps of the decode-rows FC kernel's grid (all resident: CTAs per SM x SMs);
 // fixed on the first call, which also sets the kernel's attributes.
-cudaError_t dec_fc_warps(int proj, bool w4a8, int uniform_k, int* warps);
+cudaError_t dec_fc_warps(int proj, bool w4a8, int uniform_k, bool lut, int* warps);
+// Codebook tables for the lookup variant: decode_lut_bytes() bytes, built on `st`.
+size_t decode_lut_bytes();
+cudaError_t build_decode_lut(uint16_t* lut, cudaStream_t st);
 cudaError_t launch_dec_fc(const DecArgs& d, int proj, bool w4a8, int uniform_k, cudaStream_t st);
 cudaError_t launch_dec_epilogue(const DecArgs& d, int proj, bool w4a8, cudaStream_t st);
 
