@@ -17,12 +17,13 @@
 // (mma.sync of E4M3 operands is not a native tensor instruction on sm_103).
 // The 16x8 partial sums of an item go to the workspace.
 //
-// The epilogue kernels that follow run one warp per (epilogue unit, slot):
-// the unit's partials summed in segment order (deterministic), then FC1 the
-// activation H -> svh -> SiLU(gate)*up -> suh_down -> H into z~ (sparkinfer
-// PR #90, review of kernel.py: _run_activation), FC2 the unrotation (H,
-// down_svh) and, for the route completing a (token, 128 columns) block, the
-// top-k combine in slot order. No warp waits on another.
+// The epilogue kernels that follow sum each item's partials in segment order
+// (deterministic). FC1, one warp per (epilogue unit, slot): the activation
+// H -> svh -> SiLU(gate)*up -> suh_down -> H into z~ (sparkinfer PR #90,
+// review of kernel.py: _run_activation). FC2, one CTA per (token, 128
+// columns), a warp per route: the unrotation (H, down_svh) times the route
+// weight into shared memory, then the top-k combine in route order. No CTA
+// waits on another.
 //
 // Two expansion variants: the codebook hash in registers (several four-warp
 // CTAs per SM; the default), or one shared-memory table lookup per weight
@@ -477,84 +478,55 @@ __device__ __forceinline__ void dw_epilogue_fc1(const DecArgs& d, int rb, int mb
   }
 }
 
-// FC2, token t, output channels mb*128 .. +127: for each of the token's routes
-// j = 0..k-1 in order, the route's summed partials, output scale, H, hs *
-// down_svh, and w_j times that into the FP32 sum (the deterministic top-k
-// combine); routes are taken four at a time with all their loads in flight.
-__device__ __forceinline__ void dw_epilogue_fc2(const DecArgs& d, int t, int mb, int nstrips) {
+// FC2 epilogue and top-k combine, one CTA of kDwEpiWarps warps per (token t,
+// 128 output columns mb): warp u takes the token's routes j = u, u + 8, ...;
+// for each, the route's summed partials, output scale, H, hs * down_svh and
+// the route weight w_j, into a shared row per route; then one warp adds the
+// rows in route order j = 0..k-1 (the deterministic FP32 combine). A route
+// whose expert id was dropped contributes zeros.
+constexpr int kDwEpiWarps = 8;
+__device__ __forceinline__ void dw_epilogue_fc2(const DecArgs& d, int t, int mb, int nstrips, float4* rows) {
   const FcArgs& a = d.f;
-  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h0 = mb * 128 + lane * 4;
   const int strip = h0 >> 4, r16 = h0 & 15;
   const float hs = hadamard_scale(a.rot_b);
   const int k = a.topk;
-  // the token's slots, weights and experts, one route per lane
-  int my_slot = -1, my_e = 0;
-  float my_w = 0.0f;
-  if (lane < k) {
-    my_slot = d.slot_of_route[t * k + lane];
-    my_w = d.route_w[t * k + lane];
-    my_e = d.ids[t * k + lane];
-  }
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j0 = 0; j0 < k; j0 += 4) {
-    int sl[4], ex[4];
-    float wj[4], v[4][4], sc[4][4], sv[4][4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int j = j0 + u;
-      sl[u] = __shfl_sync(0xFFFFFFFFu, my_slot, j & 31);
-      wj[u] = __shfl_sync(0xFFFFFFFFu, my_w, j & 31);
-      ex[u] = __shfl_sync(0xFFFFFFFFu, my_e, j & 31);
-      if (j >= k) sl[u] = -1;
-      const bool ok = sl[u] >= 0;  // (a dropped, out-of-range expert id has no slot)
-      dw_ld_h<4>(a.scale + (size_t)(ok ? ex[u] : 0) * a.H + h0, sc[u]);
-      dw_ld_h<4>(a.rot_tab + (size_t)(ok ? ex[u] : 0) * a.H + h0, sv[u]);
-    }
-    if (j0 == 0) dw_griddep_wait();  // the partial sums come from the predecessor
-    // partial sums of the four routes, two segments at a time
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-      for (int p = 0; p < 4; ++p) v[u][p] = 0.0f;
-    for (int s0 = 0; s0 < d.nseg; s0 += 2) {
-      float4 x[4][2];
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const bool ok = sl[u] >= 0 && s0 + q < d.nseg;
-          const int rb = ok ? sl[u] / kDecBlock : 0, n = ok ? sl[u] % kDecBlock : 0;
-          const float* pp = d.partial + ((size_t)(rb * d.nseg + (ok ? s0 + q : 0)) * nstrips + strip) * 128 + n * 16 + r16;
-          x[u][q] = ok ? __ldcg(reinterpret_cast<const float4*>(pp)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-          if (s0 + q < d.nseg) {
-            v[u][0] += x[u][q].x;
-            v[u][1] += x[u][q].y;
-            v[u][2] += x[u][q].z;
-            v[u][3] += x[u][q].w;
-          }
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (sl[u] < 0) continue;  // warp-uniform
+  for (int j = warp; j < k; j += kDwEpiWarps) {
+    // (route map, weights and tables come from the prologue or the layer,
+    // complete before this grid could start)
+    const int slot = d.slot_of_route[t * k + j];
+    const bool ok = slot >= 0;  // warp-uniform
+    const int e = ok ? d.ids[t * k + j] : 0;
+    float sc[4], sv[4], v[4];
+    dw_ld_h<4>(a.scale + (size_t)e * a.H + h0, sc);
+    dw_ld_h<4>(a.rot_tab + (size_t)e * a.H + h0, sv);
+    if (j == warp) dw_griddep_wait();  // the partial sums come from the predecessor
+    float4 y4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (ok) {
+      const float wj = d.route_w[t * k + j];
+      dw_sum_parts<4>(d, slot / kDecBlock, strip, nstrips, slot % kDecBlock, r16, v);
       float y[4];
 #pragma unroll
-      for (int p = 0; p < 4; ++p) y[p] = v[u][p] * sc[u][p];
+      for (int p = 0; p < 4; ++p) y[p] = v[p] * sc[p];
       warp_fwht<4>(y, a.rot_b);
-#pragma unroll
-      for (int p = 0; p < 4; ++p) y[p] = y[p] * hs * sv[u][p];
-      acc.x = fmaf(wj[u], y[0], acc.x);
-      acc.y = fmaf(wj[u], y[1], acc.y);
-      acc.z = fmaf(wj[u], y[2], acc.z);
-      acc.w = fmaf(wj[u], y[3], acc.w);
+      y4 = make_float4(wj * (y[0] * hs * sv[0]), wj * (y[1] * hs * sv[1]), wj * (y[2] * hs * sv[2]),
+                       wj * (y[3] * hs * sv[3]));
     }
+    rows[j * 32 + lane] = y4;
   }
-  *reinterpret_cast<float4*>(d.out + (size_t)t * a.H + h0) = acc;
+  __syncthreads();
+  if (warp == 0) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+      const float4 r = rows[j * 32 + lane];
+      acc.x += r.x;
+      acc.y += r.y;
+      acc.z += r.z;
+      acc.w += r.w;
+    }
+    *reinterpret_cast<float4*>(d.out + (size_t)t * a.H + h0) = acc;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -680,7 +652,7 @@ __global__ void __launch_bounds__(dw_cta_warps(KB, LUT) * 32, LUT ? 1 : (KB > 0 
 }
 
 // The epilogue kernels: FC1 one warp per (route block, unit of BI
-// intermediate channels, slot), FC2 one warp per (token, 128 output channels).
+// intermediate channels, slot), FC2 one CTA per (token, 128 output channels).
 template <bool W4A8, int PROJ>
 __global__ void __launch_bounds__(256) k_dec_epi(const DecArgs d) {
   // (the route map and block table come from the prologue, complete before
@@ -704,10 +676,11 @@ __global__ void __launch_bounds__(256) k_dec_epi(const DecArgs d) {
     else
       dw_epilogue_fc1<2, W4A8>(d, rb, mb, e, n, nstrips);
   } else {
-    const int mb = gw % d.units_m;
-    const int t = gw / d.units_m;
-    if (t >= d.T) return;
-    dw_epilogue_fc2(d, t, mb, a.H >> 4);
+    __shared__ float4 rows[32 * 32];  // one 128-column row per route (top-k <= 32)
+    const int mb = blockIdx.x % d.units_m;
+    const int t = blockIdx.x / d.units_m;
+    if (t >= d.T) return;  // (whole CTA)
+    dw_epilogue_fc2(d, t, mb, a.H >> 4, rows);
   }
 }
 
@@ -753,7 +726,9 @@ static cudaError_t launch_dw_t(const DecArgs& d, cudaStream_t st) {
 
 template <bool W4A8, int PROJ>
 static cudaError_t launch_epi_t(const DecArgs& d, cudaStream_t st) {
-  const long warps = (PROJ == 1) ? (long)d.max_blocks * d.units_m * kDecBlock : (long)d.T * d.units_m;
+  // FC1: one warp per (block, unit, slot); FC2: one CTA per (token, unit)
+  const long warps = (PROJ == 1) ? (long)d.max_blocks * d.units_m * kDecBlock : (long)d.T * d.units_m * 8;
+  static_assert(kDwEpiWarps == 8, "the FC2 epilogue CTA is the launch's 256 threads");
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((warps + 7) / 8));
   cfg.blockDim = dim3(256);
