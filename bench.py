@@ -258,7 +258,7 @@ def run_ours(args, rank, world):
     pk = peaks()
     # DRAM bytes per launch of the dominant kernel from one ncu capture of this
     # program (profiles/); None for workloads without a capture
-    ncu_traffic = {"decode": (28.39e6, "profiles/k_dec_warp_fc1_decode_w4a8_T8.md"),
+    ncu_traffic = {"decode": (28.387e6, "profiles/k_dec_warp_fc1_decode_w4a8_T8.md"),
                    "prefill": (127.79e6, "profiles/k_tc_fc_fc1_prefill_w4a16_T2048.md")}.get(args.workload)
     if mode == "w4a8" and T <= 64:
         achieved = statistics.mean(fc1_bytes) / (stages_us["fc1"] * 1e-6) / 1e9
