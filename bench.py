@@ -1,7 +1,7 @@
 """Throughput of the fused trellis-MoE layer on synthetic inputs.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                [--workload decode|prefill|odd|large-decode|large-prefill] [--tokens T]
+                [--workload decode|prefill|odd|large-decode|large-prefill|linear] [--tokens T]
 
 One step is one pass of the whole hot path over one token batch: router on the
 logits, route map, fused rotate+quantize, FC1 with its activation epilogue,
@@ -356,6 +356,18 @@ def cpu_baseline(cfg, T, mode, budget_s=12.0):
 
 
 def run_reference(args, rank, world):
+    if args.workload == "linear":
+        c = LINEAR
+        T = args.tokens or c["T"]
+        lin = synth.make_linear(c["N"], c["K"], c["bits"], c["rot_in"], c["rot_out"], seed=40)
+        cb = linear_cpu_baseline(lin, T, budget_s=min(60.0, 5.0 * max(args.steps, 1)))
+        return {
+            "impl": "reference", "metric": LINEAR_METRIC, "value": cb["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * 64 / cb["value"], 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "linear: N=%d K=%d W4A16 T=%d" % (c["N"], c["K"], T)}, "cpu_baseline": cb,
+            "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
     cfg_name, T_default, mode = WORKLOADS[args.workload]
     cfg = synth.CONFIGS[cfg_name]
     T = args.tokens or T_default
@@ -383,13 +395,115 @@ def run_reference(args, rank, world):
     }
 
 
+# ------------------------------------------------------- dense linear ---
+LINEAR = dict(N=4096, K=4096, bits=4, rot_in=128, rot_out=128, T=2048)
+LINEAR_METRIC = "dense trellis linear tokens/s (N=K=4096, K=4 trellis, W4A16, T=2048); % of tensor roofline"
+
+
+def run_linear(args, rank, world):
+    """The dense trellis linear layer (no routing): rotate + tensor-core
+    projection per step, replayed from one graph per weight copy."""
+    import torch
+    from trellis_quantized_moe_route_gb300 import binding, build
+
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    build.build()
+    binding.load_library()
+    c = LINEAR
+    T = args.tokens or c["T"]
+    N, K = c["N"], c["K"]
+    # weights + x + out per copy ~ N*K/2 + 2TK + 4TN bytes; copies until two
+    # uses of one copy are more than 2x L2 apart
+    per_copy = N * K * c["bits"] // 8 + 2 * T * K + 4 * T * N
+    copies = int(min(16, max(2, np.ceil(2 * L2_BYTES / per_copy) + 1)))
+    lins = [synth.make_linear(N, K, c["bits"], c["rot_in"], c["rot_out"], seed=40 + i) for i in range(copies)]
+    mods = [binding.TrellisLinear(l, max_tokens=T) for l in lins]
+    xs = [torch.from_numpy(np.ascontiguousarray(synth.make_linear_tokens(l, T, seed=1000 + 17 * rank + i).view(np.int16))).cuda()
+          for i, l in enumerate(lins)]
+    outs = [torch.empty((T, N), dtype=torch.float32, device="cuda") for _ in range(copies)]
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 1)):
+            mods[i % copies].forward(xs[i % copies], out=outs[i % copies])
+    torch.cuda.synchronize()
+    graphs = []
+    for i in range(copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            mods[i].forward(xs[i], out=outs[i])
+        graphs.append(g)
+    for i in range(max(args.warmup, 3)):
+        graphs[i % copies].replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            graphs[i % copies].replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = job_time_ms(t0.elapsed_time(t1), world)
+    step_us = total_ms * 1e3 / args.steps
+    for i in range(copies):
+        assert mods[i].poll_error() == 0
+    pk = peaks()
+    flops = 2 * T * N * K
+    achieved = flops / (step_us * 1e-6) / 1e12
+    res = {
+        "metric": LINEAR_METRIC, "value": round(job_value(args.steps, T, world, total_ms), 2), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": "linear: N=%d K=%d K_trellis=%d W4A16 rot %d/%d T=%d" % (N, K, c["bits"], c["rot_in"],
+                                                                                      c["rot_out"], T),
+                   "tokens_per_step": T, "weight_copies": copies,
+                   "l2": "inputs larger than L2: %d weight copies with their token batches cycled" % copies,
+                   "graphs": "one CUDA graph per copy (route map, rotate, projection), replayed"},
+        "roofline": {"bound": "tensor", "kernel": "whole call: k_linear_map + k_rotate_quant + k_tc_fc<FC2> (tcgen05)",
+                     "achieved": round(achieved, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": None,
+                     "peak_source": pk["source"] + " (bf16 dense burst; fp16 runs at the bf16 rate)",
+                     "flops_per_launch": flops},
+        "e2e": None, "gpu_launches": 3 * args.steps, "clocks": sampler.summary(),
+    }
+    return res, (lins[0], T)
+
+
+def linear_cpu_baseline(lin, T, budget_s=10.0):
+    """The float64 oracle on a bounded sample of the linear workload's tokens
+    (weights decoded once, counted in the time)."""
+    from oracle import linear as olinear
+    x = synth.make_linear_tokens(lin, T, seed=1000)
+    t0 = time.perf_counter()
+    w = olinear.linear_weights(lin)
+    done, n = 0, 64
+    while True:
+        olinear.linear_apply(lin, synth.bf16_to_f64(x[done % T:done % T + n]), True, w)
+        done += n
+        el = time.perf_counter() - t0
+        if el > budget_s:
+            break
+    return {"value": round(done / el, 3), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": "%d tokens of the linear workload in %.1f s (oracle: decode W once, float64 rotations and GEMM)"
+                      % (done, el)}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS) + ["linear"])
     ap.add_argument("--tokens", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -403,6 +517,17 @@ def main():
     if world > 1:
         import torch
         torch.distributed.init_process_group("gloo")
+    if args.workload == "linear":
+        res, (lin, T) = run_linear(args, rank, world)
+        if rank == 0:
+            if not args.no_cpu_baseline:
+                res["cpu_baseline"] = linear_cpu_baseline(lin, T)
+            print(json.dumps(res), flush=True)
+        if world > 1:
+            import torch
+            torch.distributed.barrier()
+            torch.distributed.destroy_process_group()
+        return
     res, (cfg, T, mode, _) = run_ours(args, rank, world)
     if rank == 0:
         if not args.no_cpu_baseline:

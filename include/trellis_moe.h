@@ -248,6 +248,53 @@ const char* trellis_moe_last_error(void);
 /* Free the handle and its descriptor tables (not the caller's arrays). */
 void trellis_moe_destroy(tm_layer* layer);
 
+/* ------------------------------------------------------------------------
+ * Dense trellis-coded linear layer (no routing): one matrix W~ [N, K] with
+ * the layer's weight code, output scales and Hadamard-and-sign rotations, for
+ * dense projections (sparkinfer PR #90 "moe: integrate EXL3 Trellis into the
+ * fused W4A16 API", review of kernel.py: run_trellis256_dense and of
+ * tests/gemm/test_trellis_linear.py). For bf16 x [T, K]:
+ *   x~  = Hblk_in(suh (.) x) rounded to fp16,
+ *   out = svh (.) Hblk_out(s (.) (W~ x~))          fp32 [T, N]
+ * with an FP16 x FP16 -> FP32 tensor-core contraction (W4A16). */
+typedef struct tm_linear tm_linear;
+
+typedef struct {
+  int32_t N, K;             /* output / input channels: multiples of 128 */
+  int32_t bits;             /* trellis K of every weight, 2..6 */
+  int32_t rot_in, rot_out;  /* Hadamard blocks along K and N: 1, 64 or 128, dividing them */
+  int32_t max_tokens;       /* workspace_bytes from prepare covers T <= max_tokens */
+  /* DEVICE pointers, caller-owned, 16-byte aligned, outliving the handle: */
+  const int16_t* payload;   /* [N/16][K/16][16*bits] words, tile (tn, tk) weight j at
+                               row 16 tn + j/16, column 16 tk + j%16 (as the layer's) */
+  const uint16_t* scale;    /* fp16 [N] */
+  const uint16_t* suh;      /* fp16 [K] input signs */
+  const uint16_t* svh;      /* fp16 [N] output signs */
+} tm_linear_desc;
+
+/* Validates desc and uploads two small tables; *workspace_bytes = the
+ * workspace a call of max_tokens tokens needs. Errors: TM_EINVAL,
+ * TM_EUNSUPPORTED, TM_ECUDA. */
+tm_status trellis_linear_prepare(const tm_linear_desc* desc, tm_linear** out, size_t* workspace_bytes);
+
+/* Workspace bytes for a call of max_tokens tokens (0 for a NULL handle). */
+size_t trellis_linear_workspace_size(const tm_linear* lin, int32_t max_tokens);
+
+/* x bf16 [T, K] (8-byte aligned), out fp32 [T, N] (16-byte aligned, written),
+ * workspace >= trellis_linear_workspace_size(lin, T) bytes, 256-byte aligned
+ * (contents on entry ignored), T <= max_tokens. Enqueued on `stream`; no
+ * allocation, graph-capturable. T = 0 is a no-op. The first 4 bytes of the
+ * workspace are the device error word (bit 1: a pipeline wait gave up).
+ * Errors: TM_EINVAL, TM_EWORKSPACE, TM_ECUDA. */
+tm_status trellis_linear_forward(tm_linear* lin, const uint16_t* x, int32_t T, float* out, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/* Read and clear the device error word of `workspace` (synchronises
+ * `stream`). Returns TM_EDEVICE if any flag was set, else TM_OK. */
+tm_status trellis_linear_poll_error(tm_linear* lin, void* workspace, uint32_t* flags, void* stream);
+
+void trellis_linear_destroy(tm_linear* lin);
+
 #ifdef __cplusplus
 }
 #endif

@@ -19,7 +19,7 @@ def lib():
 
 def declared():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"\b(trellis_moe_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(trellis_(?:moe|linear)_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_boundary():
@@ -64,5 +64,18 @@ def test_host_validation_without_gpu(lib):
     assert lib.trellis_moe_forward(None, P(8), P(8), P(8), 1, 0, P(8), P(256), 1 << 20, None) == -1
     assert lib.trellis_moe_set_stage_events(None, None, 0) == -1
     assert lib.trellis_moe_set_decode_lut(None, 1) == -1
+    # dense linear: shape checks before any CUDA call, NULL handles
+    ld = binding.LinearDesc()
+    ld.N, ld.K, ld.bits, ld.rot_in, ld.rot_out, ld.max_tokens = 256, 200, 4, 128, 128, 8
+    assert lib.trellis_linear_prepare(ctypes.byref(ld), ctypes.byref(h), None) == -2
+    assert b"K=200" in lib.trellis_moe_last_error()
+    ld.K, ld.rot_out = 256, 32
+    assert lib.trellis_linear_prepare(ctypes.byref(ld), ctypes.byref(h), None) == -2
+    ld.rot_out = 64
+    assert lib.trellis_linear_prepare(ctypes.byref(ld), ctypes.byref(h), None) == -1   # NULL payload
+    assert b"payload" in lib.trellis_moe_last_error()
+    assert lib.trellis_linear_forward(None, P(8), 1, P(16), P(256), 1 << 20, None) == -1
+    assert lib.trellis_linear_workspace_size(None, 4) == 0
+    lib.trellis_linear_destroy(None)
     lib.trellis_moe_destroy(None)
 

@@ -32,6 +32,8 @@ EXPORTED = [
     "trellis_moe_workspace_region", "trellis_moe_set_stage_events", "trellis_moe_set_decode_lut",
     "trellis_moe_poll_error",
     "trellis_moe_last_error", "trellis_moe_destroy", "trellis_moe_route_map_static",
+    "trellis_linear_prepare", "trellis_linear_workspace_size", "trellis_linear_forward",
+    "trellis_linear_poll_error", "trellis_linear_destroy",
 ]
 
 
@@ -45,6 +47,14 @@ class LayerDesc(ctypes.Structure):
         ("in_suh", ctypes.c_void_p), ("rot_tab", ctypes.c_void_p), ("out_svh", ctypes.c_void_p),
         ("max_tokens", ctypes.c_int32), ("decode_max_rows", ctypes.c_int32), ("deterministic", ctypes.c_int32),
     ]
+
+
+class LinearDesc(ctypes.Structure):
+    """tm_linear_desc (include/trellis_moe.h)."""
+    _fields_ = [("N", ctypes.c_int32), ("K", ctypes.c_int32), ("bits", ctypes.c_int32),
+                ("rot_in", ctypes.c_int32), ("rot_out", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
+                ("payload", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("suh", ctypes.c_void_p),
+                ("svh", ctypes.c_void_p)]
 
 
 class TrellisMoEError(RuntimeError):
@@ -82,6 +92,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "trellis_moe_last_error": (ctypes.c_char_p, []),
         "trellis_moe_destroy": (None, [P]),
         "trellis_moe_route_map_static": (I32, [P, I32, I32, I32, I32, P, P, P, P, P]),
+        "trellis_linear_prepare": (I32, [ctypes.POINTER(LinearDesc), ctypes.POINTER(P), ctypes.POINTER(SZ)]),
+        "trellis_linear_workspace_size": (SZ, [P, I32]),
+        "trellis_linear_forward": (I32, [P, P, I32, P, P, SZ, P]),
+        "trellis_linear_poll_error": (I32, [P, P, ctypes.POINTER(ctypes.c_uint32), P]),
+        "trellis_linear_destroy": (None, [P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -296,6 +311,67 @@ class TrellisMoE:
     def poll_error(self, stream=None) -> int:
         flags = ctypes.c_uint32()
         st = self.lib.trellis_moe_poll_error(self.handle, _ptr(self.workspace), ctypes.byref(flags), _stream_ptr(stream))
+        if st not in (TM_OK, -5):
+            _check(st)
+        return int(flags.value)
+
+
+class TrellisLinear:
+    """One prepared dense trellis linear layer. ``lin`` has the fields of
+    ``synth.Linear`` (numpy, fp16 as uint16 bit patterns); its arrays are
+    uploaded once."""
+
+    def __init__(self, lin, max_tokens: int):
+        torch = _torch()
+        self.lib = load_library()
+        self.N, self.K = int(lin.N), int(lin.K)
+        self.payload = to_device_u16(lin.payload)
+        self.scale = to_device_u16(lin.scale)
+        self.suh = to_device_u16(lin.suh)
+        self.svh = to_device_u16(lin.svh)
+        d = LinearDesc()
+        d.N, d.K, d.bits = self.N, self.K, int(lin.bits)
+        d.rot_in, d.rot_out = int(lin.rot_in), int(lin.rot_out)
+        d.max_tokens = int(max_tokens)
+        d.payload = self.payload.data_ptr()
+        d.scale = self.scale.data_ptr()
+        d.suh = self.suh.data_ptr()
+        d.svh = self.svh.data_ptr()
+        self.desc = d
+        handle = ctypes.c_void_p()
+        ws = ctypes.c_size_t()
+        _check(self.lib.trellis_linear_prepare(ctypes.byref(d), ctypes.byref(handle), ctypes.byref(ws)))
+        self.handle = handle
+        self.workspace_bytes = int(ws.value)
+        self.workspace = torch.empty(self.workspace_bytes + 256, dtype=torch.uint8, device="cuda")
+        off = (-self.workspace.data_ptr()) % 256
+        self.workspace = self.workspace[off:off + self.workspace_bytes]
+
+    def close(self):
+        if getattr(self, "handle", None):
+            self.lib.trellis_linear_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def forward(self, x, out=None, stream=None):
+        """x bf16/int16 [T, K] -> float32 [T, N]."""
+        torch = _torch()
+        T = int(x.shape[0])
+        if out is None:
+            out = torch.empty((T, self.N), dtype=torch.float32, device="cuda")
+        _check(self.lib.trellis_linear_forward(self.handle, _ptr(x), T, _ptr(out), _ptr(self.workspace),
+                                               self.workspace_bytes, _stream_ptr(stream)))
+        return out
+
+    def poll_error(self, stream=None) -> int:
+        flags = ctypes.c_uint32(0)
+        st = self.lib.trellis_linear_poll_error(self.handle, _ptr(self.workspace), ctypes.byref(flags),
+                                                _stream_ptr(stream))
         if st not in (TM_OK, -5):
             _check(st)
         return int(flags.value)

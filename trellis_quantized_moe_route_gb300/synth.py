@@ -33,6 +33,7 @@ import numpy as np
 # order in which they are requested.
 _S_BITS, _S_FC1, _S_FC2, _S_S1, _S_S2, _S_SUH, _S_ROT, _S_SVH = range(8)
 _S_X, _S_LOGITS, _S_PERM, _S_GUMBEL = 100, 101, 102, 103
+_S_LIN_W, _S_LIN_S, _S_LIN_SUH, _S_LIN_SVH, _S_LIN_X = 300, 301, 302, 303, 304
 
 
 @dataclasses.dataclass(frozen=True)
@@ -227,3 +228,38 @@ def random_ids(seed: int, T: int, E: int, k: int) -> np.ndarray:
     for t in range(T):
         out[t] = permutation(s, E)[:k]
     return out
+
+
+@dataclasses.dataclass
+class Linear:
+    """Host copy of one dense trellis-coded linear layer: W~ [N, K] as tiles
+    [N/16][K/16][16*bits] int16 words, output scales and signs [N], input
+    signs [K] (fp16 stored as uint16 bit patterns)."""
+
+    N: int
+    K: int
+    bits: int
+    rot_in: int
+    rot_out: int
+    payload: np.ndarray   # int16 [N/16 * K/16 * 16 * bits]
+    scale: np.ndarray     # uint16 (fp16) [N]
+    suh: np.ndarray       # uint16 (fp16) [K]
+    svh: np.ndarray       # uint16 (fp16) [N]
+
+
+def make_linear(N: int, K: int, bits: int = 4, rot_in: int = 128, rot_out: int = 128, seed: int = 5) -> Linear:
+    """Draw a dense trellis linear layer with the layer recipe (uniform payload
+    words, fp16 U[0.01, 0.03] scales, +-1 signs)."""
+    n = (N // 16) * (K // 16) * 16 * bits
+    return Linear(
+        N=N, K=K, bits=bits, rot_in=rot_in, rot_out=rot_out,
+        payload=Stream(seed, _S_LIN_W).words16(n),
+        scale=fp16_bits(0.01 + 0.02 * Stream(seed, _S_LIN_S).uniform(N)),
+        suh=_signs(Stream(seed, _S_LIN_SUH), K),
+        svh=_signs(Stream(seed, _S_LIN_SVH), N),
+    )
+
+
+def make_linear_tokens(lin: Linear, T: int, seed: int = 5) -> np.ndarray:
+    """Activations for a dense linear: bf16 bit patterns of N(0, 1), [T, K]."""
+    return bf16_bits(Stream(seed, _S_LIN_X).normal(T * lin.K)).reshape(T, lin.K)
