@@ -25,6 +25,7 @@ Modules:
   mxfp8     - E4M3 rounding and the UE8M0 (E8M0) block exponent
   route     - top-k softmax router and the stable route map
   layer     - the whole layer (W4A16 and W4A8)
+  linear    - the dense trellis linear layer (one matrix, no routing; W4A16)
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 against closed forms, hand-computed values, invariants or brute force. One
