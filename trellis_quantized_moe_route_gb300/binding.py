@@ -125,6 +125,18 @@ def _stream_ptr(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _raw_stream(stream=None) -> int:
+    """The CUDA stream handle as an int: the given stream's, else the current
+    one's (read without building a Stream object where torch offers that)."""
+    if stream is not None:
+        return stream.cuda_stream
+    torch = _torch()
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return raw(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
+
+
 def _ptr(t) -> ctypes.c_void_p:
     return ctypes.c_void_p(t.data_ptr())
 
@@ -239,11 +251,16 @@ class TrellisMoE:
         return out
 
     def forward_host(self, x_host, logits_host, out_host, mode="auto", stream=None):
-        """Host (pinned CPU tensor) inputs and output; synchronises the stream."""
-        T = int(x_host.shape[0])
-        _check(self.lib.trellis_moe_forward_host(self.handle, _ptr(x_host), _ptr(logits_host), T,
-                                                 MODES.get(mode, mode), _ptr(out_host), _ptr(self.workspace),
-                                                 self.workspace_bytes, _stream_ptr(stream)))
+        """Host (pinned CPU tensor) inputs and output; synchronises the stream.
+        The per-call marshalling is kept to plain ints: it is part of every
+        end-to-end call."""
+        fh = self.__dict__.get("_forward_host_fn")
+        if fh is None:
+            fh = self._forward_host_fn = self.lib.trellis_moe_forward_host
+        st = fh(self.handle, x_host.data_ptr(), logits_host.data_ptr(), x_host.shape[0], MODES.get(mode, mode),
+                out_host.data_ptr(), self.workspace.data_ptr(), self.workspace_bytes, _raw_stream(stream))
+        if st != TM_OK:
+            _check(st)
         return out_host
 
     # -- single steps (parity tests) -------------------------------------
