@@ -8,6 +8,8 @@ the top-k sum):
 
   1. x~ = Hblk_H(suh (.) x)                        input rotation
   2. y1 = s1 (.) (W1~ x~)          per route        FC1, gate rows 0..I-1, up rows I..2I-1
+     (with separate gate / up input signs, shared or per expert, the gate
+     rows see x~_g = Hblk_H(gate_suh_e (.) x) and the up rows x~_u)
   3. g = svh_g (.) Hblk_I(y1_gate), u = svh_u (.) Hblk_I(y1_up)
      a = SiLU(g) * u,  z~ = Hblk_I(suh_d (.) a)     activation epilogue
   4. y2 = s2 (.) (W2~ z~)                           FC2
@@ -53,10 +55,26 @@ def expert_weights(layer, proj: int, e: int, mode: str = "w4a16") -> np.ndarray:
     return w
 
 
-def rotate_input(layer, x_bits: np.ndarray) -> np.ndarray:
-    """Step 1 in float64: [T, H]."""
+def rotate_input(layer, x_bits: np.ndarray, suh: np.ndarray = None) -> np.ndarray:
+    """Step 1 in float64: [T, H] (suh: fp16 bits [H], default the shared in_suh)."""
     x = bf16_to_f64(x_bits)
-    return hadamard.rotate(x * fp16_to_f64(layer.in_suh)[None, :], layer.rot_block_h)
+    suh = layer.in_suh if suh is None else suh
+    return hadamard.rotate(x * fp16_to_f64(suh)[None, :], layer.rot_block_h)
+
+
+def input_signs(layer, e: int):
+    """The (gate, up) input sign vectors of expert e (fp16 bits [H] each):
+    the separate gate_suh / up_suh rows when the layer has them (one row
+    shared by the experts, or one per expert; b12x PR #129, review of
+    trellis_w4a8.py: gate_suh and up_suh of shape (1, H) or (num_experts, H)),
+    else the shared in_suh for both."""
+    g = getattr(layer, "gate_suh", None)
+    u = getattr(layer, "up_suh", None)
+    if g is None and u is None:
+        return layer.in_suh, layer.in_suh
+    g = np.asarray(g).reshape(-1, layer.H)
+    u = np.asarray(u).reshape(-1, layer.H)
+    return g[e if g.shape[0] > 1 else 0], u[e if u.shape[0] > 1 else 0]
 
 
 def round_operand(v: np.ndarray, mode: str, act_round: bool = True) -> np.ndarray:
@@ -69,9 +87,10 @@ def round_operand(v: np.ndarray, mode: str, act_round: bool = True) -> np.ndarra
 
 
 def expert_ffn(layer, e: int, xq: np.ndarray, mode: str, act_round: bool = True,
-               w1: np.ndarray = None, w2: np.ndarray = None) -> np.ndarray:
-    """Steps 2-5 (before the route weight) for the rows xq [n, H] routed to e.
-    Returns svh_d (.) Hblk_H(y2) as [n, H]."""
+               w1: np.ndarray = None, w2: np.ndarray = None, xq_up: np.ndarray = None) -> np.ndarray:
+    """Steps 2-5 (before the route weight) for the rows xq [n, H] routed to e
+    (xq_up: the up rows' own operand when the gate and up input signs
+    differ; default xq). Returns svh_d (.) Hblk_H(y2) as [n, H]."""
     I = layer.I
     if w1 is None:
         w1 = expert_weights(layer, 1, e, mode)
@@ -82,7 +101,10 @@ def expert_ffn(layer, e: int, xq: np.ndarray, mode: str, act_round: bool = True,
     rot = fp16_to_f64(layer.rot_tab[e])
     svh_g, svh_u, suh_d = rot[:I], rot[I:2 * I], rot[2 * I:]
     svh_d = fp16_to_f64(layer.out_svh[e])
-    y1 = s1[None, :] * (xq @ w1.T)
+    if xq_up is None:
+        y1 = s1[None, :] * (xq @ w1.T)
+    else:
+        y1 = s1[None, :] * np.concatenate([xq @ w1[:I].T, xq_up @ w1[I:].T], axis=1)
     g = svh_g[None, :] * hadamard.rotate(y1[:, :I], layer.rot_block_i)
     u = svh_u[None, :] * hadamard.rotate(y1[:, I:], layer.rot_block_i)
     a = g / (1.0 + np.exp(-g)) * u
@@ -102,13 +124,22 @@ def layer_forward(layer, x_bits: np.ndarray, ids: np.ndarray, w: np.ndarray,
     ids = np.asarray(ids)
     w = np.asarray(w, dtype=np.float64)
     k = ids.shape[1]
-    xr = rotate_input(layer, x_bits[tokens])
-    xq = round_operand(xr, mode, act_round)
+    separate = getattr(layer, "gate_suh", None) is not None or getattr(layer, "up_suh", None) is not None
+    if not separate:
+        xq = round_operand(rotate_input(layer, x_bits[tokens]), mode, act_round)
     per_route = np.zeros((len(tokens), k, layer.H), dtype=np.float64)
     sub_ids = ids[tokens]
     for e in np.unique(sub_ids):
         rows, js = np.nonzero(sub_ids == e)
-        per_route[rows, js] = expert_ffn(layer, int(e), xq[rows], mode, act_round)
+        if not separate:
+            per_route[rows, js] = expert_ffn(layer, int(e), xq[rows], mode, act_round)
+        else:
+            # one rotation per route: the expert's gate and up signs
+            sg, su = input_signs(layer, int(e))
+            xe = x_bits[tokens][rows]
+            xg = round_operand(rotate_input(layer, xe, sg), mode, act_round)
+            xu = round_operand(rotate_input(layer, xe, su), mode, act_round)
+            per_route[rows, js] = expert_ffn(layer, int(e), xg, mode, act_round, xq_up=xu)
     out = np.zeros((len(tokens), layer.H), dtype=np.float64)
     for j in range(k):                     # fixed per-token order j = 0..k-1
         out += w[tokens, j][:, None] * per_route[:, j]

@@ -181,6 +181,9 @@ class TrellisMoE:
     fp16 as uint16 bit patterns); its arrays are uploaded once."""
 
     def __init__(self, layer, max_tokens: int, decode_max_rows: int = 8, deterministic: bool = True):
+        if getattr(layer, "gate_suh", None) is not None or getattr(layer, "up_suh", None) is not None:
+            raise NotImplementedError("separate gate / up input signs are not on the CUDA path: "
+                                      "the layer takes one shared input sign vector (in_suh [H])")
         torch = _torch()
         self.lib = load_library()
         self.E, self.H, self.I, self.topk = int(layer.E), int(layer.H), int(layer.I), int(layer.topk)

@@ -34,6 +34,7 @@ import numpy as np
 _S_BITS, _S_FC1, _S_FC2, _S_S1, _S_S2, _S_SUH, _S_ROT, _S_SVH = range(8)
 _S_X, _S_LOGITS, _S_PERM, _S_GUMBEL = 100, 101, 102, 103
 _S_LIN_W, _S_LIN_S, _S_LIN_SUH, _S_LIN_SVH, _S_LIN_X = 300, 301, 302, 303, 304
+_S_GATE_SUH, _S_UP_SUH = 400, 401
 
 
 @dataclasses.dataclass(frozen=True)
@@ -154,6 +155,10 @@ class Layer:
     in_suh: np.ndarray        # uint16 (fp16) [H]
     rot_tab: np.ndarray       # uint16 (fp16) [E, 3I] = gate svh | up svh | down suh
     out_svh: np.ndarray       # uint16 (fp16) [E, H]
+    # optional input sign layouts: separate gate and up signs, each [1, H]
+    # (shared by the experts) or [E, H] (per expert); None = in_suh for both
+    gate_suh: Optional[np.ndarray] = None
+    up_suh: Optional[np.ndarray] = None
 
 
 def make_layer(cfg: LayerConfig, seed: Optional[int] = None,
@@ -263,3 +268,14 @@ def make_linear(N: int, K: int, bits: int = 4, rot_in: int = 128, rot_out: int =
 def make_linear_tokens(lin: Linear, T: int, seed: int = 5) -> np.ndarray:
     """Activations for a dense linear: bf16 bit patterns of N(0, 1), [T, K]."""
     return bf16_bits(Stream(seed, _S_LIN_X).normal(T * lin.K)).reshape(T, lin.K)
+
+
+def with_input_signs(layer: Layer, rows: int, seed: int = 9) -> Layer:
+    """A copy of ``layer`` with separate gate and up input signs of ``rows``
+    rows (1: shared by the experts, E: per expert), drawn as +-1."""
+    assert rows in (1, layer.E)
+    return dataclasses.replace(
+        layer,
+        gate_suh=_signs(Stream(seed, _S_GATE_SUH), rows * layer.H).reshape(rows, layer.H),
+        up_suh=_signs(Stream(seed, _S_UP_SUH), rows * layer.H).reshape(rows, layer.H),
+    )
