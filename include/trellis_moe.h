@@ -38,10 +38,17 @@
  *     returns an error has launched nothing and written nothing.
  *   - Errors: a negative tm_status; trellis_moe_last_error() gives a message
  *     for the calling thread.
- *   - No entry point other than trellis_moe_prepare allocates device memory.
- *     trellis_moe_forward* use only the caller's workspace, launch only on
+ *   - Only trellis_moe_prepare and trellis_linear_prepare allocate device
+ *     memory (small descriptor tables), and trellis_moe_forward_host builds
+ *     the CUDA graphs it caches on the handle (see there).
+ *     trellis_moe_forward, trellis_moe_forward_logits and
+ *     trellis_linear_forward use only the caller's workspace, launch only on
  *     `stream`, and can be captured in a CUDA graph (the workspace pointer must
- *     then stay the same for every replay).
+ *     then stay the same for every replay); trellis_moe_forward_host
+ *     synchronises its stream and is not capturable.
+ *
+ * Also here: a dense trellis-coded linear layer on the same kernels
+ * (trellis_linear_*, at the end of this file).
  */
 #ifndef TRELLIS_MOE_H_
 #define TRELLIS_MOE_H_
