@@ -107,7 +107,10 @@ def expert_ffn(layer, e: int, xq: np.ndarray, mode: str, act_round: bool = True,
         y1 = s1[None, :] * np.concatenate([xq @ w1[:I].T, xq_up @ w1[I:].T], axis=1)
     g = svh_g[None, :] * hadamard.rotate(y1[:, :I], layer.rot_block_i)
     u = svh_u[None, :] * hadamard.rotate(y1[:, I:], layer.rot_block_i)
-    a = g / (1.0 + np.exp(-g)) * u
+    # SiLU(g) = g / (1 + e^-g); for large negative g, e^-g overflows to inf and
+    # the quotient is the correct -0, so the overflow warning is silenced
+    with np.errstate(over="ignore"):
+        a = g / (1.0 + np.exp(-g)) * u
     z = hadamard.rotate(suh_d[None, :] * a, layer.rot_block_i)
     zq = round_operand(z, mode, act_round)
     y2 = s2[None, :] * (zq @ w2.T)

@@ -7,7 +7,7 @@ Description: one UE8M0 byte per 32 values; Evidence, precision notes: the
 exponent comes from the exact FP32 bits of amax / 448 and is clamped to
 [-127, 127]).
 
-Readings (listed in DESIGN.md):
+Readings where the pages leave the step open:
   * The exponent is the ceiling of log2(q), q = fp32(amax / 448) with IEEE
     round-to-nearest-even division, i.e. the smallest e with 2^e >= q. The
     precision note objects to a log2 that rounds quotients just above a power

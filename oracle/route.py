@@ -14,7 +14,7 @@ kernel with BLOCK_SIZE, expert_offsets and packed_route_count; b12x PR #433
 "Share trellis preparation across native and EXL3 containers", review of
 route_pack.py: a stable, token-major route order).
 
-Readings (listed in DESIGN.md):
+Readings where the pages leave the step open:
   * Router ties between equal logits go to the lower expert id; the k selected
     experts are listed by descending logit. The weights are
     exp(l_j - max) / sum over the k selected of exp(l - max), which equals a

@@ -10,7 +10,8 @@ Format facts from the pages:
   * Each weight is addressed by a 16-bit state of a bitshift trellis that wraps
     around the tile (tail-biting).
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent (each a free format choice or the plainest
+reading of the constants; the CUDA decoder follows the same statement):
   * Stream order: bit p of a tile's stream is bit (15 - p mod 16) of int16 word
     floor(p / 16) -- most significant bit first, words in storage order.
   * State of weight j (0..255): the 16 stream bits p = (j+1)K-16 .. (j+1)K-1,
