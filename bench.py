@@ -16,9 +16,12 @@ copy exceed 2x L2) and through as many token batches.
 
 Output: one JSON line on rank 0. ``roofline`` is for the dominant kernel
 (FC1): algorithmic bytes (or FLOPs) per launch divided by its CUDA-event
-duration, timed inside the captured graphs of the timed region.
-``cpu_baseline`` times the float64 CPU oracle on a bounded sample.
-``--impl reference`` runs only that oracle (the CPU reference arm).
+duration, timed inside the captured graphs of the timed region. The default
+run also measures the metric's other configurations -- decode at T = 1, 2
+and 4 and the T=2048 W4A16 prefill -- each with the same keys, under
+``sub`` (``--no-sub`` skips them). ``cpu_baseline`` times the float64 CPU
+oracle on a bounded sample. ``--impl reference`` runs only that oracle (the
+CPU reference arm).
 """
 from __future__ import annotations
 
@@ -131,7 +134,7 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------- ours ---
-def touched_bytes_fc1(cfg, ids, T):
+def touched_bytes_fc1(cfg, ids, T, mode):
     """Algorithmic DRAM bytes of one FC1 launch: trellis payload, per-channel
     scales and rotation rows of every touched expert, the quantised input rows
     read, and the FC1 epilogue's output rows written."""
@@ -139,31 +142,44 @@ def touched_bytes_fc1(cfg, ids, T):
     K = max(cfg.bits)
     d = len(np.unique(ids))
     R = ids.size
-    act_b = 1 if WORK_MODE[0] == "w4a8" else 2
+    act_b = 1 if mode == "w4a8" else 2
     weights = d * (2 * I * H * K // 8 + 2 * I * 2 + 3 * I * 2)
     acts = T * H * act_b + (T * H // 32 if act_b == 1 else 0)
     outs = R * I * act_b + (R * I // 32 if act_b == 1 else 0)
     return weights + acts + outs, d
 
 
-WORK_MODE = ["w4a8"]
 
-
-def run_ours(args, rank, world):
+def sleep_ahead(stream, us: float = 2000.0):
+    """A device-side spin on `stream` ahead of the timed region, so that the
+    host has queued the timed steps before the first one starts and the
+    region measures device throughput, not the host's launch latency."""
     import torch
-    from trellis_quantized_moe_route_gb300 import binding, build
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(us * 2.0e3))   # ~us at 2 GHz
 
-    dev = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(dev)
-    build.build()
-    binding.load_library()
-    cfg_name, T_default, mode = WORKLOADS[args.workload]
-    WORK_MODE[0] = mode
-    cfg = synth.CONFIGS[cfg_name]
-    T = args.tokens or T_default
+
+def sampler_started(dev):
+    """A clock sampler whose first sample is taken before the timed region."""
+    smp = ClockSampler(dev)
+    smp.start()
+    t_end = time.time() + 5.0
+    while not smp.samples and time.time() < t_end:
+        time.sleep(0.01)
+    return smp
+
+
+def measure_layer(name, T, mode, steps, warmup, rank, world, dev, e2e_steps):
+    """One workload of the layer: graphs per (layer copy, token batch), K timed
+    steps between CUDA events on the launching stream, stage durations from
+    events recorded inside the last few timed steps, and the host-buffer call
+    end to end. Returns the record (metric keys, roofline, stages, e2e)."""
+    import torch
+    from trellis_quantized_moe_route_gb300 import binding
+
+    cfg = synth.CONFIGS[name]
     K = max(cfg.bits)
     R = T * cfg.topk
-
     # layer copies at distinct addresses so that the bytes touched between two
     # uses of one copy exceed twice the L2
     layer = synth.make_layer(cfg)
@@ -182,14 +198,14 @@ def run_ours(args, rank, world):
 
     # warm-up (eager; also fixes kernel attributes before capture)
     with torch.cuda.stream(stream):
-        for i in range(max(args.warmup, 1)):
+        for i in range(max(warmup, 1)):
             b = i % copies
             moes[b].forward_logits(batches[b][0], batches[b][1], mode=mode, out=batches[b][2])
     torch.cuda.synchronize()
 
     # per (copy, batch): one plain graph and one that also records the
-    # library's stage-boundary events (used for the last `copies` timed steps,
-    # so that the per-kernel durations come from inside the timed region)
+    # library's stage-boundary events (used for the last few timed steps, so
+    # that the per-kernel durations come from inside the timed region)
     graphs, graphs_ev, evsets = [], [], []
     for b in range(copies):
         g = torch.cuda.CUDAGraph()
@@ -207,26 +223,26 @@ def run_ours(args, rank, world):
         moes[b].set_stage_events(None)
         graphs_ev.append(ge)
         evsets.append(evs)
-    for i in range(max(args.warmup, 3)):
+    for i in range(max(warmup, 3)):
         graphs[i % copies].replay()
         graphs_ev[i % copies].replay()
     torch.cuda.synchronize()
 
-    sampler = ClockSampler(dev)
+    sampler = sampler_started(dev)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    sampler.start()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    sleep_ahead(stream)
     t0.record(stream)
     # the last three timed steps (or fewer) use the event-recording graphs: the
     # stage statistics need only a few samples, and every recorded event adds
     # its own overhead to the timed region
-    n_ev = min(copies, args.steps, 3)
+    n_ev = min(copies, steps, 3)
     with torch.cuda.stream(stream):
-        for i in range(args.steps):
-            (graphs_ev if i >= args.steps - n_ev else graphs)[i % copies].replay()
+        for i in range(steps):
+            (graphs_ev if i >= steps - n_ev else graphs)[i % copies].replay()
     t1.record(stream)
     torch.cuda.synchronize()
     sampler.stop()
@@ -236,7 +252,7 @@ def run_ours(args, rank, world):
 
     # stage times of the event graphs replayed at the end of the timed region
     stage = {k: [] for k in ("router", "route_map", "rotate", "fc1", "fc2", "combine", "step")}
-    used = sorted(set(i % copies for i in range(args.steps - n_ev, args.steps)))
+    used = sorted(set(i % copies for i in range(steps - n_ev, steps)))
     for evs in [evsets[i] for i in used]:
         e = [evs[i] for i in range(7)]
         stage["router"].append(e[0].elapsed_time(e[1]) * 1e3)
@@ -247,48 +263,44 @@ def run_ours(args, rank, world):
         stage["combine"].append(e[5].elapsed_time(e[6]) * 1e3)
         stage["step"].append(e[0].elapsed_time(e[6]) * 1e3)
     stages_us = {k: round(statistics.mean(v), 3) for k, v in stage.items()}
+    for m in moes:
+        assert m.poll_error() == 0
 
     # algorithmic work per FC1 launch, from each batch's routes
     fc1_bytes, distinct = [], []
     for b in used:
         ids, _ = binding.route(batches[b][1], cfg.topk)
-        nb, d = touched_bytes_fc1(cfg, ids.cpu().numpy(), T)
+        nb, d = touched_bytes_fc1(cfg, ids.cpu().numpy(), T, mode)
         fc1_bytes.append(nb)
         distinct.append(d)
     pk = peaks()
-    # DRAM bytes per launch of the dominant kernel from one ncu capture of this
-    # program (profiles/); None for workloads without a capture
-    ncu_traffic = {"decode": (28.387e6, "profiles/k_dec_warp_fc1_decode_w4a8_T8.md"),
-                   "prefill": (127.79e6, "profiles/k_tc_fc_fc1_prefill_w4a16_T2048.md")}.get(args.workload)
-    if mode == "w4a8" and T <= 64:
+    decode_path = R <= 1024 and (mode == "w4a8" or R < 4 * cfg.E)   # the library's decode-rows regime
+    ncu = NCU_TRAFFIC.get((name, T, mode))
+    if decode_path:
         achieved = statistics.mean(fc1_bytes) / (stages_us["fc1"] * 1e-6) / 1e9
-        roof = {"bound": "hbm", "kernel": "k_dec_warp<W4A8,FC1,K=4> (decode rows, persistent warp items)"
-                if R <= 1024 and R < 4 * cfg.E else "k_tc_fc<FC1,K=4,W4A8> (tcgen05)",
+        roof = {"bound": "hbm", "kernel": "k_dec_warp<%s,FC1,K=%d> (decode rows, persistent warp items)" % (
+                    mode.upper(), K),
                 "achieved": round(achieved, 1),
                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
-                "traffic": ncu_traffic[0] if ncu_traffic else None,
-                "traffic_source": ncu_traffic[1] if ncu_traffic else None,
+                "traffic": ncu[0] if ncu else None, "traffic_source": ncu[1] if ncu else None,
                 "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst)",
                 "bytes_per_launch": int(statistics.mean(fc1_bytes))}
     else:
         flops = 2 * R * 2 * cfg.I * cfg.H
         achieved = flops / (stages_us["fc1"] * 1e-6) / 1e12
-        kname = "k_tc_fc<FC1,%s> (tcgen05)" % ("W4A16" if mode == "w4a16" else "W4A8")
-        roof = {"bound": "tensor", "kernel": kname, "achieved": round(achieved, 2),
+        roof = {"bound": "tensor", "kernel": "k_tc_fc<FC1,K=%d> (tcgen05, W4A16)" % K, "achieved": round(achieved, 2),
                 "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4),
-                "traffic": ncu_traffic[0] if ncu_traffic else None,
-                "traffic_source": ncu_traffic[1] if ncu_traffic else None,
+                "traffic": ncu[0] if ncu else None, "traffic_source": ncu[1] if ncu else None,
                 "peak_source": pk["source"] + " (bf16 dense burst; fp16 runs at the bf16 rate)",
                 "flops_per_launch": flops}
 
     # end to end through the host-buffer C-ABI call
-    e2e_steps = min(args.steps, 200)
     xh = [torch.from_numpy(np.ascontiguousarray(b[3].view(np.int16))).pin_memory() for b in batches]
     lh = [torch.from_numpy(np.ascontiguousarray(b[4])).pin_memory() for b in batches]
     oh = [torch.empty((T, cfg.H), dtype=torch.float32).pin_memory() for _ in batches]
     with torch.cuda.stream(stream):
-        for i in range(min(3, copies)):
-            moes[i].forward_host(xh[i], lh[i], oh[i], mode=mode)
+        for i in range(min(3, copies) * 2):
+            moes[i % copies].forward_host(xh[i % copies], lh[i % copies], oh[i % copies], mode=mode)
     torch.cuda.synchronize()
     h0 = torch.cuda.Event(enable_timing=True)
     h1 = torch.cuda.Event(enable_timing=True)
@@ -299,7 +311,7 @@ def run_ours(args, rank, world):
             moes[b].forward_host(xh[b], lh[b], oh[b], mode=mode)
     h1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = h0.elapsed_time(h1)
+    e2e_ms = job_time_ms(h0.elapsed_time(h1), world)
     e2e = {"value": round(e2e_steps * T * world / (e2e_ms / 1e3), 2), "unit": "tokens/s",
            "h2d_bytes_per_step": T * cfg.H * 2 + T * cfg.E * 4, "d2h_bytes_per_step": T * cfg.H * 4,
            "steps": e2e_steps, "api": "trellis_moe_forward_host",
@@ -307,25 +319,72 @@ def run_ours(args, rank, world):
                        "logits and write the fp32 result over NVLink-C2C each call (no staging copies); the call "
                        "replays a graph cached for the buffer set and synchronises the stream"}
 
-    decode_path = R <= 1024 and R < 4 * cfg.E   # the library's decode-rows path
-    # decode rows: prologue, FC1, FC2 (with the combine); otherwise router, route map (1 or 3), rotate, FC1, FC2, combine
+    # decode rows: prologue, FC1, FC1 epilogue, FC2, FC2 epilogue; otherwise
+    # router, route map (1 or 3 kernels), rotate, FC1, FC2, combine
     launches_per_step = 5 if decode_path else 6 + (2 if R > 1024 else 0)
-    res = {
-        "metric": METRIC, "value": job_value(args.steps, T, world, total_ms), "unit": "tokens/s",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3" if mode == "w4a8" else "f16", "data": "synthetic",
-        "config": {"workload": "%s: H=%d I=%d E=%d top-k=%d K=%d %s T=%d" % (
-            args.workload, cfg.H, cfg.I, cfg.E, cfg.topk, K, mode.upper(), T),
-            "tokens_per_step": T, "layer_copies": copies,
-            "l2": "inputs larger than L2: %d layer copies and token batches cycled" % copies,
-            "distinct_experts_per_step": round(statistics.mean(distinct), 2),
-            "graphs": "one CUDA graph per (layer copy, batch), replayed; the last %d timed steps use "
-                      "graphs that also record stage events" % min(copies, args.steps)},
-        "roofline": roof, "stages_us": stages_us,
-        "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": sampler.summary(),
+    for m in moes:
+        m.close()
+    return {
+        "value": job_value(steps, T, world, total_ms), "unit": "tokens/s",
+        "ms_per_step": round(total_ms / steps, 5), "steps": steps,
+        "dtype": "e4m3" if mode == "w4a8" else "f16",
+        "config": {"workload": workload_string(name, cfg, K, mode, T), "tokens_per_step": T,
+                   "layer_copies": copies,
+                   "l2": "inputs larger than L2: %d layer copies and token batches cycled" % copies,
+                   "distinct_experts_per_step": round(statistics.mean(distinct), 2),
+                   "graphs": "one CUDA graph per (layer copy, batch), replayed; the last %d timed steps use "
+                             "graphs that also record stage events; a ~2 ms device-side spin precedes the "
+                             "timed region so that the host has queued the steps" % n_ev},
+        "roofline": roof, "stages_us": stages_us, "e2e": e2e,
+        "gpu_launches": launches_per_step * steps, "clocks": sampler.summary(),
     }
-    return res, (cfg, T, mode, batches)
+
+
+def workload_string(name, cfg, K, mode, T):
+    """The workload named identically by both arms."""
+    return "%s: H=%d I=%d E=%d top-k=%d K=%d %s T=%d" % (name, cfg.H, cfg.I, cfg.E, cfg.topk, K, mode.upper(), T)
+
+
+# DRAM bytes per launch of the dominant kernel from one ncu capture of this
+# program (profiles/); workloads without a capture of the current kernel get
+# None
+NCU_TRAFFIC = {
+    ("decode", 8, "w4a8"): (28.387e6, "profiles/k_dec_warp_fc1_decode_w4a8_T8.md"),
+}
+
+# The metric's other configurations, measured in the same run as the headline
+# (decode T=8): decode at T = 1, 2 and 4 and the T=2048 prefill.
+SUB_RUNS = [("decode", 1, "w4a8"), ("decode", 2, "w4a8"), ("decode", 4, "w4a8"), ("prefill", 2048, "w4a16")]
+
+
+def run_ours(args, rank, world):
+    import torch
+    from trellis_quantized_moe_route_gb300 import binding, build
+
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    build.build()
+    binding.load_library()
+    name, T_default, mode = WORKLOADS[args.workload]
+    cfg = synth.CONFIGS[name]
+    T = args.tokens or T_default
+    e2e_steps = min(args.steps, 200)
+    head = measure_layer(name, T, mode, args.steps, args.warmup, rank, world, dev, e2e_steps)
+    res = {"metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic", "config": head["config"],
+           "roofline": head["roofline"], "stages_us": head["stages_us"], "e2e": head["e2e"],
+           "gpu_launches": head["gpu_launches"], "clocks": head["clocks"]}
+    if args.workload == "decode" and not args.tokens and not args.no_sub:
+        subs = []
+        for (n2, t2, m2) in SUB_RUNS:
+            r = measure_layer(n2, t2, m2, args.steps, args.warmup, rank, world, dev, e2e_steps)
+            r["metric"] = METRIC
+            r["higher_is_better"] = True
+            subs.append(r)
+        res["sub"] = subs
+        res["gpu_launches"] += sum(r["gpu_launches"] for r in subs)
+    return res, (cfg, T, mode, None)
 
 
 # -------------------------------------------------------------- reference ---
@@ -386,8 +445,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * min(T, 8) / value, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "%s: H=%d I=%d E=%d top-k=%d %s T=%d" % (args.workload, cfg.H, cfg.I, cfg.E,
-                                                                      cfg.topk, mode.upper(), T)},
+        "config": {"workload": workload_string(cfg_name, cfg, max(cfg.bits), mode, T)},
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
                          "sample": "%d steps of about %.1f s each, up to 8 tokens per oracle call (%s)" % (
                              len(vals), budget, desc)},
@@ -509,6 +567,7 @@ def main():
     ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS) + ["linear"])
     ap.add_argument("--tokens", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub", action="store_true", help="headline workload only (no decode T=1/2/4 and prefill lines)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

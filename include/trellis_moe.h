@@ -72,9 +72,11 @@ typedef enum {
 } tm_status;
 
 typedef enum {
-  TM_MODE_AUTO = 0,   /* W4A8 when T <= decode_max_rows, else W4A16 */
+  TM_MODE_AUTO = 0,   /* W4A8 when T <= decode_max_rows and T*topk <= 1024, else W4A16 */
   TM_MODE_W4A16 = 1,  /* fp16 activations x fp16 codebook weights, fp32 accumulate */
-  TM_MODE_W4A8 = 2    /* MXFP8 activations x E4M3-rounded codebook weights */
+  TM_MODE_W4A8 = 2    /* MXFP8 activations x E4M3-rounded codebook weights; bounded
+                         decode rows only (b12x PR #129, Hot path): T*topk <= 1024,
+                         else the forward calls return TM_EUNSUPPORTED */
 } tm_mode;
 
 /* Layer description. Device arrays must stay valid until trellis_moe_destroy. */
@@ -93,12 +95,27 @@ typedef struct {
   const int16_t* fc2_payload;
   const uint16_t* fc1_scale;  /* fp16 [E, 2I] per-output-channel scale */
   const uint16_t* fc2_scale;  /* fp16 [E, H] */
-  const uint16_t* in_suh;     /* fp16 [H] input signs (shared by gate and up) */
+  const uint16_t* in_suh;     /* fp16 [H] input signs (shared by gate and up; see gate_suh) */
   const uint16_t* rot_tab;    /* fp16 [E, 3I] = gate svh | up svh | down suh */
   const uint16_t* out_svh;    /* fp16 [E, H] output (down) svh */
   int32_t max_tokens;         /* largest T any forward call will pass, >= 1 */
-  int32_t decode_max_rows;    /* AUTO picks W4A8 iff T <= this (default 8) */
-  int32_t deterministic;      /* 1: fixed-order FP32 combine; 0: FP32 atomics */
+  int32_t decode_max_rows;    /* AUTO picks W4A8 iff T <= this (default 8) and T*topk <= 1024 */
+  int32_t deterministic;      /* 1: fixed-order FP32 combine; 0: FP32 atomics on the
+                                 tensor-core path. The decode-rows path (W4A8, and W4A16
+                                 at T*topk < 4E) sums every token's routes in fixed order
+                                 in either setting, so there 0 gives the deterministic
+                                 result. */
+  /* Optional separate input signs of the FC1 gate rows and of the up rows
+   * (b12x PR #129 "feat(moe): serve canonical Fruit QSRT atoms", review of
+   * trellis_w4a8.py: gate_suh and up_suh of shape (1, H) or (num_experts, H)).
+   * Both NULL: every route's gate and up rows see x~ = H_b(in_suh * x). Both
+   * set: fp16 [input_sign_rows, H] each, input_sign_rows 1 (shared by the
+   * experts) or E (row e for expert e); the gate rows of a route to expert e
+   * see H_b(gate_suh[e] * x) and its up rows H_b(up_suh[e] * x), and in_suh is
+   * not read (may be NULL). Tensor-core route blocks are then 128 routes. */
+  const uint16_t* gate_suh;
+  const uint16_t* up_suh;
+  int32_t input_sign_rows;
 } tm_layer_desc;
 
 /* Validate `desc`, upload the per-expert offset tables and return a handle and
@@ -120,7 +137,8 @@ size_t trellis_moe_workspace_size(const tm_layer* layer, int32_t max_tokens);
  *   out      fp32 [T, H] result (overwritten; 16-byte aligned)
  *   workspace >= trellis_moe_workspace_size(layer, T) bytes, 256-byte aligned;
  *            contents on entry are ignored (any bytes give the same result).
- * T = 0 is a no-op. Errors: TM_EINVAL, TM_EWORKSPACE, TM_ECUDA. */
+ * T = 0 is a no-op. Errors: TM_EINVAL, TM_EWORKSPACE, TM_ECUDA, and
+ * TM_EUNSUPPORTED for mode W4A8 with T*topk > 1024. */
 tm_status trellis_moe_forward(tm_layer* layer, const uint16_t* x, const int32_t* topk_ids,
                               const float* topk_w, int32_t T, int32_t mode, float* out,
                               void* workspace, size_t workspace_bytes, void* stream);
@@ -170,7 +188,10 @@ tm_status trellis_moe_route_map(tm_layer* layer, const int32_t* topk_ids, int32_
                                 void* stream);
 
 /* Step 3 alone: x bf16 [T, H] -> W4A16: fp16 [T, H] into xq; W4A8: E4M3 bytes
- * [T, H] into xq and E8M0 bytes [T, H/32] into xs (xs unused for W4A16). */
+ * [T, H] into xq and E8M0 bytes [T, H/32] into xs (xs unused for W4A16), with
+ * the layer's shared in_suh (TM_EUNSUPPORTED for a layer with separate gate /
+ * up signs). W4A8 rotates in fp64 and rounds each value once to fp32 before
+ * quantising. */
 tm_status trellis_moe_rotate_quant(tm_layer* layer, const uint16_t* x, int32_t T, int32_t mode,
                                    void* xq, uint8_t* xs, void* stream);
 
@@ -183,10 +204,9 @@ tm_status trellis_moe_decode_tiles(tm_layer* layer, int32_t proj, int32_t expert
 
 /* Where a forward call of `T` tokens keeps its intermediates inside the
  * workspace (for tests): which = 0 x~, 1 x~ E8M0 exponents, 2 FC1 epilogue
- * output z~, 3 z~ E8M0 exponents (x~ and z~: fp16 for W4A16; for W4A8 the
- * E4M3 codes on the mma.sync path, the codes held as fp16 on the decode-rows
- * path, the dequantized values as fp16 in slot order on the tensor-core
- * path), 4 per-slot
+ * output z~, 3 z~ E8M0 exponents (x~ and z~: fp16 for W4A16, in slot order on
+ * the tensor-core path; for W4A8, which runs on the decode rows, the E4M3
+ * codes held as fp16), 4 per-slot
  * FC2 output (fp32 [slots, H]: the unrotated route output, or, for the
  * tensor-core FC2 with the deterministic combine, the scaled FC2 accumulator
  * after the Hadamard levels within each 64-column half; not written by the
@@ -210,7 +230,8 @@ tm_status trellis_moe_workspace_region(const tm_layer* layer, int32_t T, int32_t
  * caller keeps ownership. */
 tm_status trellis_moe_set_stage_events(tm_layer* layer, void* const* events, int32_t n);
 
-/* How the decode-rows path (T*topk <= 1024 and < 4E routes) expands trellis
+/* How the decode-rows path (T*topk <= 1024: every W4A8 call, and W4A16 calls
+ * with fewer than 4E routes) expands trellis
  * states into weights. on = 0 (the default): by the codebook hash in
  * registers (several CTAs per SM); on = 1: by lookup in a table of the
  * codebook value of every 16-bit state (65,536 fp16 entries; in W4A8 mode the
@@ -225,26 +246,42 @@ tm_status trellis_moe_set_stage_events(tm_layer* layer, void* const* events, int
  * host-call graphs. Errors: TM_EINVAL. */
 tm_status trellis_moe_set_decode_lut(tm_layer* layer, int32_t on);
 
+/* Test hook for the tensor-core kernels' bounded waits (the failure detection
+ * of a stalled pipeline). Every mbarrier wait of those kernels gives up after
+ * wait_limit_ns of wall time (0 restores the default of 2 s); the CTA then
+ * sets bit 1 of the error word, lets the copies it has in flight land, frees
+ * its tensor memory and returns, leaving the call's output incomplete. With
+ * stall_issuer = 1 the MMA issuer first waits on a barrier that nothing
+ * arrives on, before it issues any MMA, so that wait runs out on every CTA:
+ * a test then sees the error bit from trellis_moe_poll_error and checks that
+ * the next call with stall_issuer = 0 is correct. Applies to later forward
+ * calls on tensor-core shapes (the decode-rows kernels do not wait on one
+ * another). Drops the handle's captured host-call graphs. Errors: TM_EINVAL. */
+tm_status trellis_moe_set_wait_test(tm_layer* layer, uint64_t wait_limit_ns, int32_t stall_issuer);
+
 /* Read and clear the device error word of `workspace` (synchronises `stream`).
- * *flags: bit 0 = an expert id was out of range. Returns TM_EDEVICE if any flag
- * was set, else TM_OK. */
+ * *flags: bit 0 = an expert id was out of range; bit 1 = a tensor-core
+ * kernel's pipeline wait gave up (the kernel stopped, released its tensor
+ * memory and left its outputs incomplete). Returns TM_EDEVICE if any flag was
+ * set, else TM_OK. */
 tm_status trellis_moe_poll_error(tm_layer* layer, void* workspace, uint32_t* flags, void* stream);
 
 /* Route map with no scratch from the caller and no allocation. No counterpart
  * on the source pages: it exists for callers that cannot allocate or lend
- * device memory -- code running while a CUDA graph is being captured (where
- * cudaMalloc is not allowed), hosts that own all device memory through a fixed
- * plan and pass only inputs and outputs, and latency-critical loops that must
- * not enter the allocator after start-up because allocation can synchronise
- * the device. Same arguments and results as trellis_moe_route_map, with the
+ * device memory -- hosts that own all device memory through a fixed plan and
+ * pass only inputs and outputs, and latency-critical loops that must not
+ * enter the allocator after start-up because allocation can synchronise the
+ * device. Same arguments and results as trellis_moe_route_map, with the
  * layer's E and topk passed directly. Its scratch is one static device array
  * of about 10 KB per GPU, held while the library is loaded; limits:
  * T*topk <= 1024 routes, E <= 256 (TM_EUNSUPPORTED beyond, with a message).
  * The first call on a device looks up that array's device address, so make it
- * before any stream capture. All calls on a device share the array: calls
- * whose kernels overlap on the GPU race, so order them on one stream. Every
- * call clears what must start at zero. Dropped (out-of-range) ids get
- * slot_of_route -1 as in trellis_moe_route_map; no error word is kept. */
+ * before any stream capture; the address is kept for the process's lifetime,
+ * so a device reset (cudaDeviceReset) while the library is loaded is not
+ * supported. All calls on a device share the array: calls whose kernels
+ * overlap on the GPU race, so order them on one stream. Every call clears what
+ * must start at zero. Dropped (out-of-range) ids get slot_of_route -1 as in
+ * trellis_moe_route_map; no error word is kept. */
 tm_status trellis_moe_route_map_static(const int32_t* topk_ids, int32_t T, int32_t E, int32_t topk,
                                        int32_t block, int32_t* counts, int32_t* offsets,
                                        int32_t* route_of_slot, int32_t* slot_of_route, void* stream);

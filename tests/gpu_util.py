@@ -52,3 +52,25 @@ def run_and_compare(moe, L, cfg, T, mode, tokens=None, seed=None):
     sel = np.arange(T) if tokens is None else np.asarray(tokens)
     ref = olayer.layer_forward(L, x_bits, ids, w.astype(np.float32), mode=mode, tokens=sel)
     return rel_row_err(y[sel], ref), y, ref
+
+
+def block_cover_tokens(ids, E, block=256, extra=()):
+    """Tokens whose routes cover every route block of every expert in a route
+    map of `block` slots: per block, the routes at its first slot, at the
+    slots either side of the 128-route accumulator split (127, 128) and at
+    its last valid slot, so every multi-block expert, both accumulators of a
+    block and each block's ragged tail are checked. `extra` tokens are added."""
+    ids = np.asarray(ids)
+    k = ids.shape[1]
+    rm = oroute.route_map(ids, E, block)
+    ros = np.asarray(rm["route_of_slot"])
+    off = np.asarray(rm["offsets"])
+    counts = np.asarray(rm["counts"])
+    toks = set(int(t) for t in extra)
+    for e in range(E):
+        n = int(counts[e])
+        for b0 in range(0, n, block):
+            last = min(n, b0 + block) - 1
+            for s in {b0, min(b0 + 127, last), min(b0 + 128, last), last}:
+                toks.add(int(ros[off[e] + s]) // k)
+    return np.asarray(sorted(toks), dtype=np.int64)

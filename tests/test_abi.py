@@ -60,6 +60,16 @@ def test_host_validation_without_gpu(lib):
     d.bits_per_expert = ctypes.cast(bits, ctypes.c_void_p)
     assert lib.trellis_moe_prepare(ctypes.byref(d), ctypes.byref(h), None) == -1   # NULL payload
     assert b"fc1_payload" in lib.trellis_moe_last_error()
+    # separate gate / up input signs: both or neither, 1 or E rows
+    d.gate_suh = 4096
+    assert lib.trellis_moe_prepare(ctypes.byref(d), ctypes.byref(h), None) == -1
+    assert b"together" in lib.trellis_moe_last_error()
+    d.up_suh, d.input_sign_rows = 8192, 3
+    assert lib.trellis_moe_prepare(ctypes.byref(d), ctypes.byref(h), None) == -1
+    assert b"input_sign_rows" in lib.trellis_moe_last_error()
+    d.gate_suh = d.up_suh = None
+    d.input_sign_rows = 0
+    assert lib.trellis_moe_set_wait_test(None, 1000, 1) == -1
     # forward on a NULL handle
     assert lib.trellis_moe_forward(None, P(8), P(8), P(8), 1, 0, P(8), P(256), 1 << 20, None) == -1
     assert lib.trellis_moe_set_stage_events(None, None, 0) == -1

@@ -3,7 +3,8 @@ import numpy as np
 import pytest
 
 from oracle import hadamard, layer as olayer, mxfp8, route as oroute, trellis
-from tests.gpu_util import TOL, oracle_routes, rel_row_err, run_and_compare, small_cfg, upload_tokens
+from tests.gpu_util import (TOL, block_cover_tokens, oracle_routes, rel_row_err, run_and_compare, small_cfg,
+                            upload_tokens)
 from trellis_quantized_moe_route_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -154,14 +155,9 @@ def test_rotate_quant_mxfp8(rot):
     codes, e8 = xq.cpu().numpy(), xs.cpu().numpy()
     ref = olayer.rotate_input(L, x_bits)
     rc, re8, rdeq = mxfp8.quantize_mxfp8(ref.astype(np.float32))
-    if rot == 1:
-        assert np.array_equal(codes, rc) and np.array_equal(e8, re8)
-    else:
-        assert (codes == rc).mean() > 0.995 and (e8 == re8).mean() > 0.99
-        deq = mxfp8.e4m3_decode(codes) * np.exp2(np.repeat(e8.astype(np.float64) - 127, 32, axis=1))
-        scale = np.exp2(np.repeat(re8.astype(np.float64) - 127, 32, axis=1))
-        # half an E4M3 ulp at the top of the range is 16 (in units of the block scale)
-        assert np.all(np.abs(deq - ref) <= scale * 32.0)
+    # the W4A8 rotation runs in fp64 and rounds once to fp32, as the oracle's
+    # float64 rotation does: the codes and exponents agree exactly
+    assert np.array_equal(codes, rc) and np.array_equal(e8, re8)
 
 
 # ---------------------------------------------------------------- layer ----
@@ -330,13 +326,6 @@ def test_host_validation_errors():
 
 
 # ----------------------------------------------- the five workloads, full size ---
-def _sample(T, n, seed):
-    if T <= n:
-        return np.arange(T)
-    s = synth.Stream(seed, 77)
-    return np.unique(np.concatenate([[0, T - 1], s.below(n - 2, T)]))
-
-
 @pytest.mark.parametrize("T", [1, 2, 4, 8])
 def test_decode_config_full(T):
     cfg = synth.CONFIGS["decode"]
@@ -346,19 +335,29 @@ def test_decode_config_full(T):
     assert err < TOL["w4a8"], err
 
 
-def test_prefill_config_full_sampled():
+def _cover(cfg, T, seed=None, extra=(0,)):
+    """The workload's tokens that cover every (expert, 256-route block) of the
+    tensor-core path, from the oracle's own router and route map."""
+    _, logits = synth.make_tokens(cfg, T=T, seed=seed)
+    ids, _ = oracle_routes(logits, cfg.topk)
+    return block_cover_tokens(ids, cfg.E, 256, extra=tuple(extra) + (T - 1,))
+
+
+def test_prefill_config_full_covering_blocks():
     cfg = synth.CONFIGS["prefill"]
     L = synth.make_layer(cfg)
     moe = _moe(L, cfg.T)
-    err, _, _ = run_and_compare(moe, L, cfg, cfg.T, "w4a16", tokens=_sample(cfg.T, 8, 1))
+    sel = _cover(cfg, cfg.T)
+    assert len(sel) > 150
+    err, _, _ = run_and_compare(moe, L, cfg, cfg.T, "w4a16", tokens=sel)
     assert err < TOL["w4a16"], err
 
 
-def test_odd_config_full_sampled():
+def test_odd_config_full_covering_blocks():
     cfg = synth.CONFIGS["odd"]
     L = synth.make_layer(cfg)
     moe = _moe(L, cfg.T)
-    err, _, _ = run_and_compare(moe, L, cfg, cfg.T, "w4a16", tokens=_sample(cfg.T, 8, 2))
+    err, _, _ = run_and_compare(moe, L, cfg, cfg.T, "w4a16", tokens=_cover(cfg, cfg.T))
     assert err < TOL["w4a16"], err
 
 
@@ -370,16 +369,18 @@ def test_large_config_decode_full():
     assert err < TOL["w4a8"], err
 
 
-def test_large_config_prefill_sampled():
+def test_large_config_prefill_covering_blocks():
     cfg = synth.CONFIGS["large"]
     L = synth.make_layer(cfg)
     moe = _moe(L, cfg.T)
-    err, _, _ = run_and_compare(moe, L, cfg, cfg.T, "w4a16", tokens=_sample(cfg.T, 3, 3))
+    sel = _cover(cfg, cfg.T)
+    assert len(sel) > 160
+    err, _, _ = run_and_compare(moe, L, cfg, cfg.T, "w4a16", tokens=sel)
     assert err < TOL["w4a16"], err
 
 
 # ------------------------------------- decode-rows path (T*topk small) ---
-# These shapes keep T*topk below 4*E, which selects the split-K decode kernels.
+# These shapes keep T*topk below 4*E, where both modes take the decode-rows kernels.
 DECODE_SHAPES = [
     dict(T=4, E=16, topk=2, bits=(2, 3, 4), I=320, rot_block_i=64, H=512),   # mixed K, 64-wide I blocks
     dict(T=3, E=32, topk=4),                                                 # K=4, rotation blocks 128
@@ -447,6 +448,43 @@ def test_decode_path_w4a8_block_exponent_ranges(scales):
     torch.cuda.synchronize()
     ref = olayer.layer_forward(L, x_bits, ids, w.astype(np.float32), mode="w4a8")
     assert rel_row_err(out.cpu().numpy(), ref) < TOL["w4a8"]
+
+
+@pytest.mark.parametrize("pattern", [(0, -24, 16, 0), (-24,), (16,)])
+def test_w4a8_many_routes_per_expert_block_exponent_ranges(pattern):
+    """Explicit W4A8 with T*topk >= 4E (16 routes per expert): W4A8 runs on
+    the decode rows at every T*topk <= 1024. Tokens scaled by 2^-24 and 2^16
+    push the block exponents of x~ and of z~ (which scales with the square
+    of the input) outside [-15, 7], alone or mixed with ordinary tokens."""
+    cfg = small_cfg(T=64, E=8, topk=2, H=256, I=128)
+    assert cfg.T * cfg.topk >= 4 * cfg.E
+    L = synth.make_layer(cfg)
+    moe = _moe(L, cfg.T)
+    x_bits, logits = synth.make_tokens(cfg)
+    x_bits = np.stack([_scale_bf16(x_bits[t], pattern[t % len(pattern)]) for t in range(cfg.T)])
+    ids, w = oracle_routes(logits, cfg.topk)
+    x, lg = upload_tokens(x_bits, logits)
+    out = moe.forward_logits(x, lg, mode="w4a8")
+    torch.cuda.synchronize()
+    assert np.all(np.isfinite(out.cpu().numpy()))
+    ref = olayer.layer_forward(L, x_bits, ids, w.astype(np.float32), mode="w4a8")
+    assert rel_row_err(out.cpu().numpy(), ref) < TOL["w4a8"]
+
+
+def test_w4a8_beyond_decode_rows_is_refused_and_auto_runs_w4a16():
+    from trellis_quantized_moe_route_gb300.binding import TrellisMoEError
+    cfg = small_cfg(T=300, E=8, topk=4, H=256, I=128)
+    L = synth.make_layer(cfg)
+    moe = _moe(L, cfg.T, decode_max_rows=cfg.T)
+    x_bits, logits = synth.make_tokens(cfg)
+    x, lg = upload_tokens(x_bits, logits)
+    with pytest.raises(TrellisMoEError) as ei:
+        moe.forward_logits(x, lg, mode="w4a8")   # 1200 routes > 1024
+    assert ei.value.status == -2
+    auto = moe.forward_logits(x, lg, mode="auto").cpu()
+    assert torch.equal(auto, moe.forward_logits(x, lg, mode="w4a16").cpu())
+    small = moe.forward_logits(x[:256], lg[:256], mode="auto").cpu()   # 1024 routes: W4A8
+    assert torch.equal(small, moe.forward_logits(x[:256], lg[:256], mode="w4a8").cpu())
 
 
 def test_decode_path_deterministic_poisoned_and_atomic():

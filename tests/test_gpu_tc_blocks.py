@@ -1,8 +1,9 @@
-"""The tensor-core contraction's route-block boundaries against the oracle:
-experts whose route counts sit on both sides of the one / two accumulator
-switch (128 / 129 routes) and of the 256-route block (256 / 257), so that
-blocks of one, two and several accumulators and multi-block experts all
-occur, in both modes."""
+"""Route-block boundaries against the oracle: experts whose route counts sit
+on both sides of the tensor-core kernels' one / two accumulator switch
+(128 / 129 routes) and of their 256-route block (256 / 257), so that blocks
+of one, two and several accumulators and multi-block experts all occur
+(W4A16). The same layer in W4A8 (872 routes) runs on the decode rows, whose
+8-slot route blocks then hold many blocks per expert."""
 import numpy as np
 import pytest
 

@@ -77,12 +77,3 @@ def test_streaming_form_equals_dense_matrices_per_expert(rows):
             y = np.diag(f16(L.out_svh[e])) @ HH @ np.diag(s2) @ w2 @ z
             out[t] += w[t, j] * y
     assert np.max(np.abs(got - out)) <= 1e-12 * np.max(np.abs(out))
-
-
-def test_cuda_binding_refuses_separate_signs():
-    """The CUDA path takes one shared input sign vector; a layer with separate
-    gate / up signs must be refused, not run with in_suh."""
-    from trellis_quantized_moe_route_gb300.binding import TrellisMoE
-    L = synth.with_input_signs(synth.make_layer(_cfg()), 1)
-    with pytest.raises(NotImplementedError):
-        TrellisMoE(L, max_tokens=4)

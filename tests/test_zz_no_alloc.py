@@ -1,9 +1,9 @@
 """The allocation-free route map against the workspace-based one (needs a GPU).
 
 trellis_moe_route_map_static serves callers that cannot allocate device memory
-or lend the library a workspace -- code running inside a CUDA graph capture,
-hosts that hand the library only inputs and outputs from their own fixed
-memory plan, and loops that must stay out of the allocator after start-up.
+or lend the library a workspace -- hosts that hand the library only inputs and
+outputs from their own fixed memory plan, and loops that must stay out of the
+allocator after start-up.
 It keeps its scratch in a static device array, so its results must equal
 those of trellis_moe_route_map (integer work: bit for bit) on every call,
 including a second call that finds the first call's leftovers in that array.

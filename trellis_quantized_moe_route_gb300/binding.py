@@ -30,7 +30,7 @@ EXPORTED = [
     "trellis_moe_forward_logits", "trellis_moe_forward_host", "trellis_moe_route",
     "trellis_moe_route_map", "trellis_moe_rotate_quant", "trellis_moe_decode_tiles",
     "trellis_moe_workspace_region", "trellis_moe_set_stage_events", "trellis_moe_set_decode_lut",
-    "trellis_moe_poll_error",
+    "trellis_moe_poll_error", "trellis_moe_set_wait_test",
     "trellis_moe_last_error", "trellis_moe_destroy", "trellis_moe_route_map_static",
     "trellis_linear_prepare", "trellis_linear_workspace_size", "trellis_linear_forward",
     "trellis_linear_poll_error", "trellis_linear_destroy",
@@ -46,6 +46,7 @@ class LayerDesc(ctypes.Structure):
         ("fc1_scale", ctypes.c_void_p), ("fc2_scale", ctypes.c_void_p),
         ("in_suh", ctypes.c_void_p), ("rot_tab", ctypes.c_void_p), ("out_svh", ctypes.c_void_p),
         ("max_tokens", ctypes.c_int32), ("decode_max_rows", ctypes.c_int32), ("deterministic", ctypes.c_int32),
+        ("gate_suh", ctypes.c_void_p), ("up_suh", ctypes.c_void_p), ("input_sign_rows", ctypes.c_int32),
     ]
 
 
@@ -89,6 +90,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "trellis_moe_set_stage_events": (I32, [P, ctypes.POINTER(P), I32]),
         "trellis_moe_set_decode_lut": (I32, [P, I32]),
         "trellis_moe_poll_error": (I32, [P, P, ctypes.POINTER(ctypes.c_uint32), P]),
+        "trellis_moe_set_wait_test": (I32, [P, ctypes.c_uint64, I32]),
         "trellis_moe_last_error": (ctypes.c_char_p, []),
         "trellis_moe_destroy": (None, [P]),
         "trellis_moe_route_map_static": (I32, [P, I32, I32, I32, I32, P, P, P, P, P]),
@@ -167,12 +169,14 @@ def route_map_static(ids, E: int, block: int, stream=None):
     lib = load_library()
     T, k = int(ids.shape[0]), int(ids.shape[1])
     R = T * k
-    counts = torch.empty(E, dtype=torch.int32, device="cuda")
-    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
-    ros = torch.empty(R + E * (block - 1) + 1, dtype=torch.int32, device="cuda")
-    sor = torch.empty(max(R, 1), dtype=torch.int32, device="cuda")
-    _check(lib.trellis_moe_route_map_static(_ptr(ids), T, E, k, block, _ptr(counts), _ptr(offsets), _ptr(ros),
-                                            _ptr(sor), _stream_ptr(stream)))
+    dev = ids.device
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    ros = torch.empty(R + E * (block - 1) + 1, dtype=torch.int32, device=dev)
+    sor = torch.empty(max(R, 1), dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib.trellis_moe_route_map_static(_ptr(ids), T, E, k, block, _ptr(counts), _ptr(offsets), _ptr(ros),
+                                                _ptr(sor), _stream_ptr(stream)))
     return {"counts": counts, "offsets": offsets, "route_of_slot": ros, "slot_of_route": sor[:R]}
 
 
@@ -181,11 +185,10 @@ class TrellisMoE:
     fp16 as uint16 bit patterns); its arrays are uploaded once."""
 
     def __init__(self, layer, max_tokens: int, decode_max_rows: int = 8, deterministic: bool = True):
-        if getattr(layer, "gate_suh", None) is not None or getattr(layer, "up_suh", None) is not None:
-            raise NotImplementedError("separate gate / up input signs are not on the CUDA path: "
-                                      "the layer takes one shared input sign vector (in_suh [H])")
         torch = _torch()
         self.lib = load_library()
+        # the handle, its tables and workspace belong to the device current now
+        self.device = torch.device("cuda", torch.cuda.current_device())
         self.E, self.H, self.I, self.topk = int(layer.E), int(layer.H), int(layer.I), int(layer.topk)
         self.bits = np.ascontiguousarray(np.asarray(layer.bits, dtype=np.uint8))
         self.fc1_payload = to_device_u16(layer.fc1_payload)
@@ -195,6 +198,11 @@ class TrellisMoE:
         self.in_suh = to_device_u16(layer.in_suh)
         self.rot_tab = to_device_u16(layer.rot_tab)
         self.out_svh = to_device_u16(layer.out_svh)
+        g, u = getattr(layer, "gate_suh", None), getattr(layer, "up_suh", None)
+        if (g is None) != (u is None):
+            raise ValueError("gate_suh and up_suh must be given together")
+        self.gate_suh = to_device_u16(np.asarray(g).reshape(-1, self.H)) if g is not None else None
+        self.up_suh = to_device_u16(np.asarray(u).reshape(-1, self.H)) if u is not None else None
         d = LayerDesc()
         d.E, d.H, d.I, d.topk = self.E, self.H, self.I, self.topk
         d.rot_block_h, d.rot_block_i = int(layer.rot_block_h), int(layer.rot_block_i)
@@ -209,6 +217,12 @@ class TrellisMoE:
         d.max_tokens = int(max_tokens)
         d.decode_max_rows = int(decode_max_rows)
         d.deterministic = 1 if deterministic else 0
+        if self.gate_suh is not None:
+            if self.gate_suh.shape != self.up_suh.shape:
+                raise ValueError("gate_suh and up_suh must have the same shape")
+            d.gate_suh = self.gate_suh.data_ptr()
+            d.up_suh = self.up_suh.data_ptr()
+            d.input_sign_rows = int(self.gate_suh.shape[0])
         self.desc = d
         handle = ctypes.c_void_p()
         ws = ctypes.c_size_t()
@@ -216,7 +230,7 @@ class TrellisMoE:
         self.handle = handle
         self.max_tokens = int(max_tokens)
         self.workspace_bytes = int(ws.value)
-        self.workspace = torch.empty(self.workspace_bytes + 256, dtype=torch.uint8, device="cuda")
+        self.workspace = torch.empty(self.workspace_bytes + 256, dtype=torch.uint8, device=self.device)
         off = (-self.workspace.data_ptr()) % 256
         self.workspace = self.workspace[off:off + self.workspace_bytes]
 
@@ -237,7 +251,7 @@ class TrellisMoE:
         torch = _torch()
         T = int(x.shape[0])
         if out is None:
-            out = torch.empty((T, self.H), dtype=torch.float32, device="cuda")
+            out = torch.empty((T, self.H), dtype=torch.float32, device=self.device)
         _check(self.lib.trellis_moe_forward(self.handle, _ptr(x), _ptr(ids), _ptr(w), T, MODES.get(mode, mode),
                                             _ptr(out), _ptr(self.workspace), self.workspace_bytes,
                                             _stream_ptr(stream)))
@@ -247,7 +261,7 @@ class TrellisMoE:
         torch = _torch()
         T = int(x.shape[0])
         if out is None:
-            out = torch.empty((T, self.H), dtype=torch.float32, device="cuda")
+            out = torch.empty((T, self.H), dtype=torch.float32, device=self.device)
         _check(self.lib.trellis_moe_forward_logits(self.handle, _ptr(x), _ptr(logits), T, MODES.get(mode, mode),
                                                    _ptr(out), _ptr(self.workspace), self.workspace_bytes,
                                                    _stream_ptr(stream)))
@@ -271,7 +285,7 @@ class TrellisMoE:
         torch = _torch()
         T = int(ids.shape[0])
         R = T * self.topk
-        dev = "cuda"
+        dev = self.device
         counts = torch.empty(self.E, dtype=torch.int32, device=dev)
         offsets = torch.empty(self.E + 1, dtype=torch.int32, device=dev)
         ros = torch.empty(R + self.E * (block - 1) + 1, dtype=torch.int32, device=dev)
@@ -286,11 +300,11 @@ class TrellisMoE:
         T = int(x.shape[0])
         m = MODES.get(mode, mode)
         if m == MODE_W4A8:
-            xq = torch.empty((T, self.H), dtype=torch.uint8, device="cuda")
-            xs = torch.empty((T, self.H // 32), dtype=torch.uint8, device="cuda")
+            xq = torch.empty((T, self.H), dtype=torch.uint8, device=self.device)
+            xs = torch.empty((T, self.H // 32), dtype=torch.uint8, device=self.device)
         else:
-            xq = torch.empty((T, self.H), dtype=torch.int16, device="cuda")
-            xs = torch.empty(1, dtype=torch.uint8, device="cuda")
+            xq = torch.empty((T, self.H), dtype=torch.int16, device=self.device)
+            xs = torch.empty(1, dtype=torch.uint8, device=self.device)
         _check(self.lib.trellis_moe_rotate_quant(self.handle, _ptr(x), T, m, _ptr(xq), _ptr(xs), _stream_ptr(stream)))
         return xq, (xs if m == MODE_W4A8 else None)
 
@@ -298,7 +312,7 @@ class TrellisMoE:
         torch = _torch()
         m = MODES.get(mode, mode)
         dt = torch.uint8 if m == MODE_W4A8 else torch.int16
-        dst = torch.empty((ntiles, 256), dtype=dt, device="cuda")
+        dst = torch.empty((ntiles, 256), dtype=dt, device=self.device)
         _check(self.lib.trellis_moe_decode_tiles(self.handle, proj, expert, tile0, ntiles, m, _ptr(dst),
                                                  _stream_ptr(stream)))
         return dst
@@ -327,6 +341,11 @@ class TrellisMoE:
                     ev.record()     # torch creates the CUDA event lazily
                 arr[i] = ev.cuda_event
         _check(self.lib.trellis_moe_set_stage_events(self.handle, arr, 7))
+
+    def set_wait_test(self, wait_limit_ns: int = 0, stall_issuer: bool = False):
+        """Limit of the tensor-core kernels' pipeline waits, and the stalled
+        issuer used to test that they give up (see the C header)."""
+        _check(self.lib.trellis_moe_set_wait_test(self.handle, int(wait_limit_ns), 1 if stall_issuer else 0))
 
     def poll_error(self, stream=None) -> int:
         flags = ctypes.c_uint32()

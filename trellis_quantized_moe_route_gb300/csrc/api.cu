@@ -28,6 +28,8 @@ struct tm_layer {
   uint16_t* d_lut;     // codebook tables for the decode-rows lookup variant (fp16 | E4M3 as fp16)
   int use_lut;         // decode rows expand by table lookup (1) or by the hash (0)
   int device;
+  uint64_t wait_ns;    // limit of the tensor-core kernels' pipeline waits (0: their default)
+  int stall_issuer;    // test of the bounded waits (trellis_moe_set_wait_test)
   cudaEvent_t stage_ev[7];  // optional stage-boundary events (NULL = off)
   // Host-buffer calls on mapped page-locked buffers replay a captured graph of
   // the layer once the same buffers come back; one entry per buffer set, least
@@ -86,8 +88,6 @@ void drop_host_graphs(tm_layer* layer) {
 }
 
 constexpr size_t kAlign = 256;
-constexpr int kBnMax = 64;
-constexpr int kBnMin = 8;
 constexpr int kBlockMax = 256;  // largest route block (tcgen05 path): expert segments pad to it
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
@@ -99,18 +99,21 @@ int fc1_bi(const tm_layer_desc& d) {
   return bi;
 }
 
-// Decode-rows path plan: used when T*topk <= 1024 and experts see fewer than
-// 4 routes on average (route blocks of 8).
+// Decode-rows path plan (route blocks of 8). W4A8 always runs here (the pages
+// select W4A8 only for bounded decode rows; T*topk <= 1024); W4A16 does when
+// T*topk <= 1024 and experts see fewer than 4 routes on average.
 struct DecPlan {
   bool use;
   int max_blocks, bi, units1, units2, nseg1, nseg2;
   size_t partial_floats, cnt_ints;
 };
 
-DecPlan dec_plan(const tm_layer_desc& d, int T) {
+constexpr long kDecMaxRoutes = 1024;
+
+DecPlan dec_plan(const tm_layer_desc& d, int T, bool w4a8) {
   DecPlan p{};
   const long R = (long)T * d.topk;
-  p.use = R >= 1 && R <= 1024 && R < 4L * d.E;
+  p.use = R >= 1 && R <= kDecMaxRoutes && (w4a8 || R < 4L * d.E);
   p.bi = fc1_bi(d);
   p.units1 = d.I / p.bi;
   p.units2 = d.H / 128;
@@ -124,10 +127,25 @@ DecPlan dec_plan(const tm_layer_desc& d, int T) {
   return p;
 }
 
+// The precision a call runs in: W4A8 when asked for, or in AUTO mode for
+// T <= decode_max_rows, and only on bounded decode rows (check_rows rejects an
+// explicit W4A8 call beyond them).
+bool uses_w4a8(const tm_layer_desc& d, int T, int mode) {
+  const long R = (long)T * d.topk;
+  return mode == TM_MODE_W4A8 || (mode == TM_MODE_AUTO && T <= d.decode_max_rows && R <= kDecMaxRoutes);
+}
+
+tm_status check_rows(const tm_layer_desc& d, int T, int mode) {
+  const long R = (long)T * d.topk;
+  if (mode == TM_MODE_W4A8 && R > kDecMaxRoutes)
+    return fail(TM_EUNSUPPORTED, "W4A8 runs on bounded decode rows: T*topk=%ld exceeds %ld", R, kDecMaxRoutes);
+  return TM_OK;
+}
+
 // Regions of a workspace sized for T tokens (T*topk routes).
 struct Layout {
   enum {
-    ERR, XQ, XS, ZQ, ZS, ROWS, SLOT_OF_ROUTE,
+    ERR, XQ, XS, ZQ, ZS, ROWS, SLOT_OF_ROUTE, XQ2, XS2,
     IDS, W, RANK, TILE_COUNTS, COUNTS, OFFSETS, BLOCK_EXPERT, NBLOCKS, ROUTE_OF_SLOT,
     HOST_X, HOST_LOGITS, HOST_OUT, DEC_PARTIAL, DEC_CNT, DEC_META, COUNT
   };
@@ -141,10 +159,30 @@ Layout make_layout(const tm_layer_desc& d, int T) {
   const size_t R = (size_t)T * d.topk;
   const size_t slots = R + (size_t)d.E * (kBlockMax - 1);
   const size_t ntiles = (R + 1023) / 1024;
-  L.bytes[Layout::XQ] = slots * d.H * 2;  // fp16 in slot order (tcgen05 path), else [T][H] fp16 or E4M3
-  L.bytes[Layout::XS] = (size_t)T * (d.H / 32);
-  L.bytes[Layout::ZQ] = slots * d.I * 2;
-  L.bytes[Layout::ZS] = slots * (d.I / 32);
+  // The decode path's scratch is not monotonic in T (larger T switches to the
+  // general path), so size it for the worst T' <= T: a workspace that fits T
+  // then fits every smaller call too. Its x~ region holds the codes and the
+  // pre-multiplied copy (2T rows), its z~ region both for every route-block
+  // slot (2 * 8 * max_blocks rows).
+  size_t dec_partial = 0, dec_cnt = 0, dec_blocks = 0, dec_x_rows = 0, dec_z_rows = 0;
+  for (int t = 1; t <= T && (long)t * d.topk <= kDecMaxRoutes; ++t) {
+    const DecPlan dp = dec_plan(d, t, true);
+    dec_partial = std::max(dec_partial, dp.partial_floats);
+    dec_cnt = std::max(dec_cnt, dp.cnt_ints);
+    dec_blocks = std::max(dec_blocks, (size_t)dp.max_blocks);
+    dec_x_rows = std::max(dec_x_rows, (size_t)2 * t);
+    dec_z_rows = std::max(dec_z_rows, (size_t)2 * tmoe::kDecBlock * dp.max_blocks);
+  }
+  // With separate gate / up input signs the decode rows keep x~ per route (R
+  // rows of codes + R pre-multiplied rows), the up operand in XQ2 / XS2.
+  const bool split = d.gate_suh != nullptr;
+  if (split) dec_x_rows = std::max(dec_x_rows, 2 * std::min<size_t>(R, kDecMaxRoutes));
+  L.bytes[Layout::XQ] = std::max(slots, dec_x_rows) * d.H * 2;  // fp16 in slot order (tcgen05 path), else [T][H]
+  L.bytes[Layout::XS] = (split ? std::max<size_t>(T, R) : (size_t)T) * (d.H / 32);
+  L.bytes[Layout::XQ2] = split ? L.bytes[Layout::XQ] : 0;
+  L.bytes[Layout::XS2] = split ? L.bytes[Layout::XS] : 0;
+  L.bytes[Layout::ZQ] = std::max(slots, dec_z_rows) * d.I * 2;
+  L.bytes[Layout::ZS] = std::max(slots, dec_z_rows / 2) * (d.I / 32);
   L.bytes[Layout::ROWS] = slots * d.H * 4;
   L.bytes[Layout::SLOT_OF_ROUTE] = R * 4;
   L.bytes[Layout::ERR] = 16;  // error word, then the tcgen05 kernels' unit counters
@@ -154,22 +192,12 @@ Layout make_layout(const tm_layer_desc& d, int T) {
   L.bytes[Layout::TILE_COUNTS] = ntiles * d.E * 4;
   L.bytes[Layout::COUNTS] = (size_t)d.E * 4;
   L.bytes[Layout::OFFSETS] = ((size_t)d.E + 1) * 4;
-  L.bytes[Layout::BLOCK_EXPERT] = (slots / kBnMin + 1) * 4;
+  L.bytes[Layout::BLOCK_EXPERT] = (slots / tmoe::kDecBlock + 1) * 4;
   L.bytes[Layout::NBLOCKS] = 4;
   L.bytes[Layout::ROUTE_OF_SLOT] = slots * 4;
   L.bytes[Layout::HOST_X] = (size_t)T * d.H * 2;
   L.bytes[Layout::HOST_LOGITS] = (size_t)T * d.E * 4;
   L.bytes[Layout::HOST_OUT] = (size_t)T * d.H * 4;
-  // The decode path's scratch is not monotonic in T (larger T switches to the
-  // general path), so size it for the worst T' <= T: a workspace that fits T
-  // then fits every smaller call too.
-  size_t dec_partial = 0, dec_cnt = 0, dec_blocks = 0;
-  for (int t = 1; t <= T && (long)t * d.topk <= 1024; ++t) {
-    const DecPlan dp = dec_plan(d, t);
-    dec_partial = std::max(dec_partial, dp.partial_floats);
-    dec_cnt = std::max(dec_cnt, dp.cnt_ints);
-    if (dp.use) dec_blocks = std::max(dec_blocks, (size_t)dp.max_blocks);
-  }
   L.bytes[Layout::DEC_PARTIAL] = dec_partial * 4;
   L.bytes[Layout::DEC_CNT] = dec_cnt * 4;
   L.bytes[Layout::DEC_META] = dec_blocks * (8 + 8 + 8);  // int64 FC1 and FC2 offsets, then int32 metadata
@@ -199,11 +227,6 @@ tm_status check_ws(const tm_layer* layer, int T, void* ws, size_t bytes, Layout*
   return TM_OK;
 }
 
-int choose_bn(const tm_layer_desc& d, int T) {
-  const long R = (long)T * d.topk;
-  return (R < 4L * d.E) ? kBnMin : kBnMax;
-}
-
 tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids, const float* w,
                           const float* logits, int T, bool w4a8, float* out, void* ws, const Layout& L,
                           const DecPlan& dp, cudaStream_t st);
@@ -213,19 +236,19 @@ tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids
 tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, const float* w, const float* logits,
                     int T, int mode, float* out, void* ws, const Layout& L, cudaStream_t st) {
   const tm_layer_desc& d = layer->desc;
-  const bool w4a8 = (mode == TM_MODE_W4A8) || (mode == TM_MODE_AUTO && T <= d.decode_max_rows);
+  const bool w4a8 = uses_w4a8(d, T, mode);
   const int R = T * d.topk;
-  // Outside the decode regime FC1 and FC2 run on the tcgen05 kernels (route
-  // blocks of up to 256 routes); the mma.sync kernels cover other geometries.
-  const bool use_tc = tmoe::tc_supported(d.H, d.I, layer->bi, d.rot_block_h, d.rot_block_i);
-  const int bn = use_tc ? tmoe::tc_route_block() : choose_bn(d, T);
+  // Outside the decode regime FC1 and FC2 run on the tcgen05 kernels (W4A16,
+  // route blocks of up to 256 routes).
+  const bool split = d.gate_suh != nullptr;  // separate gate / up input signs
+  const int bn = split ? 128 : tmoe::tc_route_block();
   cudaError_t e;
   uint32_t* err = at<uint32_t>(ws, L, Layout::ERR);
   if (logits) {
     ids = at<int32_t>(ws, L, Layout::IDS);
     w = at<float>(ws, L, Layout::W);
   }
-  const DecPlan dp = dec_plan(d, T);
+  const DecPlan dp = dec_plan(d, T, w4a8);
   // (the decode prologue clears the error word itself)
   if (dp.use) return run_decode_path(layer, x, ids, w, logits, T, w4a8, out, ws, L, dp, st);
   if ((e = cudaMemsetAsync(err, 0, 16, st)) != cudaSuccess) return cuda_fail(e, "clear error word");
@@ -255,9 +278,26 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
   void* xq = at<void>(ws, L, Layout::XQ);
   uint8_t* xs = at<uint8_t>(ws, L, Layout::XS);
   // the tcgen05 path reads x~ in slot order (one copy per route)
-  if ((e = tmoe::launch_rotate_quant(x, d.in_suh, T, d.H, d.rot_block_h, w4a8, xq, xs, st,
-                                     use_tc ? rm.slot_of_route : nullptr, d.topk)) != cudaSuccess)
-    return cuda_fail(e, "rotate+quantize");
+  if (split) {
+    tmoe::RouteRotArgs rr{};
+    rr.x = x;
+    rr.gsuh = d.gate_suh;
+    rr.usuh = d.up_suh;
+    rr.sign_rows = d.input_sign_rows;
+    rr.ids = ids;
+    rr.slot_of_route = rm.slot_of_route;
+    rr.T = T;
+    rr.H = d.H;
+    rr.E = d.E;
+    rr.topk = d.topk;
+    rr.rot_b = d.rot_block_h;
+    rr.out_g = static_cast<uint16_t*>(xq);
+    rr.out_u = at<uint16_t>(ws, L, Layout::XQ2);
+    e = tmoe::launch_rotate_routes(rr, false, st);
+  } else {
+    e = tmoe::launch_rotate_quant(x, d.in_suh, T, d.H, d.rot_block_h, false, xq, xs, st, rm.slot_of_route, d.topk);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "rotate+quantize");
   if ((e = stage_mark(layer, 3, st)) != cudaSuccess) return cuda_fail(e, "stage event");
 
   const int max_blocks = R / bn + std::min(d.E, R) + 1;
@@ -282,11 +322,11 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
   t1.err = err;
   t1.sched = err + 1;
   t1.act_rows = (int)(R + (size_t)d.E * (kBlockMax - 1));  // slots
-  if (use_tc)
-    e = tmoe::launch_tc_fc(t1, 1, layer->uniform_k, w4a8, max_blocks, st);
-  else
-    e = tmoe::launch_fc1(a1, w4a8, layer->bi, bn, layer->uniform_k, max_blocks, st);
-  if (e != cudaSuccess) return cuda_fail(e, "FC1");
+  t1.wait_ns = layer->wait_ns;
+  t1.stall_issuer = layer->stall_issuer;
+  t1.route_block = bn;
+  t1.act2 = split ? at<void>(ws, L, Layout::XQ2) : nullptr;
+  if ((e = tmoe::launch_tc_fc(t1, 1, layer->uniform_k, max_blocks, st)) != cudaSuccess) return cuda_fail(e, "FC1");
   if ((e = stage_mark(layer, 4, st)) != cudaSuccess) return cuda_fail(e, "stage event");
 
   tmoe::FcArgs a2 = a1;
@@ -302,7 +342,7 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
   a2.route_w = w;
   a2.atomic = d.deterministic ? 0 : 1;
   // the tensor-core FC2 leaves the route's output scale, H and down_svh to the combine
-  a2.raw_rows = (use_tc && !a2.atomic && d.topk <= 32) ? 1 : 0;
+  a2.raw_rows = (!a2.atomic && d.topk <= 32) ? 1 : 0;
   if (a2.atomic) {
     if ((e = cudaMemsetAsync(out, 0, (size_t)T * d.H * 4, st)) != cudaSuccess) return cuda_fail(e, "clear output");
     a2.out_f32 = out;
@@ -315,11 +355,11 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
   t2.err = err;
   t2.sched = err + 2;
   t2.act_rows = (int)(R + (size_t)d.E * (kBlockMax - 1));  // slots
-  if (use_tc)
-    e = tmoe::launch_tc_fc(t2, 2, layer->uniform_k, w4a8, max_blocks, st);
-  else
-    e = tmoe::launch_fc2(a2, w4a8, bn, layer->uniform_k, max_blocks, st);
-  if (e != cudaSuccess) return cuda_fail(e, "FC2");
+  t2.wait_ns = layer->wait_ns;
+  t2.stall_issuer = layer->stall_issuer;
+  t2.route_block = bn;
+  t2.act2 = nullptr;
+  if ((e = tmoe::launch_tc_fc(t2, 2, layer->uniform_k, max_blocks, st)) != cudaSuccess) return cuda_fail(e, "FC2");
   if ((e = stage_mark(layer, 5, st)) != cudaSuccess) return cuda_fail(e, "stage event");
   if (a2.raw_rows) {
     tmoe::CombineUnrotArgs c{a2.out_f32, rm.slot_of_route, rm.block_expert, bn, w, d.out_svh,
@@ -364,7 +404,7 @@ tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids
   pa.rot_b = d.rot_block_h;
   pa.w4a8 = w4a8 ? 1 : 0;
   pa.xq = at<void>(ws, L, Layout::XQ);
-  // W4A8: the pre-multiplied copy of x~ after the codes (the region holds slots >= 2T rows)
+  // W4A8: the pre-multiplied copy of x~ after the codes (make_layout sizes the region for 2T rows)
   pa.xq_scaled = at<uint16_t>(ws, L, Layout::XQ) + (size_t)T * d.H;
   pa.xs = at<uint8_t>(ws, L, Layout::XS);
   pa.zero_i32 = at<int32_t>(ws, L, Layout::DEC_CNT);
@@ -378,6 +418,31 @@ tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids
   pa.blk_off1 = at<long long>(ws, L, Layout::DEC_META);
   pa.blk_off2 = pa.blk_off1 + dp.max_blocks;
   pa.blk_meta = reinterpret_cast<int32_t*>(pa.blk_off2 + dp.max_blocks);
+  // separate gate / up input signs: x~_g and x~_u per route (rows r = t*topk+j),
+  // codes then the pre-multiplied copy (R rows each) in XQ and XQ2
+  const bool split = d.gate_suh != nullptr;
+  pa.split_signs = split ? 1 : 0;
+  if (split) {
+    tmoe::RouteRotArgs& rr = pa.rr;
+    rr.x = x;
+    rr.gsuh = d.gate_suh;
+    rr.usuh = d.up_suh;
+    rr.sign_rows = d.input_sign_rows;
+    rr.ids = logits ? nullptr : ids;
+    rr.logits = logits;
+    rr.slot_of_route = nullptr;
+    rr.T = T;
+    rr.H = d.H;
+    rr.E = d.E;
+    rr.topk = d.topk;
+    rr.rot_b = d.rot_block_h;
+    rr.out_g = at<uint16_t>(ws, L, Layout::XQ);
+    rr.out_u = at<uint16_t>(ws, L, Layout::XQ2);
+    rr.scaled_g = rr.out_g + (size_t)R * d.H;
+    rr.scaled_u = rr.out_u + (size_t)R * d.H;
+    rr.xs_g = at<uint8_t>(ws, L, Layout::XS);
+    rr.xs_u = at<uint8_t>(ws, L, Layout::XS2);
+  }
   if ((e = tmoe::launch_dec_prologue(pa, st)) != cudaSuccess) return cuda_fail(e, "decode prologue");
   for (int i = 1; i <= 3; ++i)
     if ((e = stage_mark(layer, i, st)) != cudaSuccess) return cuda_fail(e, "stage event");
@@ -405,9 +470,13 @@ tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids
   d1.bi = dp.bi;
   d1.partial = at<float>(ws, L, Layout::DEC_PARTIAL);
   d1.ids = pa.rm.ids;
-  d1.act_scaled = pa.xq_scaled;
+  d1.act_scaled = split ? pa.rr.scaled_g : pa.xq_scaled;
+  d1.split = split ? 1 : 0;
+  d1.act2 = split ? pa.rr.out_u : nullptr;
+  d1.act_scaled2 = split ? pa.rr.scaled_u : nullptr;
+  d1.act_scale2 = split ? pa.rr.xs_u : nullptr;
   // z~ rows are slots < max_blocks * 8; the pre-multiplied copy follows them
-  // (the region holds T*topk + 255E >= 2 * max_blocks * 8 rows in this regime)
+  // (make_layout sizes the region for 2 * max_blocks * 8 rows)
   d1.out_act_scaled = at<uint16_t>(ws, L, Layout::ZQ) + (size_t)dp.max_blocks * tmoe::kDecBlock * d.I;
   d1.blk_meta = pa.blk_meta;
   d1.blk_off = pa.blk_off1;
@@ -427,6 +496,10 @@ tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids
     return cuda_fail(e, "FC1 epilogue (decode rows)");
 
   tmoe::DecArgs d2 = d1;
+  d2.split = 0;
+  d2.act2 = nullptr;
+  d2.act_scaled2 = nullptr;
+  d2.act_scale2 = nullptr;
   tmoe::FcArgs& a2 = d2.f;
   a2.rot_b = d.rot_block_h;
   a2.payload = d.fc2_payload;
@@ -458,17 +531,6 @@ tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids
 namespace tmoe {
 void set_last_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
 
-cudaError_t launch_fc1_f16(const FcArgs& a, int bi, int bn, int uniform_k, int max_blocks, cudaStream_t st);
-cudaError_t launch_fc1_e4m3(const FcArgs& a, int bi, int bn, int uniform_k, int max_blocks, cudaStream_t st);
-cudaError_t launch_fc2_f16(const FcArgs& a, int bn, int uniform_k, int max_blocks, cudaStream_t st);
-cudaError_t launch_fc2_e4m3(const FcArgs& a, int bn, int uniform_k, int max_blocks, cudaStream_t st);
-
-cudaError_t launch_fc1(const FcArgs& a, bool w4a8, int bi, int bn, int uniform_k, int max_blocks, cudaStream_t st) {
-  return w4a8 ? launch_fc1_e4m3(a, bi, bn, uniform_k, max_blocks, st) : launch_fc1_f16(a, bi, bn, uniform_k, max_blocks, st);
-}
-cudaError_t launch_fc2(const FcArgs& a, bool w4a8, int bn, int uniform_k, int max_blocks, cudaStream_t st) {
-  return w4a8 ? launch_fc2_e4m3(a, bn, uniform_k, max_blocks, st) : launch_fc2_f16(a, bn, uniform_k, max_blocks, st);
-}
 }  // namespace tmoe
 
 extern "C" {
@@ -491,9 +553,18 @@ tm_status trellis_moe_prepare(const tm_layer_desc* desc, tm_layer** out, size_t*
   if (d.max_tokens < 1) return fail(TM_EINVAL, "max_tokens=%d must be >= 1", d.max_tokens);
   if ((long)d.max_tokens * d.topk > (1L << 24)) return fail(TM_EUNSUPPORTED, "max_tokens*topk too large");
   if (!d.bits_per_expert) return fail(TM_EINVAL, "bits_per_expert is NULL");
-  const void* ptrs[] = {d.fc1_payload, d.fc2_payload, d.fc1_scale, d.fc2_scale, d.in_suh, d.rot_tab, d.out_svh};
-  const char* names[] = {"fc1_payload", "fc2_payload", "fc1_scale", "fc2_scale", "in_suh", "rot_tab", "out_svh"};
-  for (int i = 0; i < 7; ++i) {
+  const bool split = d.gate_suh != nullptr || d.up_suh != nullptr;
+  if (split) {
+    if (!d.gate_suh || !d.up_suh) return fail(TM_EINVAL, "gate_suh and up_suh must be given together");
+    if (d.input_sign_rows != 1 && d.input_sign_rows != d.E)
+      return fail(TM_EINVAL, "input_sign_rows=%d must be 1 or E=%d", d.input_sign_rows, d.E);
+  }
+  // (with separate gate / up signs in_suh is not read and may be NULL)
+  const void* ptrs[] = {d.fc1_payload, d.fc2_payload, d.fc1_scale, d.fc2_scale, split ? d.gate_suh : d.in_suh,
+                        d.rot_tab, d.out_svh, split ? d.up_suh : d.rot_tab};
+  const char* names[] = {"fc1_payload", "fc2_payload", "fc1_scale", "fc2_scale", split ? "gate_suh" : "in_suh",
+                         "rot_tab", "out_svh", "up_suh"};
+  for (int i = 0; i < 8; ++i) {
     if (!ptrs[i]) return fail(TM_EINVAL, "%s is NULL", names[i]);
     if (((uintptr_t)ptrs[i]) % 16 != 0) return fail(TM_EINVAL, "%s must be 16-byte aligned", names[i]);
   }
@@ -517,12 +588,19 @@ tm_status trellis_moe_prepare(const tm_layer_desc* desc, tm_layer** out, size_t*
     o2 += (int64_t)(d.H / 16) * (d.I / 16) * 16 * k;
   }
   L->bi = fc1_bi(d);
+  if (!tmoe::tc_supported(d.H, d.I, L->bi, d.rot_block_h, d.rot_block_i)) {
+    delete L;
+    return fail(TM_EUNSUPPORTED, "geometry H=%d I=%d rot %d/%d not covered by the tensor-core kernels", d.H, d.I,
+                d.rot_block_h, d.rot_block_i);
+  }
   cudaError_t e;
   if ((e = cudaGetDevice(&L->device)) != cudaSuccess) { delete L; return cuda_fail(e, "cudaGetDevice"); }
   L->d_off1 = L->d_off2 = nullptr;
   L->d_bits = nullptr;
   L->d_lut = nullptr;
   L->use_lut = 0;
+  L->wait_ns = 0;
+  L->stall_issuer = 0;
   if ((e = cudaMalloc(&L->d_off1, d.E * 8)) != cudaSuccess ||
       (e = cudaMalloc(&L->d_off2, d.E * 8)) != cudaSuccess ||
       (e = cudaMalloc(&L->d_bits, d.E)) != cudaSuccess ||
@@ -582,6 +660,7 @@ tm_status trellis_moe_forward(tm_layer* layer, const uint16_t* x, const int32_t*
   Layout L;
   tm_status s = check_ws(layer, T, workspace, workspace_bytes, &L);
   if (s != TM_OK) return s;
+  if ((s = check_rows(layer->desc, T, mode)) != TM_OK) return s;
   cudaError_t e;
   if ((e = stage_mark(layer, 0, (cudaStream_t)stream)) != cudaSuccess) return cuda_fail(e, "stage event");
   return run_layer(layer, x, topk_ids, topk_w, nullptr, T, mode, out, workspace, L, (cudaStream_t)stream);
@@ -600,6 +679,7 @@ tm_status trellis_moe_forward_logits(tm_layer* layer, const uint16_t* x, const f
   Layout L;
   tm_status s = check_ws(layer, T, workspace, workspace_bytes, &L);
   if (s != TM_OK) return s;
+  if ((s = check_rows(layer->desc, T, mode)) != TM_OK) return s;
   cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e;
   if ((e = stage_mark(layer, 0, st)) != cudaSuccess) return cuda_fail(e, "stage event");
@@ -719,6 +799,7 @@ tm_status trellis_moe_forward_host(tm_layer* layer, const uint16_t* x_host, cons
   Layout L;
   tm_status s = check_ws(layer, T, workspace, workspace_bytes, &L);
   if (s != TM_OK) return s;
+  if ((s = check_rows(layer->desc, T, mode)) != TM_OK) return s;
   cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e;
   const auto* xd = static_cast<const uint16_t*>(mapped_ptr(x_host));
@@ -759,7 +840,7 @@ tm_status trellis_moe_route_map(tm_layer* layer, const int32_t* topk_ids, int32_
   g_err[0] = 0;
   if (!layer) return fail(TM_EINVAL, "layer is NULL");
   if (T < 0) return fail(TM_EINVAL, "T=%d < 0", T);
-  if (block < 1 || block > kBnMax * 4) return fail(TM_EINVAL, "block=%d outside 1..%d", block, kBnMax * 4);
+  if (block < 1 || block > kBlockMax) return fail(TM_EINVAL, "block=%d outside 1..%d", block, kBlockMax);
   if (T == 0) return TM_OK;
   if (!topk_ids || !counts || !offsets || !route_of_slot || !slot_of_route)
     return fail(TM_EINVAL, "route map arguments must be non-NULL");
@@ -802,6 +883,7 @@ tm_status trellis_moe_rotate_quant(tm_layer* layer, const uint16_t* x, int32_t T
   if (!x || !xq || (mode == TM_MODE_W4A8 && !xs)) return fail(TM_EINVAL, "x, xq (and xs for W4A8) must be non-NULL");
   if (((uintptr_t)x) % 8 || ((uintptr_t)xq) % 8) return fail(TM_EINVAL, "x and xq must be 8-byte aligned");
   const tm_layer_desc& d = layer->desc;
+  if (d.gate_suh) return fail(TM_EUNSUPPORTED, "the layer has separate gate / up input signs (one rotation per route)");
   cudaError_t e = tmoe::launch_rotate_quant(x, d.in_suh, T, d.H, d.rot_block_h, mode == TM_MODE_W4A8, xq, xs,
                                           (cudaStream_t)stream);
   return e == cudaSuccess ? TM_OK : cuda_fail(e, "rotate+quantize");
@@ -872,6 +954,20 @@ tm_status trellis_moe_set_decode_lut(tm_layer* layer, int32_t on) {
   return TM_OK;
 }
 
+tm_status trellis_moe_set_wait_test(tm_layer* layer, uint64_t wait_limit_ns, int32_t stall_issuer) {
+  g_err[0] = 0;
+  if (!layer) return fail(TM_EINVAL, "layer is NULL");
+  if (stall_issuer != 0 && stall_issuer != 1) return fail(TM_EINVAL, "stall_issuer=%d must be 0 or 1", stall_issuer);
+  {
+    // captured host-call graphs hold the old settings: drop them
+    std::lock_guard<std::mutex> lock(layer->graph_mu);
+    drop_host_graphs(layer);
+  }
+  layer->wait_ns = wait_limit_ns;
+  layer->stall_issuer = stall_issuer;
+  return TM_OK;
+}
+
 tm_status trellis_moe_poll_error(tm_layer* layer, void* workspace, uint32_t* flags, void* stream) {
   g_err[0] = 0;
   if (!layer || !workspace || !flags) return fail(TM_EINVAL, "NULL argument");
@@ -883,7 +979,8 @@ tm_status trellis_moe_poll_error(tm_layer* layer, void* workspace, uint32_t* fla
   if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "synchronize");
   if ((e = cudaMemsetAsync(workspace, 0, 4, st)) != cudaSuccess) return cuda_fail(e, "clear error word");
   *flags = h;
-  if (h != 0) return fail(TM_EDEVICE, "device error flags 0x%x (bit 0: expert id out of range)", h);
+  if (h != 0)
+    return fail(TM_EDEVICE, "device error flags 0x%x (bit 0: expert id out of range; bit 1: a pipeline wait gave up)", h);
   return TM_OK;
 }
 

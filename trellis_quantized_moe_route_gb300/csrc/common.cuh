@@ -250,6 +250,45 @@ __device__ __forceinline__ void warp_fwht(float (&v)[PER], int B) {
   }
 }
 
+// The same transform in fp64. The W4A8 input rotation runs in it: the block
+// sums of bf16 x fp16 products are then exact for ordinary data, and their
+// one rounding to fp32 matches a float64 evaluation, so the MXFP8 codes
+// (decided on those fp32 values) do not depend on the butterfly order.
+template <int PER>
+__device__ __forceinline__ void warp_fwht_f64(double (&v)[PER], int B) {
+#pragma unroll
+  for (int h = 1; h < PER; h <<= 1) {
+    if (h < B) {
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        if ((i & h) == 0) {
+          const double a = v[i], b = v[i + h];
+          v[i] = a + b;
+          v[i + h] = a - b;
+        }
+      }
+    }
+  }
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int lh = 1; lh < 32; lh <<= 1) {
+    if (lh * PER < B) {
+      const bool upper = (lane & lh) != 0;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const double o = __shfl_xor_sync(0xFFFFFFFFu, v[i], lh);
+        v[i] = upper ? (o - v[i]) : (v[i] + o);
+      }
+    }
+  }
+}
+
+// 1/sqrt(B) in fp64, as 1 / fp64(sqrt(B)) rounds (0.08838834764831843 for
+// B = 128, the rotation matrix's entries in a float64 evaluation).
+__device__ __forceinline__ double hadamard_scale_f64(int B) {
+  return B == 128 ? 0.08838834764831843 : (B == 64 ? 0.125 : (B == 32 ? 0.17677669529663687 : 1.0));
+}
+
 __device__ __forceinline__ float hadamard_scale(int B) {
   // 1/sqrt(B) rounded to fp32 (B = 128: 0.088388347648...)
   return B == 128 ? 0.08838834764831845f : (B == 64 ? 0.125f : (B == 32 ? 0.17677669529663687f : 1.0f));

@@ -145,10 +145,18 @@ __global__ void __launch_bounds__(1024) k_dec_prologue(const DecPrologueArgs a) 
   const int nrot = gridDim.x - 1;
   const int cta = blockIdx.x - 1;
   const int gw = cta * 32 + warp;
-  if (a.w4a8)
+  if (a.split_signs) {
+    // one gate and one up rotation per route (their rows indexed by route);
+    // with logits the warp selects its token's experts itself, as CTA 0 does
+    if (a.w4a8)
+      rotate_routes_warp<true>(a.rr, gw);
+    else
+      rotate_routes_warp<false>(a.rr, gw);
+  } else if (a.w4a8) {
     rotate_quant_warp<true>(a.x, a.suh, a.T, a.H, a.rot_b, a.xq, a.xs, gw, nullptr, 0, true, a.xq_scaled);
-  else
+  } else {
     rotate_quant_warp<false>(a.x, a.suh, a.T, a.H, a.rot_b, a.xq, a.xs, gw);
+  }
   const long gtid = (long)cta * blockDim.x + tid, gstride = (long)nrot * blockDim.x;
   for (long i = gtid; i < a.n_zero_i32; i += gstride) a.zero_i32[i] = 0;
   for (long i = gtid; i < a.out_n / 4; i += gstride) reinterpret_cast<float4*>(a.out)[i] = make_float4(0.f, 0.f, 0.f, 0.f);

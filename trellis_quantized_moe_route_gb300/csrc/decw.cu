@@ -56,7 +56,7 @@ struct DwRaw {
   long long o;
 };
 struct DwMetaW {
-  int row;  // lane n < 8: activation row of slot n (FC1 token, FC2 slot), -1 if empty
+  int row;  // lane n < 8: activation row of slot n (FC1 token, or route with split signs; FC2 slot), -1 if empty
   int ek;
   long long off;
 };
@@ -73,11 +73,13 @@ __device__ __forceinline__ DwRaw dw_meta_issue(const DecArgs& d, int rb, int lan
 }
 
 template <int PROJ>
-__device__ __forceinline__ DwMetaW dw_meta_final(const DwRaw& r, int rb, int lane, int topk) {
+__device__ __forceinline__ DwMetaW dw_meta_final(const DwRaw& r, int rb, int lane, int topk, int split) {
   DwMetaW m;
   m.ek = __shfl_sync(0xFFFFFFFFu, r.v, kDecBlock);
   m.off = __shfl_sync(0xFFFFFFFFu, r.o, kDecBlock + 1);
-  m.row = (lane < kDecBlock && r.v >= 0) ? ((PROJ == 1) ? r.v / topk : rb * kDecBlock + lane) : -1;
+  // FC1: the token's x~ row (the route's own rows with separate gate / up
+  // signs); FC2: the slot's z~ row
+  m.row = (lane < kDecBlock && r.v >= 0) ? ((PROJ == 1) ? (split ? r.v : r.v / topk) : rb * kDecBlock + lane) : -1;
   return m;
 }
 
@@ -160,6 +162,19 @@ __device__ __forceinline__ void dw_item_meta(DwItem& it, const DwMetaW& m) {
   it.nvalid = m.ek >> 24;
 }
 
+// The item's activation operand: the up rows' own with separate gate / up
+// input signs (FC1 strips at or past row I), else the shared one.
+struct DwAct {
+  const uint16_t* codes;   // fp16 rows (W4A8: the E4M3 codes as fp16)
+  const uint16_t* scaled;  // W4A8: code * 2^e rows
+  const uint8_t* scale;    // W4A8: E8M0 rows
+};
+__device__ __forceinline__ DwAct dw_act(const DecArgs& d, const DwItem& it) {
+  if (d.split && it.strip * 16 >= d.f.I)
+    return {reinterpret_cast<const uint16_t*>(d.act2), d.act_scaled2, d.act_scale2};
+  return {reinterpret_cast<const uint16_t*>(d.f.act), d.act_scaled, d.f.act_scale};
+}
+
 __device__ __forceinline__ const unsigned char* dw_src(const DecArgs& d, const DwMetaW& m, const DwItem& it, int kdim) {
   const int tiles_k = kdim >> 4;
   return reinterpret_cast<const unsigned char*>(d.f.payload) + m.off +
@@ -228,13 +243,14 @@ __device__ __forceinline__ void dw_compute(const DecArgs& d, const DwItem& it, i
   const int col0 = it.sg * kDecSeg;
   // activation fragment source: slot g's row, columns 32 ks + 16 tsel + 8 h
   const int arow = __shfl_sync(0xFFFFFFFFu, row, g);
-  const uint16_t* ap = (PRE ? d.act_scaled : reinterpret_cast<const uint16_t*>(a.act)) + (size_t)(arow < 0 ? 0 : arow) * kdim + col0 +
+  const DwAct src = dw_act(d, it);
+  const uint16_t* ap = (PRE ? src.scaled : src.codes) + (size_t)(arow < 0 ? 0 : arow) * kdim + col0 +
                        16 * tsel + 8 * h;
   // W4A8: E8M0 block exponents of slots 2q and 2q+1 for this segment
   const int r0 = (W4A8 && !PRE) ? __shfl_sync(0xFFFFFFFFu, row, 2 * q) : -1;
   const int r1 = (W4A8 && !PRE) ? __shfl_sync(0xFFFFFFFFu, row, 2 * q + 1) : -1;
-  const uint8_t* sp0 = a.act_scale + (size_t)(r0 < 0 ? 0 : r0) * (kdim >> 5) + (col0 >> 5);
-  const uint8_t* sp1 = a.act_scale + (size_t)(r1 < 0 ? 0 : r1) * (kdim >> 5) + (col0 >> 5);
+  const uint8_t* sp0 = src.scale + (size_t)(r0 < 0 ? 0 : r0) * (kdim >> 5) + (col0 >> 5);
+  const uint8_t* sp1 = src.scale + (size_t)(r1 < 0 ? 0 : r1) * (kdim >> 5) + (col0 >> 5);
   const uint32_t k16 = 0x10000u + (uint32_t)(d.T >> 30);  // 65536, opaque to the compiler
   const uint32_t nk16 = 0u - k16;
   const int swz = 64 * tsel;
@@ -309,7 +325,7 @@ __device__ __forceinline__ uint32_t dw_pre_issue(const DecArgs& d, const DwItem&
   const int nb = it.ncols >> 5;
   uint32_t lo = 127u, hi = 127u;
   if (r >= 0) {
-    const uint8_t* sp = d.f.act_scale + (size_t)r * (kdim >> 5) + it.sg * kDwSteps + b0;
+    const uint8_t* sp = dw_act(d, it).scale + (size_t)r * (kdim >> 5) + it.sg * kDwSteps + b0;
     if (b0 < nb) lo = __ldg(sp);
     if (b0 + 1 < nb) hi = __ldg(sp + 1);
   }
@@ -584,7 +600,7 @@ __global__ void __launch_bounds__(dw_cta_warps(KB, LUT) * 32, LUT ? 1 : (KB > 0 
       raw1 = dw_meta_issue(d, (int)(pn / per_block), lane);
     }
     it = dw_item(d, pc, nstrips, kdim);
-    m = dw_meta_final<PROJ>(raw0, it.rb, lane, a.topk);
+    m = dw_meta_final<PROJ>(raw0, it.rb, lane, a.topk, d.split);
     dw_item_meta(it, m);
     dw_copy_any(KB > 0 ? KB : it.k, ring, dw_src(d, m, it, kdim), it.ncols >> 4, lane);
   }
@@ -595,7 +611,7 @@ __global__ void __launch_bounds__(dw_cta_warps(KB, LUT) * 32, LUT ? 1 : (KB > 0 
   if (W4A8) pre_cur = dw_pre_issue(d, it, m.row, kdim, lane);
   if (has1) {
     nit = dw_item(d, pn, nstrips, kdim);
-    nm = dw_meta_final<PROJ>(raw1, nit.rb, lane, a.topk);
+    nm = dw_meta_final<PROJ>(raw1, nit.rb, lane, a.topk, d.split);
     dw_item_meta(nit, nm);
     if (W4A8) pre_next = dw_pre_issue(d, nit, nm.row, kdim, lane);
     has2 = h < h1;
@@ -637,7 +653,7 @@ __global__ void __launch_bounds__(dw_cta_warps(KB, LUT) * 32, LUT ? 1 : (KB > 0 
     if (has1) {
       pn = pn2;
       nit = dw_item(d, pn, nstrips, kdim);
-      nm = dw_meta_final<PROJ>(raw2, nit.rb, lane, a.topk);
+      nm = dw_meta_final<PROJ>(raw2, nit.rb, lane, a.topk, d.split);
       dw_item_meta(nit, nm);
       if (W4A8) pre_next = dw_pre_issue(d, nit, nm.row, kdim, lane);
       has2 = h < h1;

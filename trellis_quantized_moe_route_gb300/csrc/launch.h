@@ -47,6 +47,28 @@ struct FcArgs {
   int raw_rows;               // FC2 (tensor-core kernel, not atomic): rows leave the last Hadamard level and down_svh to the combine
 };
 
+// Separate gate / up input signs (one row shared by the experts, or one row
+// per expert: b12x PR #129 "feat(moe): serve canonical Fruit QSRT atoms",
+// review of trellis_w4a8.py, gate_suh and up_suh of shape (1, H) or
+// (num_experts, H)). The FC1 gate rows then see x~_g = H_b(gate_suh_e * x) and
+// the up rows x~_u = H_b(up_suh_e * x), one pair per route.
+struct RouteRotArgs {
+  const uint16_t* x;             // bf16 [T, H]
+  const uint16_t* gsuh;          // fp16 [sign_rows, H]
+  const uint16_t* usuh;          // fp16 [sign_rows, H]
+  int sign_rows;                 // 1 or E
+  const int32_t* ids;            // [T * topk] expert ids, or nullptr: select them from `logits`
+  const float* logits;           // [T, E] (when ids == nullptr)
+  const int32_t* slot_of_route;  // row of route r = its slot (tensor-core path), or nullptr: row r (decode rows)
+  int T, H, E, topk, rot_b;
+  uint16_t* out_g;               // x~_g rows [.][H]: fp16 (W4A16) or E4M3 codes as fp16 (W4A8)
+  uint16_t* out_u;
+  uint16_t* scaled_g;            // W4A8: code * 2^e rows
+  uint16_t* scaled_u;
+  uint8_t* xs_g;                 // W4A8: E8M0 [.][H/32]
+  uint8_t* xs_u;
+};
+
 // Decode-rows path (few tokens): one fused prologue, then FC1 and FC2 as
 // persistent warp-granular kernels over items of 16 weight rows x 256
 // contraction columns of one route block of 8 slots, each followed by an
@@ -77,6 +99,8 @@ struct DecPrologueArgs {
   int32_t* blk_meta;
   long long* blk_off1;
   long long* blk_off2;
+  int split_signs;          // separate gate / up input signs: rotate per route with `rr` (rows = routes)
+  RouteRotArgs rr;
 };
 
 constexpr int kDecSeg = 256;  // contraction columns of one decode-rows item
@@ -100,6 +124,13 @@ struct DecArgs {
   float* out;               // FC2: final output [T, H]
   int T;
   const uint16_t* lut;      // codebook table of the mode (65,536 fp16), or NULL: expand by the hash
+  // FC1 with separate gate / up input signs: activation rows are routes (not
+  // tokens); the gate strips read f.act / act_scaled / f.act_scale, the up
+  // strips these
+  int split;
+  const void* act2;
+  const uint16_t* act_scaled2;
+  const uint8_t* act_scale2;
 };
 
 cudaError_t launch_dec_prologue(const DecPrologueArgs& a, cudaStream_t st);
@@ -112,18 +143,22 @@ cudaError_t build_decode_lut(uint16_t* lut, cudaStream_t st);
 cudaError_t launch_dec_fc(const DecArgs& d, int proj, bool w4a8, int uniform_k, cudaStream_t st);
 cudaError_t launch_dec_epilogue(const DecArgs& d, int proj, bool w4a8, cudaStream_t st);
 
-// FC1 / FC2 on tcgen05 outside the decode regime: x~ [slots][H] and z~
-// [slots][I] fp16 in slot order (W4A8: the exact dequantized MXFP8 values),
-// route blocks of tc_route_block() slots.
+// FC1 / FC2 on tcgen05 outside the decode regime (W4A16): x~ [slots][H] and
+// z~ [slots][I] fp16 in slot order, route blocks of tc_route_block() slots.
 struct TcArgs {
   FcArgs f;
   int bi;          // FC1 half-row block (64 or 128)
   uint32_t* err;   // device error word (bit 1: a pipeline wait gave up)
   uint32_t* sched; // device unit counter, zero before the launch
   int act_rows;    // rows of the activation operand, in slot order: slots
+  uint64_t wait_ns;  // limit of every pipeline wait in ns (0: the default, 2 s)
+  int stall_issuer;  // test of the bounded waits: the MMA issuer first waits on a barrier nothing arrives on
+  int route_block;   // slots per route block: 256, or 128 with split activations
+  const void* act2;  // FC1 with separate gate / up input signs: the up rows' operand (f.act: the gate rows'), else NULL
+  CUtensorMap amap2; // filled by launch_tc_fc from act2
   CUtensorMap amap;  // filled by launch_tc_fc: the activations as [act_rows][K] fp16, box 64 x 128, 128-byte swizzle
 };
-cudaError_t launch_tc_fc(const TcArgs& args, int proj, int uniform_k, bool w4a8, int max_blocks, cudaStream_t st);
+cudaError_t launch_tc_fc(const TcArgs& args, int proj, int uniform_k, int max_blocks, cudaStream_t st);
 int tc_route_block();
 // Geometry the tcgen05 kernels handle (H, I, FC1 half-row block, rotation blocks).
 bool tc_supported(int H, int I, int bi, int rot_h, int rot_i);
@@ -135,11 +170,8 @@ int route_map_tiles(int R);
 cudaError_t launch_rotate_quant(const uint16_t* x, const uint16_t* suh, int T, int H, int rot_b, bool w4a8,
                                 void* xq, uint8_t* xs, cudaStream_t st, const int32_t* slot_of_route = nullptr,
                                 int topk = 0);
-
-// FC kernels. `bn` is the route block (8 or 64), `bi` the FC1 half-row block
-// (64 or 128), `uniform_k` the trellis K of every expert or 0 when mixed.
-cudaError_t launch_fc1(const FcArgs& a, bool w4a8, int bi, int bn, int uniform_k, int max_blocks, cudaStream_t st);
-cudaError_t launch_fc2(const FcArgs& a, bool w4a8, int bn, int uniform_k, int max_blocks, cudaStream_t st);
+// Separate gate / up input signs: both rotations per route (rotate_routes_warp).
+cudaError_t launch_rotate_routes(const RouteRotArgs& a, bool w4a8, cudaStream_t st);
 
 struct CombineUnrotArgs {
   const float* rows;            // [slots, H]: per 128-column block, (I_2 x H_64)(scale * FC2 accumulator)

@@ -180,7 +180,8 @@ tm_status trellis_linear_forward(tm_linear* lin, const uint16_t* x, int32_t T, f
   t.err = err;
   t.sched = err + 1;
   t.act_rows = slots;
-  if ((e = tmoe::launch_tc_fc(t, 2, d.bits, false, L.blocks, st)) != cudaSuccess) return lin_cuda_fail(e, "projection");
+  t.route_block = tmoe::tc_route_block();
+  if ((e = tmoe::launch_tc_fc(t, 2, d.bits, L.blocks, st)) != cudaSuccess) return lin_cuda_fail(e, "projection");
   return TM_OK;
 }
 

@@ -18,12 +18,29 @@ __global__ void __launch_bounds__(256) k_rotate_quant(const uint16_t* __restrict
 cudaError_t launch_rotate_quant(const uint16_t* x, const uint16_t* suh, int T, int H, int rot_b, bool w4a8,
                                 void* xq, uint8_t* xs, cudaStream_t st, const int32_t* slot_of_route, int topk) {
   if (T == 0) return cudaSuccess;
+  if (w4a8 && slot_of_route != nullptr) return cudaErrorInvalidValue;  // slot order is the fp16 (W4A16) form
   const long warps = (long)T * (H / 128);
   const int blocks = (int)((warps * 32 + 255) / 256);
   if (w4a8)
     k_rotate_quant<true><<<blocks, 256, 0, st>>>(x, suh, T, H, rot_b, xq, xs, slot_of_route, topk);
   else
     k_rotate_quant<false><<<blocks, 256, 0, st>>>(x, suh, T, H, rot_b, xq, xs, slot_of_route, topk);
+  return cudaGetLastError();
+}
+
+template <bool W4A8>
+__global__ void __launch_bounds__(256) k_rotate_routes(const RouteRotArgs a) {
+  rotate_routes_warp<W4A8>(a, (blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+}
+
+cudaError_t launch_rotate_routes(const RouteRotArgs& a, bool w4a8, cudaStream_t st) {
+  if (a.T == 0) return cudaSuccess;
+  const long warps = (long)a.T * (a.H / 128);
+  const int blocks = (int)((warps * 32 + 255) / 256);
+  if (w4a8)
+    k_rotate_routes<true><<<blocks, 256, 0, st>>>(a);
+  else
+    k_rotate_routes<false><<<blocks, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -15,11 +15,12 @@ static __device__ __forceinline__ float route_unkey(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Top-k softmax of one token's logits by one warp: k rounds of a warp-wide
-// max of the remaining keys, ties to the lowest expert id; weights
-// exp(l - l_max) / sum over the selected, summed in selection order.
-static __device__ __forceinline__ void route_token_redux(const float* __restrict__ row, int E, int k, int t,
-                                                int32_t* __restrict__ ids, float* __restrict__ w, int* s_ids = nullptr) {
+// Top-k selection of one token's logits by one warp: k rounds of a warp-wide
+// max of the remaining keys, ties to the lowest expert id. Lane j < k gets the
+// j-th selected id and its unnormalised weight exp(l - l_max); *wsum the sum
+// of those weights in selection order (every lane).
+static __device__ __forceinline__ void route_token_select(const float* __restrict__ row, int E, int k, int& my_id,
+                                                          float& my_w, float& wsum) {
   const int lane = threadIdx.x & 31;
   uint32_t key[kMaxExperts / 32];
 #pragma unroll
@@ -27,8 +28,10 @@ static __device__ __forceinline__ void route_token_redux(const float* __restrict
     const int e = lane + 32 * i;
     key[i] = (e < E) ? route_key(__ldg(row + e)) : 0u;  // 0: absent or taken
   }
-  float best0 = 0.0f, wsum = 0.0f, my_w = 0.0f;
-  int my_id = 0;
+  float best0 = 0.0f;
+  wsum = 0.0f;
+  my_w = 0.0f;
+  my_id = 0;
   for (int j = 0; j < k; ++j) {
     uint32_t lm = 0;
 #pragma unroll
@@ -51,6 +54,17 @@ static __device__ __forceinline__ void route_token_redux(const float* __restrict
       my_w = ex;
     }
   }
+}
+
+// Top-k softmax of one token's logits by one warp (route_token_select); the
+// weights are exp(l - l_max) / sum over the selected, summed in selection
+// order.
+static __device__ __forceinline__ void route_token_redux(const float* __restrict__ row, int E, int k, int t,
+                                                int32_t* __restrict__ ids, float* __restrict__ w, int* s_ids = nullptr) {
+  const int lane = threadIdx.x & 31;
+  int my_id;
+  float my_w, wsum;
+  route_token_select(row, E, k, my_id, my_w, wsum);
   if (lane < k) {
     ids[(size_t)t * k + lane] = my_id;
     w[(size_t)t * k + lane] = my_w / wsum;

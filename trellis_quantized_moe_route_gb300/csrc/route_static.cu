@@ -2,11 +2,10 @@
 //
 // trellis_moe_route_map takes a caller-provided workspace for its scratch
 // (per-route ranks, per-tile counts, the route-block table). Some callers
-// cannot hand over scratch memory: code that runs while a CUDA graph is being
-// captured, where cudaMalloc is not allowed; hosts that own every byte of
-// device memory through a fixed plan and pass the library only its inputs and
-// outputs; and latency-critical loops that must never enter the allocator
-// after start-up, because an allocation can synchronise the device. For them,
+// cannot hand over scratch memory: hosts that own every byte of device memory
+// through a fixed plan and pass the library only its inputs and outputs, and
+// latency-critical loops that must never enter the allocator after start-up,
+// because an allocation can synchronise the device. For them,
 // trellis_moe_route_map_static keeps its scratch in one statically sized
 // array in device memory that exists for as long as the library is loaded.
 //
@@ -15,7 +14,10 @@
 // array, so two calls whose kernels overlap on the GPU (different streams
 // without ordering between them) race and corrupt each other's result; order
 // them on one stream. The array keeps the previous call's contents; the parts
-// that must start from zero (the error word) are cleared by every call.
+// that must start from zero (the error word) are cleared by every call. The
+// array's device address is looked up once per device and kept for the life
+// of the process, so a device reset (cudaDeviceReset) while the library is
+// loaded is not supported: the kept address would be stale afterwards.
 #include <mutex>
 
 #include "../../include/trellis_moe.h"

@@ -1,6 +1,7 @@
 // FC1 / FC2 on the 5th-generation tensor cores (sm_103a) outside the decode
-// regime: W4A16, and W4A8 with E4M3-rounded weights and exactly dequantized
-// MXFP8 activations held in fp16.
+// regime, W4A16: fp16 activations x fp16 trellis weights -> fp32 (W4A8 is the
+// bounded-decode-rows mode, b12x PR #129 "feat(moe): serve canonical Fruit
+// QSRT atoms", Hot path, and runs on the decode-rows kernels).
 //
 // A persistent, warp-specialised kernel; one CTA per SM takes work units
 // (route block rb of up to 256 routes of one expert) x (block mb of N weight
@@ -68,7 +69,7 @@ constexpr int kTcEpiWarps = 8;         // two per TMEM lane quarter, one per col
 constexpr int kEvecBytes = 1024;       // per epilogue warp: its half of the unit's folded vectors (fp32)
 constexpr int kStageWords = 20;        // per epilogue warp: 32 rows x 16 words of output staging, stride 20 words
 constexpr int kStageBytes = 32 * kStageWords * 4;
-constexpr int kTcBN = 256;             // routes per route block
+constexpr int kTcBN = 256;             // routes per route block (128 with split gate / up operands)
 constexpr int kTcKS = 64;              // contraction columns per stage
 constexpr int kSA = 2, kSW = 4, kSBMax = 3;
 // decoded-operand ring depth: 3 for the 4-bit payload, 2 for the general
@@ -76,7 +77,11 @@ constexpr int kSA = 2, kSW = 4, kSBMax = 3;
 __host__ __device__ constexpr int tc_sb(int KB) { return KB > 0 ? 3 : 2; }
 constexpr int kABytes = 256 * 128;     // activation operand: 256 routes x 128 bytes
 constexpr int kBBytes = 256 * 128;     // decoded operand: 256 weight rows x 128 bytes
-constexpr uint64_t kTcWaitNs = 2000000000ull;
+constexpr uint64_t kTcWaitNs = 2000000000ull;   // default limit of a pipeline wait
+constexpr uint64_t kTcDrainNs = kTcWaitNs / 4;   // limit of a wait for copies in flight after an abort
+
+// Limit (ns) of every pipeline wait of this CTA, from the launch arguments.
+__shared__ uint64_t tc_wait_limit;
 
 // Payload of one stage: 16 tile rows x 4 tiles of 32K bytes.
 __host__ __device__ constexpr int tc_wslot_bytes(int kmax) { return 16 * 4 * 32 * kmax; }
@@ -89,6 +94,7 @@ __host__ __device__ constexpr int tc_smem_total(int kmax, int sb) {
 struct TcBars {
   uint64_t fullA[kSA], emptyA[kSA], fullB[kSBMax], emptyB[kSBMax], fullW[kSW], emptyW[kSW], accFull[2], accEmpty[2];
   uint64_t pair[4];  // epilogue warp pairs, one per TMEM lane quarter
+  uint64_t never;    // nothing arrives here: the issuer's wait on it runs out (stall_issuer test)
   uint64_t fullU[4], emptyU[4];  // unit ring: the scheduler's picks, read by every role in order
 };
 
@@ -128,13 +134,6 @@ __device__ __forceinline__ void run_window_smem(const uint16_t* tile, int j0, ui
   lo = (w2 << 16) | w3;
 }
 
-// W4A8 weights: every fp16 codebook value replaced by its E4M3 rounding
-// (nearest even, saturating), held exactly in fp16.
-__device__ __forceinline__ void e4m3_round(uint32_t (&w)[4]) {
-#pragma unroll
-  for (int p = 0; p < 4; ++p) w[p] = e4m3x2_to_f16x2(cvt_e4m3x2(w[p]));
-}
-
 __device__ __forceinline__ void sts128(unsigned char* p, const uint32_t (&w)[4]) {
   *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
@@ -144,7 +143,7 @@ __device__ __forceinline__ void sts128(unsigned char* p, const uint32_t (&w)[4])
 // into the swizzled operand `bsl`. Thread t takes row t % NR and 8 * NR / 256
 // of the row's 8 chunks of 8 columns; chunk c of a row is run (tile c / 2,
 // half c % 2) of the row's trellis tiles.
-template <int NR, int K, bool W4A8>
+template <int NR, int K>
 __device__ __forceinline__ void tc_expand_stage(const unsigned char* wsl, unsigned char* bsl, int tid,
                                                 uint32_t k16, uint32_t nk16) {
   constexpr int CPT = 8 * NR / 256;
@@ -168,11 +167,9 @@ __device__ __forceinline__ void tc_expand_stage(const unsigned char* wsl, unsign
       uint32_t y[8], w[4];
       run_mcg_k4(pw, cw.x, k16, nk16, y);
       raw_to_f16(y, w);
-      if (W4A8) e4m3_round(w);
       sts128(brow + (((uint32_t)(2 * t) ^ sw) << 4), w);
       run_mcg_k4(cw.x, cw.y, k16, nk16, y);
       raw_to_f16(y, w);
-      if (W4A8) e4m3_round(w);
       sts128(brow + (((uint32_t)(2 * t + 1) ^ sw) << 4), w);
     }
   } else {
@@ -187,7 +184,6 @@ __device__ __forceinline__ void tc_expand_stage(const unsigned char* wsl, unsign
 #pragma unroll
       for (int q = 0; q < 8; ++q) y[q] = mcg_raw(s8[q]);
       raw_to_f16(y, w);
-      if (W4A8) e4m3_round(w);
       sts128(brow + (((uint32_t)c ^ sw) << 4), w);
     }
   }
@@ -197,7 +193,7 @@ __device__ __forceinline__ void tc_expand_stage(const unsigned char* wsl, unsign
 __device__ __forceinline__ void mbar_wait_drain(uint64_t* mbar, uint32_t parity) {
   const uint32_t a = smem_u32(mbar);
   const uint64_t t0 = global_ns();
-  while (!mbar_try(a, parity) && global_ns() - t0 < kTcWaitNs / 4) {
+  while (!mbar_try(a, parity) && global_ns() - t0 < kTcDrainNs) {
   }
 }
 
@@ -318,7 +314,7 @@ __device__ __forceinline__ bool pair_sync(PairSync& p, volatile int* abort) {
   tc_fence_before();
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(p.bar);
-  const bool ok = mbar_wait_abort(p.bar, p.phase & 1, abort, kTcWaitNs);
+  const bool ok = mbar_wait_abort_lim(p.bar, p.phase & 1, abort, &tc_wait_limit);
   ++p.phase;
   tc_fence_after();
   return __all_sync(0xFFFFFFFFu, ok);
@@ -346,7 +342,7 @@ __device__ __forceinline__ void combine_half(float2 (&w)[HF / 2], uint32_t their
 // partner's, then parks SiLU(gate) in the partner's gate half (which only it
 // reads from then on) and later publishes its final half there too.
 // ev (fp32, HF each): gate scale, hs * gate svh, up scale, hs * up svh * down suh.
-template <int BI, bool W4A8>
+template <int BI>
 __device__ __forceinline__ bool tc_epi_fc1(const FcArgs& a, const float* ev, uint32_t* stg, int mb, int slot, bool valid,
                                            uint32_t tg, int h, PairSync& ps, volatile int* abort) {
   constexpr int HF = BI / 2;
@@ -394,25 +390,6 @@ __device__ __forceinline__ bool tc_epi_fc1(const FcArgs& a, const float* ev, uin
     const float2 h2s = make_float2(hs, hs);
 #pragma unroll
     for (int j = 0; j < HF / 2; ++j) w[j] = __fmul2_rn(w[j], h2s);
-    if (W4A8) {
-      // MXFP8 over each 32 consecutive values (E8M0 exponent from the block's
-      // max |z|, E4M3 nearest even, saturating), stored as the exact
-      // dequantized values
-#pragma unroll
-      for (int b0 = 0; b0 < HF / 2; b0 += 16) {
-        float amax = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fmaxf(fabsf(w[b0 + j].x), fabsf(w[b0 + j].y)));
-        const int ex = e8m0_exponent(amax);
-        const float inv = exp2_int(-ex), sc = exp2_int(ex);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const uint32_t q = e4m3x2_to_f16x2(e4m3x2_from_float2(w[b0 + j].x * inv, w[b0 + j].y * inv));
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&q));
-          w[b0 + j] = make_float2(f.x * sc, f.y * sc);
-        }
-      }
-    }
     // this half of the z~ row, 32 fp16 (16 words) at a time
     uint32_t* zb = reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(a.out_act) + mb * BI + h * HF);
 #pragma unroll
@@ -506,9 +483,9 @@ __device__ __forceinline__ bool tc_epi_fc2(const FcArgs& a, const float* ev, uin
 // Roles. Every role walks the same unit sequence u = blockIdx.x, +gridDim.x, ...
 // and the same global stage counter g, so ring slots and phases agree.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ int tc_macc(const FcArgs& a, int slot0) {
+__device__ __forceinline__ int tc_macc(const TcArgs& args, int slot0) {
   // valid routes are a prefix of the block: a second accumulator iff route 128 exists
-  return (a.route_of_slot[slot0 + 128] >= 0) ? 2 : 1;
+  return (args.route_block > 128 && args.f.route_of_slot[slot0 + 128] >= 0) ? 2 : 1;
 }
 
 // Unit ring. The payload warp, the first role to need a unit, claims units
@@ -523,7 +500,7 @@ constexpr int kUnitConsumers = 8 + kTcEpiWarps + 2;  // expander warps, epilogue
 // -1 when the units are done or a wait gave up (then *ok = false).
 __device__ __forceinline__ int pop_unit_warp(TcBars& B, volatile int* uring, int& i, volatile int* abort, bool* ok) {
   const int slot = i % kUnitRing;
-  const bool w = mbar_wait_abort(&B.fullU[slot], (i / kUnitRing) & 1, abort, kTcWaitNs);
+  const bool w = mbar_wait_abort_lim(&B.fullU[slot], (i / kUnitRing) & 1, abort, &tc_wait_limit);
   if (!__all_sync(0xFFFFFFFFu, w)) {
     *ok = false;
     return -1;
@@ -536,7 +513,7 @@ __device__ __forceinline__ int pop_unit_warp(TcBars& B, volatile int* uring, int
 }
 __device__ __forceinline__ int pop_unit_thread(TcBars& B, volatile int* uring, int& i, volatile int* abort, bool* ok) {
   const int slot = i % kUnitRing;
-  if (!mbar_wait_abort(&B.fullU[slot], (i / kUnitRing) & 1, abort, kTcWaitNs)) {
+  if (!mbar_wait_abort_lim(&B.fullU[slot], (i / kUnitRing) & 1, abort, &tc_wait_limit)) {
     *ok = false;
     return -1;
   }
@@ -555,7 +532,7 @@ struct TcAccPlan {
   __device__ __forceinline__ void advance(int macc) { nb = (macc == 2) ? 0 : (nb ^ 1); }
 };
 
-template <int PROJ, int KB, int NR, bool W4A8>
+template <int PROJ, int KB, int NR>
 __device__ __forceinline__ void tc_expanders(const TcArgs& args, const TcGeom<PROJ, NR>& G, volatile int* uring, TcBars& B,
                                              const unsigned char* wring, unsigned char* bring, volatile int* abort) {
   const FcArgs& a = args.f;
@@ -569,20 +546,20 @@ __device__ __forceinline__ void tc_expanders(const TcArgs& args, const TcGeom<PR
     const int K = (KB > 0) ? KB : a.bits[a.block_expert[rb]];
     for (int s = 0; s < G.nst; ++s, ++g) {
       const int ws = g % kSW, bs = g % tc_sb(KB);
-      bool ok = mbar_wait_abort(&B.fullW[ws], (g / kSW) & 1, abort, kTcWaitNs);
-      if (ok && g >= tc_sb(KB)) ok = mbar_wait_abort(&B.emptyB[bs], ((g / tc_sb(KB)) - 1) & 1, abort, kTcWaitNs);
+      bool ok = mbar_wait_abort_lim(&B.fullW[ws], (g / kSW) & 1, abort, &tc_wait_limit);
+      if (ok && g >= tc_sb(KB)) ok = mbar_wait_abort_lim(&B.emptyB[bs], ((g / tc_sb(KB)) - 1) & 1, abort, &tc_wait_limit);
       if (!__all_sync(0xFFFFFFFFu, ok)) return;
       const unsigned char* wsl = wring + ws * wsz;
       unsigned char* bsl = bring + bs * kBBytes;
       if (KB > 0) {
-        tc_expand_stage<NR, (KB > 0 ? KB : 4), W4A8>(wsl, bsl, tid, k16, nk16);
+        tc_expand_stage<NR, (KB > 0 ? KB : 4)>(wsl, bsl, tid, k16, nk16);
       } else {
         switch (K) {
-          case 2: tc_expand_stage<NR, 2, W4A8>(wsl, bsl, tid, k16, nk16); break;
-          case 3: tc_expand_stage<NR, 3, W4A8>(wsl, bsl, tid, k16, nk16); break;
-          case 4: tc_expand_stage<NR, 4, W4A8>(wsl, bsl, tid, k16, nk16); break;
-          case 5: tc_expand_stage<NR, 5, W4A8>(wsl, bsl, tid, k16, nk16); break;
-          default: tc_expand_stage<NR, 6, W4A8>(wsl, bsl, tid, k16, nk16); break;
+          case 2: tc_expand_stage<NR, 2>(wsl, bsl, tid, k16, nk16); break;
+          case 3: tc_expand_stage<NR, 3>(wsl, bsl, tid, k16, nk16); break;
+          case 4: tc_expand_stage<NR, 4>(wsl, bsl, tid, k16, nk16); break;
+          case 5: tc_expand_stage<NR, 5>(wsl, bsl, tid, k16, nk16); break;
+          default: tc_expand_stage<NR, 6>(wsl, bsl, tid, k16, nk16); break;
         }
       }
       fence_proxy_async();  // generic-proxy stores -> visible to the tensor core
@@ -595,7 +572,7 @@ __device__ __forceinline__ void tc_expanders(const TcArgs& args, const TcGeom<PR
   }
 }
 
-template <int PROJ, int KB, int NR, bool W4A8>
+template <int PROJ, int KB, int NR>
 __device__ __forceinline__ void tc_epilogue(const TcArgs& args, const TcGeom<PROJ, NR>& G, volatile int* uring, TcBars& B,
                                             float* ev, uint32_t* stg, uint32_t tmem, volatile int* abort) {
   const FcArgs& a = args.f;
@@ -609,8 +586,8 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& args, const TcGeom<PRO
   for (int u; (u = pop_unit_warp(B, uring, iu, abort, &ok)) >= 0;) {
     const int rb = u / G.mblocks, mb = u - rb * G.mblocks;
     const int e = a.block_expert[rb];
-    const int slot0 = rb * kTcBN;
-    const int macc = tc_macc(a, slot0);
+    const int slot0 = rb * args.route_block;
+    const int macc = tc_macc(args, slot0);
     // this warp's half of the unit's vectors, converted to fp32 and folded
     // (its reads of the last unit are done)
     __syncwarp();
@@ -639,7 +616,7 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& args, const TcGeom<PRO
     __syncwarp();
     for (int acc = 0; acc < macc; ++acc) {
       const int b = plan.buf(macc, acc);
-      const bool ok = mbar_wait_abort(&B.accFull[b], plan.uses[b] & 1, abort, kTcWaitNs);
+      const bool ok = mbar_wait_abort_lim(&B.accFull[b], plan.uses[b] & 1, abort, &tc_wait_limit);
       if (!__all_sync(0xFFFFFFFFu, ok)) return;
       tc_fence_after();
       const int n = acc * 128 + 32 * q + lane;
@@ -649,7 +626,7 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& args, const TcGeom<PRO
       // of the pair see the same lanes, so they skip together)
       if (__any_sync(0xFFFFFFFFu, route >= 0)) {
         const bool done = (PROJ == 1)
-                              ? tc_epi_fc1<NR / 2, W4A8>(a, ev, stg, mb, slot0 + n, route >= 0, taddr, h, ps, abort)
+                              ? tc_epi_fc1<NR / 2>(a, ev, stg, mb, slot0 + n, route >= 0, taddr, h, ps, abort)
                               : tc_epi_fc2<NR>(a, ev, stg, mb, slot0 + n, route, route >= 0, taddr, h, ps, abort);
         if (!done) return;
       }
@@ -675,7 +652,7 @@ __device__ __forceinline__ void tc_payload_loader(const TcArgs& args, const TcGe
   for (int iu = 0;; ++iu) {
     const int slot = iu % kUnitRing;
     if (iu >= kUnitRing) {
-      const bool okr = mbar_wait_abort(&B.emptyU[slot], ((iu / kUnitRing) - 1) & 1, abort, kTcWaitNs);
+      const bool okr = mbar_wait_abort_lim(&B.emptyU[slot], ((iu / kUnitRing) - 1) & 1, abort, &tc_wait_limit);
       if (!__all_sync(0xFFFFFFFFu, okr)) {
         ok = false;
         break;
@@ -697,7 +674,7 @@ __device__ __forceinline__ void tc_payload_loader(const TcArgs& args, const TcGe
     if (lane < NR / 16) wsrc += a.word_off[e] + (size_t)(G.tile_row0(a, mb, lane) >> 4) * G.tiles_k * 16 * K;
     for (int s = 0; s < G.nst; ++s, ++g) {
       const int ws = g % kSW;
-      const bool okw = (g < kSW) || mbar_wait_abort(&B.emptyW[ws], ((g / kSW) - 1) & 1, abort, kTcWaitNs);
+      const bool okw = (g < kSW) || mbar_wait_abort_lim(&B.emptyW[ws], ((g / kSW) - 1) & 1, abort, &tc_wait_limit);
       if (!__all_sync(0xFFFFFFFFu, okw)) {
         ok = false;
         break;
@@ -733,18 +710,22 @@ __device__ __forceinline__ void tc_act_loader(const TcArgs& args, const TcGeom<P
   int g = 0, ga = 0, iu = 0;
   bool ok = true;
   for (int u; ok && (u = pop_unit_thread(B, uring, iu, abort, &ok)) >= 0;) {
-    const int slot0 = (u / G.mblocks) * kTcBN;
-    const int macc = tc_macc(a, slot0);
+    const int slot0 = (u / G.mblocks) * args.route_block;
+    const int macc = tc_macc(args, slot0);
+    const bool split = args.act2 != nullptr;  // (route blocks of 128: one accumulator)
     for (int s = 0; s < G.nst; ++s, ++g) {
       const int as = g % kSA;
-      if (g >= kSA && !mbar_wait_abort(&B.emptyA[as], ((g / kSA) - 1) & 1, abort, kTcWaitNs)) {
+      if (g >= kSA && !mbar_wait_abort_lim(&B.emptyA[as], ((g / kSA) - 1) & 1, abort, &tc_wait_limit)) {
         ok = false;
         break;
       }
-      mbar_arrive_expect_tx(&B.fullA[as], (uint32_t)macc * 128 * 128);
+      mbar_arrive_expect_tx(&B.fullA[as], (uint32_t)(split ? 2 : macc) * 128 * 128);
       unsigned char* dst = aring + as * kABytes;
       tma_tile2d(dst, map, s * kTcKS, slot0, &B.fullA[as]);
-      if (macc == 2) tma_tile2d(dst + 128 * 128, map, s * kTcKS, slot0 + 128, &B.fullA[as]);
+      if (split)  // the up rows' operand in the second half
+        tma_tile2d(dst + 128 * 128, &args.amap2, s * kTcKS, slot0, &B.fullA[as]);
+      else if (macc == 2)
+        tma_tile2d(dst + 128 * 128, map, s * kTcKS, slot0 + 128, &B.fullA[as]);
       ga = g + 1;
     }
   }
@@ -758,24 +739,29 @@ __device__ __forceinline__ void tc_issuer(const TcArgs& args, const TcGeom<PROJ,
                                           volatile int* abort) {
   const FcArgs& a = args.f;
   const uint32_t idesc = idesc_f16(128, NR);
+  const uint32_t idesc_half = idesc_f16(128, NR / 2);
+  const bool split = args.act2 != nullptr;
   const uint64_t adesc0 = smem_desc_sw128(smem_u32(aring));
   const uint64_t bdesc0 = smem_desc_sw128(smem_u32(bring));
   TcAccPlan plan;
   int g = 0, glast = -1, iu = 0;
   bool ok = true;
+  // test of the bounded waits: a wait that nothing ends, before any MMA is
+  // issued, so that the CTA aborts with only completed copies behind it
+  if (args.stall_issuer && !mbar_wait_abort_lim(&B.never, 0, abort, &tc_wait_limit)) return;
   for (int u; ok && (u = pop_unit_thread(B, uring, iu, abort, &ok)) >= 0;) {
-    const int macc = tc_macc(a, (u / G.mblocks) * kTcBN);
+    const int macc = tc_macc(args, (u / G.mblocks) * args.route_block);
     for (int acc = 0; acc < macc && ok; ++acc) {  // the unit's buffers drained by the epilogue
       const int b = plan.buf(macc, acc);
-      if (plan.uses[b] > 0) ok = mbar_wait_abort(&B.accEmpty[b], (plan.uses[b] - 1) & 1, abort, kTcWaitNs);
+      if (plan.uses[b] > 0) ok = mbar_wait_abort_lim(&B.accEmpty[b], (plan.uses[b] - 1) & 1, abort, &tc_wait_limit);
     }
     if (!ok) break;
     tc_fence_after();
     const uint32_t d0 = tmem + (uint32_t)(plan.buf(macc, 0) * 256);
     for (int s = 0; s < G.nst; ++s, ++g) {
       const int as = g % kSA, bs = g % tc_sb(KB);
-      if (!mbar_wait_abort(&B.fullA[as], (g / kSA) & 1, abort, kTcWaitNs) ||
-          !mbar_wait_abort(&B.fullB[bs], (g / tc_sb(KB)) & 1, abort, kTcWaitNs)) {
+      if (!mbar_wait_abort_lim(&B.fullA[as], (g / kSA) & 1, abort, &tc_wait_limit) ||
+          !mbar_wait_abort_lim(&B.fullB[bs], (g / tc_sb(KB)) & 1, abort, &tc_wait_limit)) {
         ok = false;
         break;
       }
@@ -783,11 +769,24 @@ __device__ __forceinline__ void tc_issuer(const TcArgs& args, const TcGeom<PROJ,
       tc_fence_after();
       const uint64_t ad = adesc0 + (uint64_t)(as * (kABytes >> 4));
       const uint64_t bd = bdesc0 + (uint64_t)(bs * (kBBytes >> 4));
+      if (split) {
+        // gate rows (decoded rows 0..NR/2-1) x the gate operand into columns
+        // 0..NR/2-1, up rows x the up operand (second half of the A slot)
+        // into columns NR/2..NR-1
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint32_t accum = (s > 0 || kk > 0) ? 1u : 0u;
-        tc_mma_f16(d0, ad + 2 * kk, bd + 2 * kk, idesc, accum);
-        if (macc == 2) tc_mma_f16(tmem + 256, ad + 1024 + 2 * kk, bd + 2 * kk, idesc, accum);
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t accum = (s > 0 || kk > 0) ? 1u : 0u;
+          tc_mma_f16(d0, ad + 2 * kk, bd + 2 * kk, idesc_half, accum);
+          tc_mma_f16(d0 + NR / 2, ad + 1024 + 2 * kk, bd + (uint64_t)(NR / 2 * 128 >> 4) + 2 * kk, idesc_half,
+                     accum);
+        }
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t accum = (s > 0 || kk > 0) ? 1u : 0u;
+          tc_mma_f16(d0, ad + 2 * kk, bd + 2 * kk, idesc, accum);
+          if (macc == 2) tc_mma_f16(tmem + 256, ad + 1024 + 2 * kk, bd + 2 * kk, idesc, accum);
+        }
       }
       tc_commit(&B.emptyA[as]);
       tc_commit(&B.emptyB[bs]);
@@ -809,7 +808,7 @@ __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.a
 template <int N>
 __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N)); }
 
-template <int PROJ, int KB, int NR, bool W4A8>
+template <int PROJ, int KB, int NR>
 __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__ TcArgs args) {
   extern __shared__ unsigned char tc_smem_raw[];
   __shared__ __align__(8) TcBars bars;
@@ -843,6 +842,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__
       mbar_init(&bars.accEmpty[i], kTcEpiWarps);
     }
     for (int i = 0; i < 4; ++i) mbar_init(&bars.pair[i], 2);
+    mbar_init(&bars.never, 1);
+    tc_wait_limit = args.wait_ns ? args.wait_ns : kTcWaitNs;
     for (int i = 0; i < kUnitRing; ++i) {
       mbar_init(&bars.fullU[i], 1);
       mbar_init(&bars.emptyU[i], kUnitConsumers);
@@ -860,10 +861,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__
   volatile int* uring = s_uring;
   if (warp < 8) {
     if (TcRegs<KB>::exp < kRegLaunch) regs_dec<TcRegs<KB>::exp>();
-    tc_expanders<PROJ, KB, NR, W4A8>(args, G, uring, bars, wring, bring, abort);
+    tc_expanders<PROJ, KB, NR>(args, G, uring, bars, wring, bring, abort);
   } else if (warp < 16) {
     regs_inc<TcRegs<KB>::epi>();
-    tc_epilogue<PROJ, KB, NR, W4A8>(args, G, uring, bars, reinterpret_cast<float*>(evec + (warp - 8) * kEvecBytes),
+    tc_epilogue<PROJ, KB, NR>(args, G, uring, bars, reinterpret_cast<float*>(evec + (warp - 8) * kEvecBytes),
                                     reinterpret_cast<uint32_t*>(evec + kTcEpiWarps * kEvecBytes + (warp - 8) * kStageBytes),
                                     tmem, abort);
   } else {
@@ -882,9 +883,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-template <int PROJ, int KB, int NR, bool W4A8>
+template <int PROJ, int KB, int NR>
 static cudaError_t launch_tc_t(const TcArgs& args, int max_blocks, cudaStream_t st) {
-  auto kern = k_tc_fc<PROJ, KB, NR, W4A8>;
+  auto kern = k_tc_fc<PROJ, KB, NR>;
   constexpr int kmax = KB > 0 ? KB : 6;
   static_assert(tc_smem_total(kmax, tc_sb(KB)) + 1024 <= 232448, "dynamic + static shared memory over the per-block limit");
   static bool attr_done = false;  // first forward call, before any capture
@@ -927,7 +928,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-cudaError_t launch_tc_fc(const TcArgs& args_in, int proj, int uniform_k, bool w4a8, int max_blocks, cudaStream_t st) {
+cudaError_t launch_tc_fc(const TcArgs& args_in, int proj, int uniform_k, int max_blocks, cudaStream_t st) {
   TcArgs args = args_in;
   {
     // the activation operand [act_rows][K] fp16 in boxes of 64 columns (128
@@ -943,11 +944,19 @@ cudaError_t launch_tc_fc(const TcArgs& args_in, int proj, int uniform_k, bool w4
                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (args.act2 != nullptr) {
+      // separate gate / up operands: FC1 only, one 128-route accumulator per unit
+      if (proj != 1 || args.route_block != 128) return cudaErrorInvalidValue;
+      const CUresult r2 = enc(&args.amap2, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(args.act2), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r2 != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    if (args.route_block != 128 && args.route_block != kTcBN) return cudaErrorInvalidValue;
   }
   const bool k4 = uniform_k == 4;
-#define TC_DISPATCH(P, N)                                                                                  \
-  return w4a8 ? (k4 ? launch_tc_t<P, 4, N, true>(args, max_blocks, st) : launch_tc_t<P, 0, N, true>(args, max_blocks, st)) \
-              : (k4 ? launch_tc_t<P, 4, N, false>(args, max_blocks, st) : launch_tc_t<P, 0, N, false>(args, max_blocks, st))
+#define TC_DISPATCH(P, N) \
+  return k4 ? launch_tc_t<P, 4, N>(args, max_blocks, st) : launch_tc_t<P, 0, N>(args, max_blocks, st)
   if (proj == 1) {
     if (args.bi == 128) TC_DISPATCH(1, 256);
     TC_DISPATCH(1, 128);

@@ -178,4 +178,24 @@ __device__ __forceinline__ bool mbar_wait_abort(uint64_t* mbar, uint32_t parity,
   }
 }
 
+// As mbar_wait_abort, with the limit read from `*limit_ns` only after the
+// first test failed, so that no register holds it across the caller's loops.
+__device__ __forceinline__ bool mbar_wait_abort_lim(uint64_t* mbar, uint32_t parity, volatile int* abort,
+                                                    const volatile uint64_t* limit_ns) {
+  const uint32_t a = smem_u32(mbar);
+  if (mbar_try(a, parity)) return true;
+  const uint64_t limit = *limit_ns;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try(a, parity)) return true;
+    if ((it & 31) == 0) {
+      if (*abort) return false;
+      if (global_ns() - t0 > limit) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 }  // namespace tmoe
