@@ -150,11 +150,14 @@ def touched_bytes_fc1(cfg, ids, T, mode):
 
 
 
-def sleep_ahead(stream, us: float = 2000.0):
-    """A device-side spin on `stream` ahead of the timed region, so that the
-    host has queued the timed steps before the first one starts and the
-    region measures device throughput, not the host's launch latency."""
+def sleep_ahead(stream, steps: int):
+    """A device-side spin on `stream` ahead of the timed region, long enough
+    for the host to queue the timed steps (~150 us of host time per graph
+    replay, plus 2 ms), so that the region measures the device's throughput
+    on resident inputs rather than the host's launch rate. The end-to-end
+    host-buffer figure (`e2e`) is the number with the host in the loop."""
     import torch
+    us = min(200000.0, 2000.0 + 150.0 * steps)
     with torch.cuda.stream(stream):
         torch.cuda._sleep(int(us * 2.0e3))   # ~us at 2 GHz
 
@@ -234,7 +237,7 @@ def measure_layer(name, T, mode, steps, warmup, rank, world, dev, e2e_steps):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    sleep_ahead(stream)
+    sleep_ahead(stream, steps)
     t0.record(stream)
     # the last three timed steps (or fewer) use the event-recording graphs: the
     # stage statistics need only a few samples, and every recorded event adds
@@ -333,7 +336,7 @@ def measure_layer(name, T, mode, steps, warmup, rank, world, dev, e2e_steps):
                    "l2": "inputs larger than L2: %d layer copies and token batches cycled" % copies,
                    "distinct_experts_per_step": round(statistics.mean(distinct), 2),
                    "graphs": "one CUDA graph per (layer copy, batch), replayed; the last %d timed steps use "
-                             "graphs that also record stage events; a ~2 ms device-side spin precedes the "
+                             "graphs that also record stage events; a device-side spin precedes the "
                              "timed region so that the host has queued the steps" % n_ev},
         "roofline": roof, "stages_us": stages_us, "e2e": e2e,
         "gpu_launches": launches_per_step * steps, "clocks": sampler.summary(),

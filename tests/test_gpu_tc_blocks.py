@@ -1,9 +1,11 @@
 """Route-block boundaries against the oracle: experts whose route counts sit
-on both sides of the tensor-core kernels' one / two accumulator switch
-(128 / 129 routes) and of their 256-route block (256 / 257), so that blocks
-of one, two and several accumulators and multi-block experts all occur
-(W4A16). The same layer in W4A8 (872 routes) runs on the decode rows, whose
-8-slot route blocks then hold many blocks per expert."""
+on both sides of 128 and 256 routes. With at most 128 routes per expert on
+average the tensor-core kernels use 128-route blocks (one accumulator each;
+the 128 / 129 and 256 / 257 counts give one, two and three blocks per
+expert); with more they use 256-route blocks, where 129 routes switch a unit
+to two accumulators and 257 to a second block (W4A16). The first layer in
+W4A8 (872 routes) runs on the decode rows, whose 8-slot route blocks then
+hold many blocks per expert."""
 import numpy as np
 import pytest
 
@@ -13,7 +15,10 @@ from trellis_quantized_moe_route_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 
-COUNTS = [257, 256, 129, 128, 1, 37, 60, 4]   # routes per expert (E = 8, top-2)
+COUNTS = {
+    "128-route blocks": [257, 256, 129, 128, 1, 37, 60, 4],   # E = 8, top-2: 109 routes per expert
+    "256-route blocks": [257, 256, 129, 128],                 # E = 4, top-2: 192.5 routes per expert
+}
 
 
 def _ids_with_counts(counts):
@@ -29,13 +34,15 @@ def _ids_with_counts(counts):
     return ids
 
 
-@pytest.mark.parametrize("mode", ["w4a16", "w4a8"])
-def test_block_boundaries_match_oracle(mode):
+@pytest.mark.parametrize("mode,blocks", [("w4a16", "128-route blocks"), ("w4a16", "256-route blocks"),
+                                         ("w4a8", "128-route blocks")])
+def test_block_boundaries_match_oracle(mode, blocks):
     import torch
     from trellis_quantized_moe_route_gb300.binding import TrellisMoE
-    ids = _ids_with_counts(COUNTS)
+    counts = COUNTS[blocks]
+    ids = _ids_with_counts(counts)
     T = ids.shape[0]
-    cfg = small_cfg(E=len(COUNTS), topk=2, T=T, seed=77)
+    cfg = small_cfg(E=len(counts), topk=2, T=T, seed=77)
     L = synth.make_layer(cfg)
     x_bits, _ = synth.make_tokens(cfg, T=T)
     rng = np.random.default_rng(5)

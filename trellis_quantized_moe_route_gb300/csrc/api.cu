@@ -241,7 +241,13 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
   // Outside the decode regime FC1 and FC2 run on the tcgen05 kernels (W4A16,
   // route blocks of up to 256 routes).
   const bool split = d.gate_suh != nullptr;  // separate gate / up input signs
-  const int bn = split ? 128 : tmoe::tc_route_block();
+  // Route blocks of 128 routes give every unit one tensor-memory accumulator,
+  // so a unit's epilogue overlaps the next unit's contraction; blocks of 256
+  // expand each weight once for up to 256 routes. Measured on one GB300:
+  // with 128 routes per expert on average (Zipf prefill) the 128-route blocks
+  // win (step 236 -> 221 us), with 205 (the large layer) the 256-route ones
+  // (FC1 1.14 vs 1.96 ms).
+  const int bn = (split || R <= 128L * d.E) ? 128 : tmoe::tc_route_block();
   cudaError_t e;
   uint32_t* err = at<uint32_t>(ws, L, Layout::ERR);
   if (logits) {
