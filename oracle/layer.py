@@ -15,6 +15,10 @@ the top-k sum):
   4. y2 = s2 (.) (W2~ z~)                           FC2
   5. y_t = sum_j w_{t,j} * (svh_d (.) Hblk_H(y2_{t,j}))   unrotate + top-k combine
 
+TrellisMX-style weights (a layer with UE8M0 weight scales; see
+expert_weights) keep the same steps; their hidden-side rotation blocks may be
+512 wide (H4 (x) H128 in Sylvester order, the "coupled H512/H128 boundary").
+
 Modes:
   * "w4a16": weights are the fp16 codebook values; x~ and z~ are rounded to
     fp16 (the operands of an FP16 x FP16 -> FP32 contraction). Reading: the
@@ -44,14 +48,33 @@ def fp16_to_f64(bits: np.ndarray) -> np.ndarray:
     return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
 
 
+def weight_scales(layer, proj: int, e: int):
+    """The UE8M0 weight scale bytes of expert e's projection ([rows, cols/32]),
+    or None for a layer without them (TrellisMX-style weights only)."""
+    ws = getattr(layer, "fc1_wscale" if proj == 1 else "fc2_wscale", None)
+    return None if ws is None else np.asarray(ws)[e]
+
+
 def expert_weights(layer, proj: int, e: int, mode: str = "w4a16") -> np.ndarray:
-    """Dense float64 weights of expert e: proj 1 -> [2I, H], proj 2 -> [H, I]."""
+    """Dense float64 weights of expert e: proj 1 -> [2I, H], proj 2 -> [H, I].
+
+    Plain trellis weights are the fp16 codebook values (W4A16), rounded to
+    E4M3 in W4A8. TrellisMX-style weights (the layer carries fc1_wscale /
+    fc2_wscale) decode to E4M3 in both modes and carry one UE8M0 scale per
+    32 consecutive weights of a row along the contraction axis (flashinfer PR
+    #69 "b12x fused MoE: TrellisMX ...", Description: trellis streams of K2
+    to K4 bits that decode to E4M3, one UE8M0 scale per 32 weights):
+    w = E4M3(cb(s)) * 2^(u - 127)."""
     rows, cols = (2 * layer.I, layer.H) if proj == 1 else (layer.H, layer.I)
     payload = layer.fc1_payload if proj == 1 else layer.fc2_payload
     tiles = trellis.expert_payload(payload, rows, cols, layer.bits, e)
     w = trellis.decode_matrix(tiles, int(layer.bits[e])).astype(np.float64)
-    if mode == "w4a8":
+    u = weight_scales(layer, proj, e)
+    if mode == "w4a8" or u is not None:
         w = mxfp8.e4m3_round(w)
+    if u is not None:
+        u = np.asarray(u, dtype=np.int64).reshape(rows, cols // 32)
+        w = w * np.exp2(np.repeat(u - 127, 32, axis=1).astype(np.float64))
     return w
 
 

@@ -12,14 +12,15 @@ platform and numpy version. Uniform and normal variates are derived from the
 raw words here (53-bit uniforms, Box-Muller normals) instead of through
 ``Generator`` methods, whose streams numpy does not promise to keep stable.
 
-Recipe (the five workloads named in ``CONFIGS``):
+Recipe (the workloads named in ``CONFIGS``):
   * payload: uniform random int16 words, 16*K words per 256-weight tile;
   * per-channel scales: fp16 of U[0.01, 0.03];
   * rotation sign vectors (input suh, gate/up svh, down suh, output svh): +-1 fp16;
   * activations: bf16 of N(0, 1);
   * router logits: N(0, sigma^2), or a Zipf(s) expert preference plus
     Gumbel(0, 1) noise, which makes top-k selection sample experts without
-    replacement with probability proportional to rank^-s.
+    replacement with probability proportional to rank^-s;
+  * TrellisMX-style weight scales: UE8M0 bytes 127 + k, k uniform in [-3, 3].
 """
 from __future__ import annotations
 
@@ -35,6 +36,7 @@ _S_BITS, _S_FC1, _S_FC2, _S_S1, _S_S2, _S_SUH, _S_ROT, _S_SVH = range(8)
 _S_X, _S_LOGITS, _S_PERM, _S_GUMBEL = 100, 101, 102, 103
 _S_LIN_W, _S_LIN_S, _S_LIN_SUH, _S_LIN_SVH, _S_LIN_X = 300, 301, 302, 303, 304
 _S_GATE_SUH, _S_UP_SUH = 400, 401
+_S_WS1, _S_WS2 = 500, 501
 
 
 @dataclasses.dataclass(frozen=True)
@@ -55,6 +57,7 @@ class LayerConfig:
     logit_sigma: float = 1.0
     zipf_s: float = 1.1
     seed: int = 0
+    mx: bool = False   # TrellisMX-style weights: UE8M0 scale bytes per 32 weights
 
 
 CONFIGS = {
@@ -73,6 +76,11 @@ CONFIGS = {
     "large": LayerConfig("large", E=160, H=5120, I=1536, topk=8, T=4096, bits=(4,),
                          rot_block_h=128, rot_block_i=128, mode="w4a16",
                          logits="normal", logit_sigma=1.0, seed=4),
+    # TrellisMX-style decode layer: K2-K4 per expert, E4M3 weights with one
+    # UE8M0 scale per 32 weights, 512-point hidden-side rotation blocks
+    "trellismx": LayerConfig("trellismx", E=64, H=2048, I=512, topk=8, T=8, bits=(2, 3, 4),
+                             rot_block_h=512, rot_block_i=128, mode="w4a8",
+                             logits="normal", logit_sigma=1.0, seed=5, mx=True),
 }
 
 
@@ -159,6 +167,10 @@ class Layer:
     # (shared by the experts) or [E, H] (per expert); None = in_suh for both
     gate_suh: Optional[np.ndarray] = None
     up_suh: Optional[np.ndarray] = None
+    # optional TrellisMX-style weight scales: UE8M0 bytes, one per 32 weights
+    # of a row along the contraction axis: [E, 2I, H/32] and [E, H, I/32]
+    fc1_wscale: Optional[np.ndarray] = None
+    fc2_wscale: Optional[np.ndarray] = None
 
 
 def make_layer(cfg: LayerConfig, seed: Optional[int] = None,
@@ -193,7 +205,15 @@ def make_layer(cfg: LayerConfig, seed: Optional[int] = None,
         in_suh=_signs(Stream(seed, _S_SUH), H),
         rot_tab=_signs(Stream(seed, _S_ROT), E * 3 * I).reshape(E, 3 * I),
         out_svh=_signs(Stream(seed, _S_SVH), E * H).reshape(E, H),
+        fc1_wscale=_ue8m0(Stream(seed, _S_WS1), (E, 2 * I, H // 32)) if cfg.mx else None,
+        fc2_wscale=_ue8m0(Stream(seed, _S_WS2), (E, H, I // 32)) if cfg.mx else None,
     )
+
+
+def _ue8m0(stream: Stream, shape) -> np.ndarray:
+    """UE8M0 scale bytes 127 + k with k uniform in [-3, 3]."""
+    n = int(np.prod(shape))
+    return (124 + stream.below(n, 7)).astype(np.uint8).reshape(shape)
 
 
 def make_tokens(cfg: LayerConfig, T: Optional[int] = None, seed: Optional[int] = None):
