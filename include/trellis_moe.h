@@ -85,7 +85,10 @@ typedef struct {
   int32_t H;              /* hidden size, multiple of 128 */
   int32_t I;              /* intermediate size per half, multiple of 64 */
   int32_t topk;           /* experts per token, 1..min(E, 32) */
-  int32_t rot_block_h;    /* Hadamard block on H: 1 (identity), 64 or 128 */
+  int32_t rot_block_h;    /* Hadamard block on H: 1 (identity), 64, 128, or 512 (H4 (x) H128 in
+                             Sylvester order, the coupled H512/H128 boundary of TrellisMX-style
+                             layers; H a multiple of 512; the output side then always takes the
+                             ordered combine) */
   int32_t rot_block_i;    /* Hadamard block on I: 1, 64 or 128 (must divide I) */
   const uint8_t* bits_per_expert; /* HOST [E], trellis bits K_e in 2..6 */
   /* Payload words, experts concatenated in order. Expert e's FC1 block is
@@ -116,6 +119,18 @@ typedef struct {
   const uint16_t* gate_suh;
   const uint16_t* up_suh;
   int32_t input_sign_rows;
+  /* Optional TrellisMX-style weight scales (flashinfer PR #69 "b12x fused
+   * MoE: TrellisMX ...", Description: trellis streams that decode to E4M3,
+   * one UE8M0 scale per 32 weights). Both NULL: plain trellis weights. Both
+   * set: UE8M0 bytes u, one per 32 consecutive weights of a row along the
+   * contraction axis, fc1_wscale [E][2I][H/32] and fc2_wscale [E][H][I/32]
+   * (16-byte aligned); every weight is then E4M3(cb(s)) * 2^(u - 127) in both
+   * modes. prepare reads them once and requires u - 127 in [-15, 13], the
+   * range in which the tensor-core path's fp16 operands hold the weights
+   * exactly (TM_EUNSUPPORTED otherwise). Such layers expand by the codebook
+   * hash (set_decode_lut has no effect on them). */
+  const uint8_t* fc1_wscale;
+  const uint8_t* fc2_wscale;
 } tm_layer_desc;
 
 /* Validate `desc`, upload the per-expert offset tables and return a handle and

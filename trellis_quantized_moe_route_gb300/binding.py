@@ -47,6 +47,7 @@ class LayerDesc(ctypes.Structure):
         ("in_suh", ctypes.c_void_p), ("rot_tab", ctypes.c_void_p), ("out_svh", ctypes.c_void_p),
         ("max_tokens", ctypes.c_int32), ("decode_max_rows", ctypes.c_int32), ("deterministic", ctypes.c_int32),
         ("gate_suh", ctypes.c_void_p), ("up_suh", ctypes.c_void_p), ("input_sign_rows", ctypes.c_int32),
+        ("fc1_wscale", ctypes.c_void_p), ("fc2_wscale", ctypes.c_void_p),
     ]
 
 
@@ -143,6 +144,12 @@ def _ptr(t) -> ctypes.c_void_p:
     return ctypes.c_void_p(t.data_ptr())
 
 
+def to_device_u8(arr: np.ndarray):
+    """Upload a uint8 numpy array as a uint8 CUDA tensor."""
+    torch = _torch()
+    return torch.from_numpy(np.ascontiguousarray(np.asarray(arr, dtype=np.uint8))).cuda()
+
+
 def to_device_u16(arr: np.ndarray):
     """Upload a uint16 / int16 numpy array as an int16 CUDA tensor."""
     torch = _torch()
@@ -203,6 +210,11 @@ class TrellisMoE:
             raise ValueError("gate_suh and up_suh must be given together")
         self.gate_suh = to_device_u16(np.asarray(g).reshape(-1, self.H)) if g is not None else None
         self.up_suh = to_device_u16(np.asarray(u).reshape(-1, self.H)) if u is not None else None
+        w1, w2 = getattr(layer, "fc1_wscale", None), getattr(layer, "fc2_wscale", None)
+        if (w1 is None) != (w2 is None):
+            raise ValueError("fc1_wscale and fc2_wscale must be given together")
+        self.fc1_wscale = to_device_u8(w1) if w1 is not None else None
+        self.fc2_wscale = to_device_u8(w2) if w2 is not None else None
         d = LayerDesc()
         d.E, d.H, d.I, d.topk = self.E, self.H, self.I, self.topk
         d.rot_block_h, d.rot_block_i = int(layer.rot_block_h), int(layer.rot_block_i)
@@ -223,6 +235,9 @@ class TrellisMoE:
             d.gate_suh = self.gate_suh.data_ptr()
             d.up_suh = self.up_suh.data_ptr()
             d.input_sign_rows = int(self.gate_suh.shape[0])
+        if self.fc1_wscale is not None:
+            d.fc1_wscale = self.fc1_wscale.data_ptr()
+            d.fc2_wscale = self.fc2_wscale.data_ptr()
         self.desc = d
         handle = ctypes.c_void_p()
         ws = ctypes.c_size_t()

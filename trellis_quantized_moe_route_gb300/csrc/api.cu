@@ -116,7 +116,7 @@ DecPlan dec_plan(const tm_layer_desc& d, int T, bool w4a8) {
   p.use = R >= 1 && R <= kDecMaxRoutes && (w4a8 || R < 4L * d.E);
   p.bi = fc1_bi(d);
   p.units1 = d.I / p.bi;
-  p.units2 = d.H / 128;
+  p.units2 = d.H / (d.rot_block_h > 128 ? 512 : 128);  // FC2 epilogue: one CTA per token x rotation span
   p.max_blocks = (int)(R / tmoe::kDecBlock + std::min<long>(d.E, R) + 1);
   p.nseg1 = (d.H + tmoe::kDecSeg - 1) / tmoe::kDecSeg;
   p.nseg2 = (d.I + tmoe::kDecSeg - 1) / tmoe::kDecSeg;
@@ -216,6 +216,9 @@ P* at(void* ws, const Layout& L, int region) {
 }
 
 bool pow2_block_ok(int b) { return b == 1 || b == 64 || b == 128; }
+// Hidden-side blocks may also be 512 wide (the coupled H512 boundary of
+// TrellisMX-style layers).
+bool h_block_ok(int b, int H) { return pow2_block_ok(b) || (b == 512 && H % 512 == 0); }
 
 tm_status check_ws(const tm_layer* layer, int T, void* ws, size_t bytes, Layout* out) {
   if (T > layer->desc.max_tokens) return fail(TM_EINVAL, "T=%d exceeds prepared max_tokens=%d", T, layer->desc.max_tokens);
@@ -322,6 +325,9 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
   a1.nblocks = rm.nblocks;
   a1.out_act = at<void>(ws, L, Layout::ZQ);
   a1.out_scale = at<uint8_t>(ws, L, Layout::ZS);
+  a1.wscale = d.fc1_wscale;
+  a1.wrows = 2 * d.I;
+  a1.wcols = d.H / 32;
   tmoe::TcArgs t1{};
   t1.f = a1;
   t1.bi = layer->bi;
@@ -346,7 +352,11 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
   a2.out_act = nullptr;
   a2.out_scale = nullptr;
   a2.route_w = w;
-  a2.atomic = d.deterministic ? 0 : 1;
+  a2.wscale = d.fc2_wscale;
+  a2.wrows = d.H;
+  a2.wcols = d.I / 32;
+  // (512-point output rotations always take the ordered combine)
+  a2.atomic = (d.deterministic || d.rot_block_h > 128) ? 0 : 1;
   // the tensor-core FC2 leaves the route's output scale, H and down_svh to the combine
   a2.raw_rows = (!a2.atomic && d.topk <= 32) ? 1 : 0;
   if (a2.atomic) {
@@ -491,8 +501,12 @@ tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids
   d1.out = out;
   d1.T = T;
   d1.max_blocks = dp.max_blocks;
-  d1.lut = layer->use_lut ? layer->d_lut + (w4a8 ? 65536 : 0) : nullptr;
-  if ((e = tmoe::dec_fc_warps(1, w4a8, layer->uniform_k, d1.lut != nullptr, &d1.fc_warps)) != cudaSuccess)
+  a1.wscale = d.fc1_wscale;
+  a1.wrows = 2 * d.I;
+  a1.wcols = d.H / 32;
+  const bool mx = d.fc1_wscale != nullptr;  // (TrellisMX-style weights expand by the hash)
+  d1.lut = (layer->use_lut && !mx) ? layer->d_lut + (w4a8 ? 65536 : 0) : nullptr;
+  if ((e = tmoe::dec_fc_warps(1, w4a8, layer->uniform_k, d1.lut != nullptr, mx, &d1.fc_warps)) != cudaSuccess)
     return cuda_fail(e, "FC1 (decode rows) setup");
   if ((e = tmoe::launch_dec_fc(d1, 1, w4a8, layer->uniform_k, st)) != cudaSuccess)
     return cuda_fail(e, "FC1 (decode rows)");
@@ -517,11 +531,14 @@ tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids
   a2.out_act = nullptr;
   a2.out_scale = nullptr;
   a2.out_f32 = at<float>(ws, L, Layout::ROWS);
+  a2.wscale = d.fc2_wscale;
+  a2.wrows = d.H;
+  a2.wcols = d.I / 32;
   d2.nseg = dp.nseg2;
   d2.act_scaled = d1.out_act_scaled;
   d2.units_m = dp.units2;
   d2.blk_off = pa.blk_off2;
-  if ((e = tmoe::dec_fc_warps(2, w4a8, layer->uniform_k, d2.lut != nullptr, &d2.fc_warps)) != cudaSuccess)
+  if ((e = tmoe::dec_fc_warps(2, w4a8, layer->uniform_k, d2.lut != nullptr, mx, &d2.fc_warps)) != cudaSuccess)
     return cuda_fail(e, "FC2 (decode rows) setup");
   if ((e = tmoe::launch_dec_fc(d2, 2, w4a8, layer->uniform_k, st)) != cudaSuccess)
     return cuda_fail(e, "FC2 (decode rows)");
@@ -552,8 +569,8 @@ tm_status trellis_moe_prepare(const tm_layer_desc* desc, tm_layer** out, size_t*
   if (d.H < 128 || d.H % 128 != 0) return fail(TM_EUNSUPPORTED, "H=%d must be a positive multiple of 128", d.H);
   if (d.I < 64 || d.I % 64 != 0) return fail(TM_EUNSUPPORTED, "I=%d must be a positive multiple of 64", d.I);
   if (d.topk < 1 || d.topk > 32 || d.topk > d.E) return fail(TM_EINVAL, "topk=%d outside 1..min(E,32)", d.topk);
-  if (!pow2_block_ok(d.rot_block_h) || d.H % d.rot_block_h != 0)
-    return fail(TM_EUNSUPPORTED, "rot_block_h=%d must be 1, 64 or 128 and divide H", d.rot_block_h);
+  if (!h_block_ok(d.rot_block_h, d.H) || d.H % d.rot_block_h != 0)
+    return fail(TM_EUNSUPPORTED, "rot_block_h=%d must be 1, 64, 128 or 512 and divide H", d.rot_block_h);
   if (!pow2_block_ok(d.rot_block_i) || d.I % d.rot_block_i != 0)
     return fail(TM_EUNSUPPORTED, "rot_block_i=%d must be 1, 64 or 128 and divide I", d.rot_block_i);
   if (d.max_tokens < 1) return fail(TM_EINVAL, "max_tokens=%d must be >= 1", d.max_tokens);
@@ -573,6 +590,26 @@ tm_status trellis_moe_prepare(const tm_layer_desc* desc, tm_layer** out, size_t*
   for (int i = 0; i < 8; ++i) {
     if (!ptrs[i]) return fail(TM_EINVAL, "%s is NULL", names[i]);
     if (((uintptr_t)ptrs[i]) % 16 != 0) return fail(TM_EINVAL, "%s must be 16-byte aligned", names[i]);
+  }
+  if ((d.fc1_wscale != nullptr) != (d.fc2_wscale != nullptr))
+    return fail(TM_EINVAL, "fc1_wscale and fc2_wscale must be given together");
+  if (d.fc1_wscale && (((uintptr_t)d.fc1_wscale) % 16 || ((uintptr_t)d.fc2_wscale) % 16))
+    return fail(TM_EINVAL, "fc1_wscale and fc2_wscale must be 16-byte aligned");
+  if (d.fc1_wscale) {
+    // every scale exponent within [-15, 13]: E4M3(cb) * 2^k is then an exact
+    // fp16 value (|E4M3(cb)| <= 4), as the tensor-core path holds it
+    const size_t n1 = (size_t)d.E * 2 * d.I * (d.H / 32), n2 = (size_t)d.E * d.H * (d.I / 32);
+    std::vector<uint8_t> h(std::max(n1, n2));
+    const uint8_t* src[2] = {d.fc1_wscale, d.fc2_wscale};
+    const size_t cnt[2] = {n1, n2};
+    for (int i = 0; i < 2; ++i) {
+      cudaError_t e = cudaMemcpy(h.data(), src[i], cnt[i], cudaMemcpyDeviceToHost);
+      if (e != cudaSuccess) return cuda_fail(e, "read weight scales");
+      for (size_t j = 0; j < cnt[i]; ++j)
+        if (h[j] < 127 - 15 || h[j] > 127 + 13)
+          return fail(TM_EUNSUPPORTED, "fc%d_wscale[%zu] = %u: exponent %d outside [-15, 13]", i + 1, j, h[j],
+                      (int)h[j] - 127);
+    }
   }
   tm_layer* L = new tm_layer();
   L->desc = d;

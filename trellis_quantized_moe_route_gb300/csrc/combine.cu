@@ -109,8 +109,81 @@ __global__ void __launch_bounds__(256, 3) k_combine_unrot(CombineUnrotArgs a) {
   }
 }
 
+// The same for 512-point output rotation blocks (the coupled H512 boundary
+// of TrellisMX-style layers: flashinfer PR #69 "b12x fused MoE: TrellisMX
+// ...", Description): one warp per (token, 512 output channels); lane l (h =
+// l / 16, i = l % 16) holds, for each 128-column quarter b of the block,
+// channels 128 b + 64 h + 4 i .. +3. The remaining levels: across the halves
+// (64) with the partner lane l ^ 16, across quarters (128 and 256) in
+// registers; then hs * down_svh and w * that into the FP32 sum, routes in
+// ascending j.
+__global__ void __launch_bounds__(256) k_combine_unrot512(CombineUnrotArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int chunks = a.H >> 9;
+  const long wid = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (wid >= (long)a.T * chunks) return;
+  const int t = (int)(wid / chunks);
+  const int hb = lane >> 4;
+  const int c0 = (int)(wid % chunks) * 512 + 64 * hb + 4 * (lane & 15);
+  int my_slot = -1, my_e = 0;
+  float my_w = 0.0f;
+  if (lane < a.k) {
+    my_slot = a.slot_of_route[(size_t)t * a.k + lane];
+    my_w = a.w[(size_t)t * a.k + lane];
+    if (my_slot >= 0) my_e = a.block_expert[my_slot / a.bn];
+  }
+  const float hs = hadamard_scale(512);
+  float4 acc[4];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) acc[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < a.k; ++j) {
+    const int slot = __shfl_sync(0xFFFFFFFFu, my_slot, j);
+    const float wj = __shfl_sync(0xFFFFFFFFu, my_w, j);
+    const int e = __shfl_sync(0xFFFFFFFFu, my_e, j);
+    if (slot < 0) continue;  // warp-uniform: a dropped (out-of-range) expert id has no slot
+    float4 v[4];
+    uint2 g[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      v[b] = __ldcs(reinterpret_cast<const float4*>(a.rows + (size_t)slot * a.H + c0 + 128 * b));
+      g[b] = __ldg(reinterpret_cast<const uint2*>(a.svh + (size_t)e * a.H + c0 + 128 * b));
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {  // level 64: the lower half keeps x + x', the upper x' - x
+      const float4 o = make_float4(__shfl_xor_sync(0xFFFFFFFFu, v[b].x, 16), __shfl_xor_sync(0xFFFFFFFFu, v[b].y, 16),
+                                   __shfl_xor_sync(0xFFFFFFFFu, v[b].z, 16), __shfl_xor_sync(0xFFFFFFFFu, v[b].w, 16));
+      v[b] = hb ? make_float4(o.x - v[b].x, o.y - v[b].y, o.z - v[b].z, o.w - v[b].w)
+                : make_float4(v[b].x + o.x, v[b].y + o.y, v[b].z + o.z, v[b].w + o.w);
+    }
+#pragma unroll
+    for (int d = 1; d <= 2; d <<= 1) {  // levels 128 and 256 across the quarters
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        if (b & d) continue;
+        const float4 x = v[b], y = v[b + d];
+        v[b] = make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w);
+        v[b + d] = make_float4(x.x - y.x, x.y - y.y, x.z - y.z, x.w - y.w);
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float4 f = h4_to_f4(g[b]);
+      acc[b] = make_float4(fmaf(wj, v[b].x * (hs * f.x), acc[b].x), fmaf(wj, v[b].y * (hs * f.y), acc[b].y),
+                           fmaf(wj, v[b].z * (hs * f.z), acc[b].z), fmaf(wj, v[b].w * (hs * f.w), acc[b].w));
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < 4; ++b) *reinterpret_cast<float4*>(a.out + (size_t)t * a.H + c0 + 128 * b) = acc[b];
+}
+
 cudaError_t launch_combine_unrot(const CombineUnrotArgs& a, cudaStream_t st) {
   if (a.T == 0) return cudaSuccess;
+  if (a.rot_b == 512) {
+    if (a.H % 512 != 0 || a.k > kCombineMaxK) return cudaErrorInvalidValue;
+    const long warps = (long)a.T * (a.H / 512);
+    k_combine_unrot512<<<(int)((warps + 7) / 8), 256, 0, st>>>(a);
+    return cudaGetLastError();
+  }
   if (a.H % 128 != 0 || a.k > kCombineMaxK || a.rot_b > 128) return cudaErrorInvalidValue;
   const long warps = (long)a.T * ((a.H + 255) / 256);
   k_combine_unrot<<<(int)((warps + 7) / 8), 256, 0, st>>>(a);

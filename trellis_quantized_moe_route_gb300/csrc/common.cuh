@@ -286,12 +286,14 @@ __device__ __forceinline__ void warp_fwht_f64(double (&v)[PER], int B) {
 // 1/sqrt(B) in fp64, as 1 / fp64(sqrt(B)) rounds (0.08838834764831843 for
 // B = 128, the rotation matrix's entries in a float64 evaluation).
 __device__ __forceinline__ double hadamard_scale_f64(int B) {
-  return B == 128 ? 0.08838834764831843 : (B == 64 ? 0.125 : (B == 32 ? 0.17677669529663687 : 1.0));
+  return B == 128 ? 0.08838834764831843
+                  : (B == 64 ? 0.125 : (B == 512 ? 0.04419417382415922 : (B == 32 ? 0.17677669529663687 : 1.0)));
 }
 
 __device__ __forceinline__ float hadamard_scale(int B) {
   // 1/sqrt(B) rounded to fp32 (B = 128: 0.088388347648...)
-  return B == 128 ? 0.08838834764831845f : (B == 64 ? 0.125f : (B == 32 ? 0.17677669529663687f : 1.0f));
+  return B == 128 ? 0.08838834764831845f
+                  : (B == 64 ? 0.125f : (B == 512 ? 0.044194173824159216f : (B == 32 ? 0.17677669529663687f : 1.0f)));
 }
 
 // UE8M0 exponent of a block from its max |v|: e = ceil(log2(fp32(amax/448))),

@@ -23,7 +23,8 @@ __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.
 // Prologue. CTA 0: router (when logits are given) and the route map for R <=
 // 1024 routes (one per thread), held in shared memory from the ranks to the
 // route-block table; the other CTAs: rotate+quantize (one warp per token x
-// 128 columns), clearing of counters and output.
+// chunk of 128 columns, 512 with 512-point rotation blocks), clearing of
+// counters and output.
 // ---------------------------------------------------------------------------
 struct DecRouteSmem {
   int cnt[32][kMaxExperts];  // per-warp counts, then per-warp bases within the expert
@@ -133,6 +134,24 @@ __device__ __forceinline__ void dec_route_map(const DecPrologueArgs& a, DecRoute
   }
 }
 
+// The prologue's rotation of warp gw (PER values per lane: rot_per).
+template <int PER>
+__device__ __forceinline__ void dec_rotate(const DecPrologueArgs& a, int gw) {
+  if (a.split_signs) {
+    // one gate and one up rotation per route (their rows indexed by route);
+    // with logits the warp selects its token's experts itself, as CTA 0 does
+    if (a.w4a8)
+      rotate_routes_warp<true, PER>(a.rr, gw);
+    else
+      rotate_routes_warp<false, PER>(a.rr, gw);
+  } else if (a.w4a8) {
+    rotate_quant_warp<true, PER>(a.x, a.suh, a.T, a.H, a.rot_b, a.xq, a.xs, gw, nullptr, 0, true, a.xq_scaled);
+  } else {
+    rotate_quant_warp<false, PER>(a.x, a.suh, a.T, a.H, a.rot_b, a.xq, a.xs, gw);
+  }
+}
+
+template <int PER>
 __global__ void __launch_bounds__(1024) k_dec_prologue(const DecPrologueArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5;
   griddep_launch();  // FC1's CTAs may take free SMs now; they wait for this grid to finish
@@ -144,28 +163,35 @@ __global__ void __launch_bounds__(1024) k_dec_prologue(const DecPrologueArgs a) 
   }
   const int nrot = gridDim.x - 1;
   const int cta = blockIdx.x - 1;
-  const int gw = cta * 32 + warp;
-  if (a.split_signs) {
-    // one gate and one up rotation per route (their rows indexed by route);
-    // with logits the warp selects its token's experts itself, as CTA 0 does
-    if (a.w4a8)
-      rotate_routes_warp<true>(a.rr, gw);
-    else
-      rotate_routes_warp<false>(a.rr, gw);
-  } else if (a.w4a8) {
-    rotate_quant_warp<true>(a.x, a.suh, a.T, a.H, a.rot_b, a.xq, a.xs, gw, nullptr, 0, true, a.xq_scaled);
-  } else {
-    rotate_quant_warp<false>(a.x, a.suh, a.T, a.H, a.rot_b, a.xq, a.xs, gw);
-  }
+  // a.rot_per rotation warps per CTA, so that the W4A8 rotation's fp64
+  // butterflies spread over many SMs' fp64 units
+  const int gw = (warp < a.rot_per) ? cta * a.rot_per + warp : 0x7FFFFFFF;
+  dec_rotate<PER>(a, gw);
   const long gtid = (long)cta * blockDim.x + tid, gstride = (long)nrot * blockDim.x;
   for (long i = gtid; i < a.n_zero_i32; i += gstride) a.zero_i32[i] = 0;
   for (long i = gtid; i < a.out_n / 4; i += gstride) reinterpret_cast<float4*>(a.out)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-cudaError_t launch_dec_prologue(const DecPrologueArgs& a, cudaStream_t st) {
-  const long warps = (long)a.T * (a.H / 128);
-  const int nrot = (int)std::max<long>(1, (warps + 31) / 32);
-  k_dec_prologue<<<1 + nrot, 1024, 0, st>>>(a);
+cudaError_t launch_dec_prologue(const DecPrologueArgs& a_in, cudaStream_t st) {
+  // one rotation warp per CTA while the SMs last (T*H/128 warps), then more
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  DecPrologueArgs a = a_in;
+  const long warps = (long)a.T * (a.H / (32 * rot_per(a.rot_b)));
+  const long slots = std::max(1, sms - 1);
+  a.rot_per = (int)std::min<long>(32, std::max<long>(1, (warps + slots - 1) / slots));
+  const int nrot = (int)std::max<long>(1, (warps + a.rot_per - 1) / a.rot_per);
+  // (one kernel per rotation width, so that the 512-point variant's
+  // registers do not constrain the common one)
+  if (a.rot_b > 128)
+    k_dec_prologue<16><<<1 + nrot, 1024, 0, st>>>(a);
+  else
+    k_dec_prologue<4><<<1 + nrot, 1024, 0, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -233,7 +233,10 @@ constexpr int kDwLutRuns = 2;
 // PRE (W4A8): the activations are read as code * 2^e, so the MMAs accumulate
 // straight into acc with no per-block scaling (every block of the item has
 // its exponent in [-15, 7]; see dw_pre_issue).
-template <bool W4A8, bool PRE, int K, bool LUT>
+// MX (TrellisMX-style weights): the weights are E4M3-rounded in both modes
+// and every 32-column block of a weight row carries a UE8M0 scale, applied
+// to that k-step's MMA result per row (exact powers of two in fp32).
+template <bool W4A8, bool PRE, int K, bool LUT, bool MX>
 __device__ __forceinline__ void dw_compute(const DecArgs& d, const DwItem& it, int row,
                                            const unsigned char* wt, const uint16_t* lut, int kdim, float (&acc)[4]) {
   const FcArgs& a = d.f;
@@ -253,6 +256,9 @@ __device__ __forceinline__ void dw_compute(const DecArgs& d, const DwItem& it, i
   const uint8_t* sp1 = src.scale + (size_t)(r1 < 0 ? 0 : r1) * (kdim >> 5) + (col0 >> 5);
   const uint32_t k16 = 0x10000u + (uint32_t)(d.T >> 30);  // 65536, opaque to the compiler
   const uint32_t nk16 = 0u - k16;
+  // MX: the UE8M0 bytes of weight rows 16 strip + g and + 8 for this segment
+  const uint8_t* wsg = nullptr;
+  if (MX) wsg = a.wscale + ((size_t)it.e * a.wrows + 16 * it.strip + g) * a.wcols + (col0 >> 5);
   const int swz = 64 * tsel;
   const int oc0 = (4 * (2 * g + h)) ^ swz, op0 = (4 * ((2 * g + h + 31) & 31)) ^ swz;
   const int oc1 = (4 * (2 * g + 16 + h)) ^ swz, op1 = (4 * (2 * g + 15 + h)) ^ swz;
@@ -265,14 +271,26 @@ __device__ __forceinline__ void dw_compute(const DecArgs& d, const DwItem& it, i
       if (LUT)
         dw_run_lut<K>(tile, lut, g, h, oc0, op0, wa);
       else
-        dw_run_hash<W4A8, K>(tile, g, h, oc0, op0, k16, nk16, wa);
+        dw_run_hash<W4A8 || MX, K>(tile, g, h, oc0, op0, k16, nk16, wa);
       if (LUT && kDwLutRuns == 2)
         dw_run_lut<K>(tile, lut, g + 8, h, oc1, op1, wb);
       else
-        dw_run_hash<W4A8, K>(tile, g + 8, h, oc1, op1, k16, nk16, wb);
+        dw_run_hash<W4A8 || MX, K>(tile, g + 8, h, oc1, op1, k16, nk16, wb);
       const uint32_t a0[4] = {wa[0], wb[0], wa[1], wb[1]};
       const uint32_t a1[4] = {wa[2], wb[2], wa[3], wb[3]};
-      if (W4A8 && !PRE) {
+      if (MX) {
+        const float s0 = (W4A8 && !PRE) ? ((r0 >= 0) ? exp2_int((int)__ldg(sp0 + ks) - 127) : 0.0f) : 1.0f;
+        const float s1 = (W4A8 && !PRE) ? ((r1 >= 0) ? exp2_int((int)__ldg(sp1 + ks) - 127) : 0.0f) : 1.0f;
+        const float wg = exp2_int((int)__ldg(wsg + ks) - 127);
+        const float wg8 = exp2_int((int)__ldg(wsg + 8 * a.wcols + ks) - 127);
+        float dd[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f16_16816(dd, a0, bv.x, bv.y);
+        mma_f16_16816(dd, a1, bv.z, bv.w);
+        acc[0] = fmaf(dd[0], wg * s0, acc[0]);
+        acc[1] = fmaf(dd[1], wg * s1, acc[1]);
+        acc[2] = fmaf(dd[2], wg8 * s0, acc[2]);
+        acc[3] = fmaf(dd[3], wg8 * s1, acc[3]);
+      } else if (W4A8 && !PRE) {
         const float s0 = (r0 >= 0) ? exp2_int((int)__ldg(sp0 + ks) - 127) : 0.0f;
         const float s1 = (r1 >= 0) ? exp2_int((int)__ldg(sp1 + ks) - 127) : 0.0f;
         float dd[4] = {0.f, 0.f, 0.f, 0.f};
@@ -290,30 +308,30 @@ __device__ __forceinline__ void dw_compute(const DecArgs& d, const DwItem& it, i
   }
 }
 
-template <bool W4A8, bool PRE, int KB, bool LUT>
+template <bool W4A8, bool PRE, int KB, bool LUT, bool MX>
 __device__ __forceinline__ void dw_compute_k(const DecArgs& d, const DwItem& it, int row, const unsigned char* wt,
                                              const uint16_t* lut, int kdim, float (&acc)[4]) {
   if (KB > 0) {
-    dw_compute<W4A8, PRE, (KB > 0 ? KB : 4), LUT>(d, it, row, wt, lut, kdim, acc);
+    dw_compute<W4A8, PRE, (KB > 0 ? KB : 4), LUT, MX>(d, it, row, wt, lut, kdim, acc);
     return;
   }
   switch (it.k) {
-    case 2: dw_compute<W4A8, PRE, 2, LUT>(d, it, row, wt, lut, kdim, acc); break;
-    case 3: dw_compute<W4A8, PRE, 3, LUT>(d, it, row, wt, lut, kdim, acc); break;
-    case 4: dw_compute<W4A8, PRE, 4, LUT>(d, it, row, wt, lut, kdim, acc); break;
-    case 5: dw_compute<W4A8, PRE, 5, LUT>(d, it, row, wt, lut, kdim, acc); break;
-    default: dw_compute<W4A8, PRE, 6, LUT>(d, it, row, wt, lut, kdim, acc); break;
+    case 2: dw_compute<W4A8, PRE, 2, LUT, MX>(d, it, row, wt, lut, kdim, acc); break;
+    case 3: dw_compute<W4A8, PRE, 3, LUT, MX>(d, it, row, wt, lut, kdim, acc); break;
+    case 4: dw_compute<W4A8, PRE, 4, LUT, MX>(d, it, row, wt, lut, kdim, acc); break;
+    case 5: dw_compute<W4A8, PRE, 5, LUT, MX>(d, it, row, wt, lut, kdim, acc); break;
+    default: dw_compute<W4A8, PRE, 6, LUT, MX>(d, it, row, wt, lut, kdim, acc); break;
   }
 }
 
-template <bool W4A8, int KB, bool LUT>
+template <bool W4A8, int KB, bool LUT, bool MX>
 __device__ __forceinline__ void dw_compute_any(const DecArgs& d, const DwItem& it, bool pre, int row,
                                                const unsigned char* wt, const uint16_t* lut, int kdim,
                                                float (&acc)[4]) {
   if (W4A8 && pre)
-    dw_compute_k<W4A8, true, KB, LUT>(d, it, row, wt, lut, kdim, acc);
+    dw_compute_k<W4A8, true, KB, LUT, MX>(d, it, row, wt, lut, kdim, acc);
   else
-    dw_compute_k<W4A8, false, KB, LUT>(d, it, row, wt, lut, kdim, acc);
+    dw_compute_k<W4A8, false, KB, LUT, MX>(d, it, row, wt, lut, kdim, acc);
 }
 
 // W4A8: the E8M0 exponents an item reads (its valid slots x its 32-column
@@ -545,6 +563,82 @@ __device__ __forceinline__ void dw_epilogue_fc2(const DecArgs& d, int t, int mb,
   }
 }
 
+// The same for 512-point output rotation blocks (the coupled H512 boundary of
+// TrellisMX-style layers: flashinfer PR #69 "b12x fused MoE: TrellisMX ...",
+// Description): one CTA of kDwEpiWarps warps per (token t, 512 output columns
+// mb); lane l holds the 16 columns of strip (mb * 512 + 16 l) / 16; the
+// routes' rows sit in dynamic shared memory, [k][32 lanes][16] fp32.
+__device__ __forceinline__ void dw_epilogue_fc2_512(const DecArgs& d, int t, int mb, int nstrips, float* rows) {
+  const FcArgs& a = d.f;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h0 = mb * 512 + lane * 16;
+  const int strip = h0 >> 4;
+  const float hs = hadamard_scale(a.rot_b);
+  const int k = a.topk;
+  for (int j = warp; j < k; j += kDwEpiWarps) {
+    const int slot = d.slot_of_route[t * k + j];
+    const bool ok = slot >= 0;  // warp-uniform
+    const int e = ok ? d.ids[t * k + j] : 0;
+    float sc[16], sv[16], y[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float f[4];
+      dw_ld_h<4>(a.scale + (size_t)e * a.H + h0 + 4 * q, f);
+#pragma unroll
+      for (int p = 0; p < 4; ++p) sc[4 * q + p] = f[p];
+      dw_ld_h<4>(a.rot_tab + (size_t)e * a.H + h0 + 4 * q, f);
+#pragma unroll
+      for (int p = 0; p < 4; ++p) sv[4 * q + p] = f[p];
+    }
+    if (j == warp) dw_griddep_wait();  // the partial sums come from the predecessor
+#pragma unroll
+    for (int p = 0; p < 16; ++p) y[p] = 0.0f;
+    if (ok) {
+      const float wj = d.route_w[t * k + j];
+      const int rb = slot / kDecBlock, n = slot % kDecBlock;
+      for (int sg = 0; sg < d.nseg; ++sg) {  // the item's partial sums in segment order
+        const float4* p4 = reinterpret_cast<const float4*>(d.partial + ((size_t)(rb * d.nseg + sg) * nstrips + strip) * 128 + n * 16);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 v = __ldcg(p4 + q);
+          y[4 * q] += v.x;
+          y[4 * q + 1] += v.y;
+          y[4 * q + 2] += v.z;
+          y[4 * q + 3] += v.w;
+        }
+      }
+#pragma unroll
+      for (int p = 0; p < 16; ++p) y[p] *= sc[p];
+      warp_fwht<16>(y, a.rot_b);
+#pragma unroll
+      for (int p = 0; p < 16; ++p) y[p] = wj * (y[p] * hs * sv[p]);
+    }
+    float4* r4 = reinterpret_cast<float4*>(rows + ((size_t)j * 32 + lane) * 16);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) r4[q] = make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float acc[16];
+#pragma unroll
+    for (int p = 0; p < 16; ++p) acc[p] = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      const float4* r4 = reinterpret_cast<const float4*>(rows + ((size_t)j * 32 + lane) * 16);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 r = r4[q];
+        acc[4 * q] += r.x;
+        acc[4 * q + 1] += r.y;
+        acc[4 * q + 2] += r.z;
+        acc[4 * q + 3] += r.w;
+      }
+    }
+    float4* o4 = reinterpret_cast<float4*>(d.out + (size_t)t * a.H + h0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) o4[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // The kernel. Warp w of W takes items w, w + W, ..., so that the warps work
 // through the payload together, one window of W consecutive items at a time
@@ -555,7 +649,7 @@ __device__ __forceinline__ void dw_epilogue_fc2(const DecArgs& d, int t, int mb,
 // constant weights before it waits for its predecessor, so its first payload
 // copy overlaps the FC1 epilogue. Partial sums: per item, [slot][16 rows] fp32.
 // ---------------------------------------------------------------------------
-template <bool W4A8, int PROJ, int KB, bool LUT>
+template <bool W4A8, int PROJ, int KB, bool LUT, bool MX>
 __global__ void __launch_bounds__(dw_cta_warps(KB, LUT) * 32, LUT ? 1 : (KB > 0 ? 6 : 4)) k_dec_warp(const DecArgs d) {
   extern __shared__ __align__(128) unsigned char dw_smem[];
   constexpr int NW = dw_cta_warps(KB, LUT);
@@ -630,7 +724,7 @@ __global__ void __launch_bounds__(dw_cta_warps(KB, LUT) * 32, LUT ? 1 : (KB > 0 
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     const bool pre = W4A8 && dw_pre_final(pre_cur);
-    dw_compute_any<W4A8, KB, LUT>(d, it, pre, m.row, ring + (n & 1) * slot_bytes, lut, kdim, acc);
+    dw_compute_any<W4A8, KB, LUT, MX>(d, it, pre, m.row, ring + (n & 1) * slot_bytes, lut, kdim, acc);
 
     // partial sums of the valid slots, [slot][16 rows]
     const int g = lane >> 2, c = 2 * (lane & 3);
@@ -700,13 +794,13 @@ __global__ void __launch_bounds__(256) k_dec_epi(const DecArgs d) {
   }
 }
 
-template <bool W4A8, int PROJ, int KB, bool LUT>
+template <bool W4A8, int PROJ, int KB, bool LUT, bool MX = false>
 static cudaError_t dw_warps_t(int* warps) {
   // attributes and the resident-CTA count are fixed on the first call (before any capture)
   constexpr int NW = dw_cta_warps(KB, LUT);
   static int resident = 0;
   if (resident == 0) {
-    auto kern = k_dec_warp<W4A8, PROJ, KB, LUT>;
+    auto kern = k_dec_warp<W4A8, PROJ, KB, LUT, MX>;
     const int smem = dw_smem_bytes(KB > 0 ? KB : 6, LUT, NW);
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
@@ -722,7 +816,7 @@ static cudaError_t dw_warps_t(int* warps) {
   return cudaSuccess;
 }
 
-template <bool W4A8, int PROJ, int KB, bool LUT>
+template <bool W4A8, int PROJ, int KB, bool LUT, bool MX = false>
 static cudaError_t launch_dw_t(const DecArgs& d, cudaStream_t st) {
   constexpr int NW = dw_cta_warps(KB, LUT);
   if (d.fc_warps <= 0 || d.fc_warps % NW) return cudaErrorInvalidValue;
@@ -737,7 +831,39 @@ static cudaError_t launch_dw_t(const DecArgs& d, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_dec_warp<W4A8, PROJ, KB, LUT>, d);
+  return cudaLaunchKernelEx(&cfg, k_dec_warp<W4A8, PROJ, KB, LUT, MX>, d);
+}
+
+// FC2 epilogue for 512-point output rotation blocks: one CTA per (token,
+// 512 columns), the routes' rows in topk * 2 KB of dynamic shared memory.
+__global__ void __launch_bounds__(256) k_dec_epi512(const DecArgs d) {
+  extern __shared__ __align__(16) float dw_rows512[];
+  dw_griddep_launch();
+  const int mb = blockIdx.x % d.units_m;
+  const int t = blockIdx.x / d.units_m;
+  if (t >= d.T) return;  // (whole CTA)
+  dw_epilogue_fc2_512(d, t, mb, d.f.H >> 4, dw_rows512);
+}
+
+static cudaError_t launch_epi512(const DecArgs& d, cudaStream_t st) {
+  const int smem = d.f.topk * 32 * 16 * 4;
+  static bool attr_done = false;  // first call, before any capture
+  if (!attr_done) {
+    const cudaError_t err = cudaFuncSetAttribute(k_dec_epi512, cudaFuncAttributeMaxDynamicSharedMemorySize, 32 * 32 * 16 * 4);
+    if (err != cudaSuccess) return err;
+    attr_done = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((long)d.T * d.units_m));
+  cfg.blockDim = dim3(32 * kDwEpiWarps);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_dec_epi512, d);
 }
 
 template <bool W4A8, int PROJ>
@@ -757,6 +883,13 @@ static cudaError_t launch_epi_t(const DecArgs& d, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, k_dec_epi<W4A8, PROJ>, d);
 }
 
+// TrellisMX-style weights (scales present): the general-K, hash-expansion
+// kernels only.
+static cudaError_t dec_fc_warps_mx(int proj, bool w4a8, int* warps) {
+  if (proj == 1) return w4a8 ? dw_warps_t<true, 1, 0, false, true>(warps) : dw_warps_t<false, 1, 0, false, true>(warps);
+  return w4a8 ? dw_warps_t<true, 2, 0, false, true>(warps) : dw_warps_t<false, 2, 0, false, true>(warps);
+}
+
 template <bool LUT>
 static cudaError_t dec_fc_warps_t(int proj, bool w4a8, int uniform_k, int* warps) {
   const bool k4 = uniform_k == 4;
@@ -768,12 +901,14 @@ static cudaError_t dec_fc_warps_t(int proj, bool w4a8, int uniform_k, int* warps
   return k4 ? dw_warps_t<false, 2, 4, LUT>(warps) : dw_warps_t<false, 2, 0, LUT>(warps);
 }
 
-cudaError_t dec_fc_warps(int proj, bool w4a8, int uniform_k, bool lut, int* warps) {
+cudaError_t dec_fc_warps(int proj, bool w4a8, int uniform_k, bool lut, bool mx, int* warps) {
+  if (mx) return dec_fc_warps_mx(proj, w4a8, warps);
   return lut ? dec_fc_warps_t<true>(proj, w4a8, uniform_k, warps) : dec_fc_warps_t<false>(proj, w4a8, uniform_k, warps);
 }
 
 cudaError_t launch_dec_epilogue(const DecArgs& d, int proj, bool w4a8, cudaStream_t st) {
   if (proj == 1) return w4a8 ? launch_epi_t<true, 1>(d, st) : launch_epi_t<false, 1>(d, st);
+  if (d.f.rot_b > 128) return launch_epi512(d, st);  // (units_m = H / 512)
   return w4a8 ? launch_epi_t<true, 2>(d, st) : launch_epi_t<false, 2>(d, st);
 }
 
@@ -789,6 +924,10 @@ static cudaError_t launch_dec_fc_t(const DecArgs& d, int proj, bool w4a8, int un
 }
 
 cudaError_t launch_dec_fc(const DecArgs& d, int proj, bool w4a8, int uniform_k, cudaStream_t st) {
+  if (d.f.wscale) {
+    if (proj == 1) return w4a8 ? launch_dw_t<true, 1, 0, false, true>(d, st) : launch_dw_t<false, 1, 0, false, true>(d, st);
+    return w4a8 ? launch_dw_t<true, 2, 0, false, true>(d, st) : launch_dw_t<false, 2, 0, false, true>(d, st);
+  }
   return d.lut ? launch_dec_fc_t<true>(d, proj, w4a8, uniform_k, st) : launch_dec_fc_t<false>(d, proj, w4a8, uniform_k, st);
 }
 

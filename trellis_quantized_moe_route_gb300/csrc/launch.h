@@ -45,6 +45,10 @@ struct FcArgs {
   const float* route_w;       // FC2 atomic: route weights [T*topk]
   int atomic;
   int raw_rows;               // FC2 (tensor-core kernel, not atomic): rows leave the last Hadamard level and down_svh to the combine
+  // TrellisMX-style weights: UE8M0 bytes of this projection, [E][wrows][wcols]
+  // (one per 32 weights of a row along the contraction axis), or NULL
+  const uint8_t* wscale;
+  int wrows, wcols;
 };
 
 // Separate gate / up input signs (one row shared by the experts, or one row
@@ -101,6 +105,7 @@ struct DecPrologueArgs {
   long long* blk_off2;
   int split_signs;          // separate gate / up input signs: rotate per route with `rr` (rows = routes)
   RouteRotArgs rr;
+  int rot_per;              // rotation warps per rotation CTA (set by launch_dec_prologue)
 };
 
 constexpr int kDecSeg = 256;  // contraction columns of one decode-rows item
@@ -136,7 +141,7 @@ struct DecArgs {
 cudaError_t launch_dec_prologue(const DecPrologueArgs& a, cudaStream_t st);
 // Warps of the decode-rows FC kernel's grid (all resident: CTAs per SM x SMs);
 // fixed on the first call, which also sets the kernel's attributes.
-cudaError_t dec_fc_warps(int proj, bool w4a8, int uniform_k, bool lut, int* warps);
+cudaError_t dec_fc_warps(int proj, bool w4a8, int uniform_k, bool lut, bool mx, int* warps);
 // Codebook tables for the lookup variant: decode_lut_bytes() bytes, built on `st`.
 size_t decode_lut_bytes();
 cudaError_t build_decode_lut(uint16_t* lut, cudaStream_t st);

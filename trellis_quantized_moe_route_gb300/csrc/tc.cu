@@ -134,6 +134,27 @@ __device__ __forceinline__ void run_window_smem(const uint16_t* tile, int j0, ui
   lo = (w2 << 16) | w3;
 }
 
+// 2^(u - 127) as an fp16 pair for a UE8M0 byte u with u - 127 in [-15, 13]
+// (the prepared layer guarantees the range; 2^-15 is an fp16 subnormal).
+__device__ __forceinline__ uint32_t ue8m0_half2(uint32_t u) {
+  const int k = (int)u - 127;
+  const uint32_t h = (k >= -14) ? ((uint32_t)(k + 15) << 10) : 0x0200u;
+  return h | (h << 16);
+}
+
+// TrellisMX-style weights for the fp16 contraction: each codebook value
+// rounded to E4M3, times its block's power of two. Both steps are exact in
+// fp16 (E4M3 values carry 4 significant bits, |E4M3(cb)| <= 4 and the
+// exponent lies in [-15, 13]).
+__device__ __forceinline__ void mx_scale(uint32_t (&w)[4], uint32_t f2) {
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const uint32_t q = e4m3x2_to_f16x2(cvt_e4m3x2(w[p]));
+    __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&q), *reinterpret_cast<const __half2*>(&f2));
+    w[p] = *reinterpret_cast<uint32_t*>(&r);
+  }
+}
+
 __device__ __forceinline__ void sts128(unsigned char* p, const uint32_t (&w)[4]) {
   *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
@@ -143,9 +164,11 @@ __device__ __forceinline__ void sts128(unsigned char* p, const uint32_t (&w)[4])
 // into the swizzled operand `bsl`. Thread t takes row t % NR and 8 * NR / 256
 // of the row's 8 chunks of 8 columns; chunk c of a row is run (tile c / 2,
 // half c % 2) of the row's trellis tiles.
-template <int NR, int K>
+// MX: `ws` points at the thread's weight row's UE8M0 bytes for this stage
+// (two 32-column blocks).
+template <int NR, int K, bool MX>
 __device__ __forceinline__ void tc_expand_stage(const unsigned char* wsl, unsigned char* bsl, int tid,
-                                                uint32_t k16, uint32_t nk16) {
+                                                uint32_t k16, uint32_t nk16, const uint8_t* ws) {
   constexpr int CPT = 8 * NR / 256;
   const int n = tid % NR;
   const int c0 = (tid / NR) * CPT;
@@ -153,6 +176,12 @@ __device__ __forceinline__ void tc_expand_stage(const unsigned char* wsl, unsign
   const unsigned char* trow = wsl + (n >> 4) * 4 * 32 * K;
   unsigned char* brow = bsl + (n >> 3) * 1024 + (n & 7) * 128;
   const uint32_t sw = (uint32_t)(n & 7);
+  uint32_t f2[2] = {0u, 0u};
+  if (MX) {
+    const uint32_t sb = __ldg(reinterpret_cast<const uint16_t*>(ws));
+    f2[0] = ue8m0_half2(sb & 0xFFu);
+    f2[1] = ue8m0_half2(sb >> 8);
+  }
   if (K == 4) {
     // A K=4 tile row rr is the 32-bit words 2rr (first 8 weights) and 2rr+1;
     // a run also needs the word before it, which for the first half is the
@@ -167,9 +196,11 @@ __device__ __forceinline__ void tc_expand_stage(const unsigned char* wsl, unsign
       uint32_t y[8], w[4];
       run_mcg_k4(pw, cw.x, k16, nk16, y);
       raw_to_f16(y, w);
+      if (MX) mx_scale(w, f2[t >> 1]);
       sts128(brow + (((uint32_t)(2 * t) ^ sw) << 4), w);
       run_mcg_k4(cw.x, cw.y, k16, nk16, y);
       raw_to_f16(y, w);
+      if (MX) mx_scale(w, f2[t >> 1]);
       sts128(brow + (((uint32_t)(2 * t + 1) ^ sw) << 4), w);
     }
   } else {
@@ -184,6 +215,7 @@ __device__ __forceinline__ void tc_expand_stage(const unsigned char* wsl, unsign
 #pragma unroll
       for (int q = 0; q < 8; ++q) y[q] = mcg_raw(s8[q]);
       raw_to_f16(y, w);
+      if (MX) mx_scale(w, f2[c >> 2]);
       sts128(brow + (((uint32_t)c ^ sw) << 4), w);
     }
   }
@@ -532,7 +564,7 @@ struct TcAccPlan {
   __device__ __forceinline__ void advance(int macc) { nb = (macc == 2) ? 0 : (nb ^ 1); }
 };
 
-template <int PROJ, int KB, int NR>
+template <int PROJ, int KB, int NR, bool MX>
 __device__ __forceinline__ void tc_expanders(const TcArgs& args, const TcGeom<PROJ, NR>& G, volatile int* uring, TcBars& B,
                                              const unsigned char* wring, unsigned char* bring, volatile int* abort) {
   const FcArgs& a = args.f;
@@ -544,6 +576,13 @@ __device__ __forceinline__ void tc_expanders(const TcArgs& args, const TcGeom<PR
   for (int u; (u = pop_unit_warp(B, uring, iu, abort, &ok)) >= 0;) {
     const int rb = u / G.mblocks;
     const int K = (KB > 0) ? KB : a.bits[a.block_expert[rb]];
+    // MX: the UE8M0 bytes of this thread's weight row (tc_expand_stage: row tid % NR)
+    const uint8_t* wsr = nullptr;
+    if (MX) {
+      const int mb = u - rb * G.mblocks, n = tid % NR;
+      const int row = G.tile_row0(a, mb, n >> 4) + (n & 15);
+      wsr = a.wscale + ((size_t)a.block_expert[rb] * a.wrows + row) * a.wcols;
+    }
     for (int s = 0; s < G.nst; ++s, ++g) {
       const int ws = g % kSW, bs = g % tc_sb(KB);
       bool ok = mbar_wait_abort_lim(&B.fullW[ws], (g / kSW) & 1, abort, &tc_wait_limit);
@@ -551,15 +590,16 @@ __device__ __forceinline__ void tc_expanders(const TcArgs& args, const TcGeom<PR
       if (!__all_sync(0xFFFFFFFFu, ok)) return;
       const unsigned char* wsl = wring + ws * wsz;
       unsigned char* bsl = bring + bs * kBBytes;
+      const uint8_t* wss = MX ? wsr + 2 * s : nullptr;
       if (KB > 0) {
-        tc_expand_stage<NR, (KB > 0 ? KB : 4)>(wsl, bsl, tid, k16, nk16);
+        tc_expand_stage<NR, (KB > 0 ? KB : 4), MX>(wsl, bsl, tid, k16, nk16, wss);
       } else {
         switch (K) {
-          case 2: tc_expand_stage<NR, 2>(wsl, bsl, tid, k16, nk16); break;
-          case 3: tc_expand_stage<NR, 3>(wsl, bsl, tid, k16, nk16); break;
-          case 4: tc_expand_stage<NR, 4>(wsl, bsl, tid, k16, nk16); break;
-          case 5: tc_expand_stage<NR, 5>(wsl, bsl, tid, k16, nk16); break;
-          default: tc_expand_stage<NR, 6>(wsl, bsl, tid, k16, nk16); break;
+          case 2: tc_expand_stage<NR, 2, MX>(wsl, bsl, tid, k16, nk16, wss); break;
+          case 3: tc_expand_stage<NR, 3, MX>(wsl, bsl, tid, k16, nk16, wss); break;
+          case 4: tc_expand_stage<NR, 4, MX>(wsl, bsl, tid, k16, nk16, wss); break;
+          case 5: tc_expand_stage<NR, 5, MX>(wsl, bsl, tid, k16, nk16, wss); break;
+          default: tc_expand_stage<NR, 6, MX>(wsl, bsl, tid, k16, nk16, wss); break;
         }
       }
       fence_proxy_async();  // generic-proxy stores -> visible to the tensor core
@@ -702,7 +742,7 @@ __device__ __forceinline__ void tma_tile2d(void* dst, const CUtensorMap* map, in
 // Lane 0 loads each stage's activation operand: one box per 128 routes. Rows
 // of padding routes hold whatever the slot holds; they only reach accumulator
 // rows that no epilogue stores.
-template <int PROJ, int KB, int NR>
+template <int PROJ, int KB, int NR, bool SPLIT>
 __device__ __forceinline__ void tc_act_loader(const TcArgs& args, const TcGeom<PROJ, NR>& G, volatile int* uring,
                                               TcBars& B, unsigned char* aring, volatile int* abort) {
   const FcArgs& a = args.f;
@@ -712,7 +752,7 @@ __device__ __forceinline__ void tc_act_loader(const TcArgs& args, const TcGeom<P
   for (int u; ok && (u = pop_unit_thread(B, uring, iu, abort, &ok)) >= 0;) {
     const int slot0 = (u / G.mblocks) * args.route_block;
     const int macc = tc_macc(args, slot0);
-    const bool split = args.act2 != nullptr;  // (route blocks of 128: one accumulator)
+    constexpr bool split = SPLIT;  // separate gate / up operands (route blocks of 128: one accumulator)
     for (int s = 0; s < G.nst; ++s, ++g) {
       const int as = g % kSA;
       if (g >= kSA && !mbar_wait_abort_lim(&B.emptyA[as], ((g / kSA) - 1) & 1, abort, &tc_wait_limit)) {
@@ -722,7 +762,7 @@ __device__ __forceinline__ void tc_act_loader(const TcArgs& args, const TcGeom<P
       mbar_arrive_expect_tx(&B.fullA[as], (uint32_t)(split ? 2 : macc) * 128 * 128);
       unsigned char* dst = aring + as * kABytes;
       tma_tile2d(dst, map, s * kTcKS, slot0, &B.fullA[as]);
-      if (split)  // the up rows' operand in the second half
+      if constexpr (split)  // the up rows' operand in the second half
         tma_tile2d(dst + 128 * 128, &args.amap2, s * kTcKS, slot0, &B.fullA[as]);
       else if (macc == 2)
         tma_tile2d(dst + 128 * 128, map, s * kTcKS, slot0 + 128, &B.fullA[as]);
@@ -733,14 +773,14 @@ __device__ __forceinline__ void tc_act_loader(const TcArgs& args, const TcGeom<P
     for (int gg = (ga > kSA ? ga - kSA : 0); gg < ga; ++gg) mbar_wait_drain(&B.fullA[gg % kSA], (gg / kSA) & 1);
 }
 
-template <int PROJ, int KB, int NR>
+template <int PROJ, int KB, int NR, bool SPLIT>
 __device__ __forceinline__ void tc_issuer(const TcArgs& args, const TcGeom<PROJ, NR>& G, volatile int* uring, TcBars& B,
                                           const unsigned char* aring, const unsigned char* bring, uint32_t tmem,
                                           volatile int* abort) {
   const FcArgs& a = args.f;
   const uint32_t idesc = idesc_f16(128, NR);
   const uint32_t idesc_half = idesc_f16(128, NR / 2);
-  const bool split = args.act2 != nullptr;
+  constexpr bool split = SPLIT;
   const uint64_t adesc0 = smem_desc_sw128(smem_u32(aring));
   const uint64_t bdesc0 = smem_desc_sw128(smem_u32(bring));
   TcAccPlan plan;
@@ -769,7 +809,7 @@ __device__ __forceinline__ void tc_issuer(const TcArgs& args, const TcGeom<PROJ,
       tc_fence_after();
       const uint64_t ad = adesc0 + (uint64_t)(as * (kABytes >> 4));
       const uint64_t bd = bdesc0 + (uint64_t)(bs * (kBBytes >> 4));
-      if (split) {
+      if constexpr (split) {
         // gate rows (decoded rows 0..NR/2-1) x the gate operand into columns
         // 0..NR/2-1, up rows x the up operand (second half of the A slot)
         // into columns NR/2..NR-1
@@ -808,7 +848,7 @@ __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.a
 template <int N>
 __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N)); }
 
-template <int PROJ, int KB, int NR>
+template <int PROJ, int KB, int NR, bool MX, bool SPLIT>
 __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__ TcArgs args) {
   extern __shared__ unsigned char tc_smem_raw[];
   __shared__ __align__(8) TcBars bars;
@@ -861,7 +901,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__
   volatile int* uring = s_uring;
   if (warp < 8) {
     if (TcRegs<KB>::exp < kRegLaunch) regs_dec<TcRegs<KB>::exp>();
-    tc_expanders<PROJ, KB, NR>(args, G, uring, bars, wring, bring, abort);
+    tc_expanders<PROJ, KB, NR, MX>(args, G, uring, bars, wring, bring, abort);
   } else if (warp < 16) {
     regs_inc<TcRegs<KB>::epi>();
     tc_epilogue<PROJ, KB, NR>(args, G, uring, bars, reinterpret_cast<float*>(evec + (warp - 8) * kEvecBytes),
@@ -872,9 +912,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__
     if (warp == 16)
       tc_payload_loader<PROJ, KB, NR>(args, G, units, uring, bars, wring, abort);
     else if (warp == 17 && (tid & 31) == 0)
-      tc_act_loader<PROJ, KB, NR>(args, G, uring, bars, aring, abort);
+      tc_act_loader<PROJ, KB, NR, SPLIT>(args, G, uring, bars, aring, abort);
     else if (warp == 18 && (tid & 31) == 0)
-      tc_issuer<PROJ, KB, NR>(args, G, uring, bars, aring, bring, tmem, abort);
+      tc_issuer<PROJ, KB, NR, SPLIT>(args, G, uring, bars, aring, bring, tmem, abort);
   }
   tc_fence_before();
   __syncthreads();
@@ -883,9 +923,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-template <int PROJ, int KB, int NR>
+template <int PROJ, int KB, int NR, bool MX = false, bool SPLIT = false>
 static cudaError_t launch_tc_t(const TcArgs& args, int max_blocks, cudaStream_t st) {
-  auto kern = k_tc_fc<PROJ, KB, NR>;
+  auto kern = k_tc_fc<PROJ, KB, NR, MX, SPLIT>;
   constexpr int kmax = KB > 0 ? KB : 6;
   static_assert(tc_smem_total(kmax, tc_sb(KB)) + 1024 <= 232448, "dynamic + static shared memory over the per-block limit");
   static bool attr_done = false;  // first forward call, before any capture
@@ -912,7 +952,10 @@ static cudaError_t launch_tc_t(const TcArgs& args, int max_blocks, cudaStream_t 
 int tc_route_block() { return kTcBN; }
 
 bool tc_supported(int H, int I, int bi, int rot_h, int rot_i) {
-  return H % 128 == 0 && I % 64 == 0 && (bi == 64 || bi == 128) && I % bi == 0 && rot_h <= 128 && rot_i <= bi;
+  // (512-point output rotations: the FC2 epilogue takes the levels inside
+  // 64 columns, the combine the rest)
+  return H % 128 == 0 && I % 64 == 0 && (bi == 64 || bi == 128) && I % bi == 0 &&
+         (rot_h <= 128 || (rot_h == 512 && H % 512 == 0)) && rot_i <= bi;
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
@@ -955,15 +998,25 @@ cudaError_t launch_tc_fc(const TcArgs& args_in, int proj, int uniform_k, int max
     if (args.route_block != 128 && args.route_block != kTcBN) return cudaErrorInvalidValue;
   }
   const bool k4 = uniform_k == 4;
-#define TC_DISPATCH(P, N) \
-  return k4 ? launch_tc_t<P, 4, N>(args, max_blocks, st) : launch_tc_t<P, 0, N>(args, max_blocks, st)
+  // TrellisMX-style weights: the general-K kernels with the scale step; the
+  // separate gate / up operands (FC1) are a variant of their own, so that
+  // the common kernels' single-thread issuer keeps its register budget
+  const bool split = args.act2 != nullptr;
+#define TC_PICK(P, N, SP)                                                                     \
+  return args.f.wscale ? launch_tc_t<P, 0, N, true, SP>(args, max_blocks, st)                 \
+                       : (k4 ? launch_tc_t<P, 4, N, false, SP>(args, max_blocks, st)          \
+                             : launch_tc_t<P, 0, N, false, SP>(args, max_blocks, st))
   if (proj == 1) {
-    if (args.bi == 128) TC_DISPATCH(1, 256);
-    TC_DISPATCH(1, 128);
+    if (args.bi == 128) {
+      if (split) TC_PICK(1, 256, true);
+      TC_PICK(1, 256, false);
+    }
+    if (split) TC_PICK(1, 128, true);
+    TC_PICK(1, 128, false);
   }
-  if (args.f.H % 256 == 0) TC_DISPATCH(2, 256);
-  TC_DISPATCH(2, 128);
-#undef TC_DISPATCH
+  if (args.f.H % 256 == 0) TC_PICK(2, 256, false);
+  TC_PICK(2, 128, false);
+#undef TC_PICK
 }
 
 }  // namespace tmoe
