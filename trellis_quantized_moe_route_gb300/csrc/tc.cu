@@ -71,6 +71,14 @@ constexpr int kStageWords = 20;        // per epilogue warp: 32 rows x 16 words 
 constexpr int kStageBytes = 32 * kStageWords * 4;
 constexpr int kTcBN = 256;             // routes per route block (128 with split gate / up operands)
 constexpr int kTcKS = 64;              // contraction columns per stage
+// Stage barriers: full[g % SB] completes when stage g's activation box has
+// landed and every expander warp has stored its decoded rows (one wait for
+// the MMA issuer); empty[g % SB] when the stage's MMAs have completed (one
+// commit), which frees both the decoded buffer and the activation slot.
+// Every barrier operation costs the issuer a shared-memory round trip while
+// the tensor core streams its operands, so it waits and commits once per
+// stage. The activation ring is no deeper than the decoded ring (kSA <= SB),
+// so a phase of empty[] is never overtaken before the loader has seen it.
 constexpr int kSA = 2, kSW = 4, kSBMax = 3;
 // decoded-operand ring depth: 3 for the 4-bit payload, 2 for the general
 // case, whose larger payload slots leave no room for a third
@@ -92,7 +100,7 @@ __host__ __device__ constexpr int tc_smem_total(int kmax, int sb) {
 }
 
 struct TcBars {
-  uint64_t fullA[kSA], emptyA[kSA], fullB[kSBMax], emptyB[kSBMax], fullW[kSW], emptyW[kSW], accFull[2], accEmpty[2];
+  uint64_t full[kSBMax], empty[kSBMax], fullW[kSW], emptyW[kSW], accFull[2], accEmpty[2];
   uint64_t pair[4];  // epilogue warp pairs, one per TMEM lane quarter
   uint64_t never;    // nothing arrives here: the issuer's wait on it runs out (stall_issuer test)
   uint64_t fullU[4], emptyU[4];  // unit ring: the scheduler's picks, read by every role in order
@@ -571,7 +579,8 @@ __device__ __forceinline__ void tc_expanders(const TcArgs& args, const TcGeom<PR
   const int tid = threadIdx.x, lane = tid & 31;
   const uint32_t k16 = 0x10000u + (uint32_t)((unsigned)G.nst >> 30), nk16 = 0u - k16;
   const int wsz = tc_wslot_bytes(KB > 0 ? KB : 6);
-  int g = 0, iu = 0;
+  constexpr int SB = tc_sb(KB);
+  int g = 0, iu = 0, ready = -1;  // stages up to `ready` have their inputs
   bool ok = true;
   for (int u; (u = pop_unit_warp(B, uring, iu, abort, &ok)) >= 0;) {
     const int rb = u / G.mblocks;
@@ -584,10 +593,27 @@ __device__ __forceinline__ void tc_expanders(const TcArgs& args, const TcGeom<PR
       wsr = a.wscale + ((size_t)a.block_expert[rb] * a.wrows + row) * a.wcols;
     }
     for (int s = 0; s < G.nst; ++s, ++g) {
-      const int ws = g % kSW, bs = g % tc_sb(KB);
-      bool ok = mbar_wait_abort_lim(&B.fullW[ws], (g / kSW) & 1, abort, &tc_wait_limit);
-      if (ok && g >= tc_sb(KB)) ok = mbar_wait_abort_lim(&B.emptyB[bs], ((g / tc_sb(KB)) - 1) & 1, abort, &tc_wait_limit);
-      if (!__all_sync(0xFFFFFFFFu, ok)) return;
+      const int ws = g % kSW, bs = g % SB;
+      if (g > ready) {
+        // the stage's payload slot full and decoded buffer free, tested
+        // together; with three decoded buffers also the next stage's (its
+        // buffer was released by the MMAs of the stage before this one)
+        const bool two = SB >= 3 && s + 1 < G.nst;
+        const int g1 = two ? g + 1 : g;
+        const uint32_t fw0 = smem_u32(&B.fullW[ws]), fw1 = smem_u32(&B.fullW[g1 % kSW]);
+        const uint32_t eb0 = (g >= SB) ? smem_u32(&B.empty[bs]) : fw0;
+        const uint32_t eb1 = (g1 >= SB) ? smem_u32(&B.empty[g1 % SB]) : fw1;
+        const uint32_t pw0 = (g / kSW) & 1, pw1 = (g1 / kSW) & 1;
+        const uint32_t pb0 = (g >= SB) ? ((g / SB) - 1) & 1 : pw0, pb1 = (g1 >= SB) ? ((g1 / SB) - 1) & 1 : pw1;
+        if (mbar_test4(fw0, pw0, eb0, pb0, fw1, pw1, eb1, pb1)) {
+          ready = g1;
+        } else {
+          bool okw = mbar_wait_abort_lim(&B.fullW[ws], pw0, abort, &tc_wait_limit);
+          if (okw && g >= SB) okw = mbar_wait_abort_lim(&B.empty[bs], pb0, abort, &tc_wait_limit);
+          if (!__all_sync(0xFFFFFFFFu, okw)) return;
+          ready = g;
+        }
+      }
       const unsigned char* wsl = wring + ws * wsz;
       unsigned char* bsl = bring + bs * kBBytes;
       const uint8_t* wss = MX ? wsr + 2 * s : nullptr;
@@ -605,7 +631,7 @@ __device__ __forceinline__ void tc_expanders(const TcArgs& args, const TcGeom<PR
       fence_proxy_async();  // generic-proxy stores -> visible to the tensor core
       __syncwarp();
       if (lane == 0) {      // one arrival per warp
-        mbar_arrive(&B.fullB[bs]);
+        mbar_arrive(&B.full[bs]);
         mbar_arrive(&B.emptyW[ws]);
       }
     }
@@ -745,8 +771,9 @@ __device__ __forceinline__ void tma_tile2d(void* dst, const CUtensorMap* map, in
 template <int PROJ, int KB, int NR, bool SPLIT>
 __device__ __forceinline__ void tc_act_loader(const TcArgs& args, const TcGeom<PROJ, NR>& G, volatile int* uring,
                                               TcBars& B, unsigned char* aring, volatile int* abort) {
-  const FcArgs& a = args.f;
   const CUtensorMap* map = &args.amap;
+  constexpr int SB = tc_sb(KB);
+  static_assert(kSA <= SB, "the activation ring must not be deeper than the decoded ring");
   int g = 0, ga = 0, iu = 0;
   bool ok = true;
   for (int u; ok && (u = pop_unit_thread(B, uring, iu, abort, &ok)) >= 0;) {
@@ -755,22 +782,27 @@ __device__ __forceinline__ void tc_act_loader(const TcArgs& args, const TcGeom<P
     constexpr bool split = SPLIT;  // separate gate / up operands (route blocks of 128: one accumulator)
     for (int s = 0; s < G.nst; ++s, ++g) {
       const int as = g % kSA;
-      if (g >= kSA && !mbar_wait_abort_lim(&B.emptyA[as], ((g / kSA) - 1) & 1, abort, &tc_wait_limit)) {
+      uint64_t* fb = &B.full[g % SB];
+      // the slot's previous stage, g - kSA, has completed its MMAs
+      if (g >= kSA && !mbar_wait_abort_lim(&B.empty[(g - kSA) % SB], ((g - kSA) / SB) & 1, abort, &tc_wait_limit)) {
         ok = false;
         break;
       }
-      mbar_arrive_expect_tx(&B.fullA[as], (uint32_t)(split ? 2 : macc) * 128 * 128);
+      mbar_arrive_expect_tx(fb, (uint32_t)(split ? 2 : macc) * 128 * 128);
       unsigned char* dst = aring + as * kABytes;
-      tma_tile2d(dst, map, s * kTcKS, slot0, &B.fullA[as]);
+      tma_tile2d(dst, map, s * kTcKS, slot0, fb);
       if constexpr (split)  // the up rows' operand in the second half
-        tma_tile2d(dst + 128 * 128, &args.amap2, s * kTcKS, slot0, &B.fullA[as]);
+        tma_tile2d(dst + 128 * 128, &args.amap2, s * kTcKS, slot0, fb);
       else if (macc == 2)
-        tma_tile2d(dst + 128 * 128, map, s * kTcKS, slot0 + 128, &B.fullA[as]);
+        tma_tile2d(dst + 128 * 128, map, s * kTcKS, slot0 + 128, fb);
       ga = g + 1;
     }
   }
-  if (!ok)  // copies in flight land before the CTA exits
-    for (int gg = (ga > kSA ? ga - kSA : 0); gg < ga; ++gg) mbar_wait_drain(&B.fullA[gg % kSA], (gg / kSA) & 1);
+  // copies in flight land before the CTA exits (their stage barrier also
+  // counts the expanders' arrivals, so after an abort elsewhere this wait
+  // can run to its limit)
+  if (!ok)
+    for (int gg = (ga > kSA ? ga - kSA : 0); gg < ga; ++gg) mbar_wait_drain(&B.full[gg % SB], (gg / SB) & 1);
 }
 
 template <int PROJ, int KB, int NR, bool SPLIT>
@@ -800,12 +832,11 @@ __device__ __forceinline__ void tc_issuer(const TcArgs& args, const TcGeom<PROJ,
     const uint32_t d0 = tmem + (uint32_t)(plan.buf(macc, 0) * 256);
     for (int s = 0; s < G.nst; ++s, ++g) {
       const int as = g % kSA, bs = g % tc_sb(KB);
-      if (!mbar_wait_abort_lim(&B.fullA[as], (g / kSA) & 1, abort, &tc_wait_limit) ||
-          !mbar_wait_abort_lim(&B.fullB[bs], (g / tc_sb(KB)) & 1, abort, &tc_wait_limit)) {
+      if (!mbar_wait_abort_lim(&B.full[bs], (g / tc_sb(KB)) & 1, abort, &tc_wait_limit)) {
         ok = false;
         break;
       }
-      fence_proxy_async();  // cp.async / st.shared operand writes -> visible to the tensor core
+      // (each expander warp fenced its stores to the async proxy before arriving)
       tc_fence_after();
       const uint64_t ad = adesc0 + (uint64_t)(as * (kABytes >> 4));
       const uint64_t bd = bdesc0 + (uint64_t)(bs * (kBBytes >> 4));
@@ -828,8 +859,7 @@ __device__ __forceinline__ void tc_issuer(const TcArgs& args, const TcGeom<PROJ,
           if (macc == 2) tc_mma_f16(tmem + 256, ad + 1024 + 2 * kk, bd + 2 * kk, idesc, accum);
         }
       }
-      tc_commit(&B.emptyA[as]);
-      tc_commit(&B.emptyB[bs]);
+      tc_commit(&B.empty[bs]);
       glast = g;
     }
     if (!ok) break;
@@ -840,7 +870,7 @@ __device__ __forceinline__ void tc_issuer(const TcArgs& args, const TcGeom<PROJ,
     }
     plan.advance(macc);
   }
-  if (*abort && glast >= 0) mbar_wait_drain(&B.emptyB[glast % tc_sb(KB)], (glast / tc_sb(KB)) & 1);
+  if (*abort && glast >= 0) mbar_wait_drain(&B.empty[glast % tc_sb(KB)], (glast / tc_sb(KB)) & 1);
 }
 
 template <int N>
@@ -865,13 +895,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__
   const int tid = threadIdx.x, warp = tid >> 5;
   const TcGeom<PROJ, NR> G(args);
   if (tid == 0) {
-    for (int i = 0; i < kSA; ++i) {
-      mbar_init(&bars.fullA[i], 1);   // the loader's expect_tx arrival; the gathers complete the bytes
-      mbar_init(&bars.emptyA[i], 1);
-    }
     for (int i = 0; i < tc_sb(KB); ++i) {
-      mbar_init(&bars.fullB[i], kTcExp / 32);
-      mbar_init(&bars.emptyB[i], 1);
+      mbar_init(&bars.full[i], kTcExp / 32 + 1);  // expander warps + the activation loader's expect_tx
+      mbar_init(&bars.empty[i], 1);
     }
     for (int i = 0; i < kSW; ++i) {
       mbar_init(&bars.fullW[i], 1);

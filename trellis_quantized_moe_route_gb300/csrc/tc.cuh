@@ -159,6 +159,25 @@ __device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
                : "=r"(done) : "r"(a), "r"(parity) : "memory");
   return done != 0;
 }
+// Non-blocking test of four phases, issued back to back so that the tests'
+// latencies overlap: true when all four are complete.
+__device__ __forceinline__ bool mbar_test4(uint32_t a0, uint32_t p0, uint32_t a1, uint32_t p1, uint32_t a2,
+                                           uint32_t p2, uint32_t a3, uint32_t p3) {
+  uint32_t done;
+  asm volatile(
+      "{\n.reg .pred q0, q1, q2, q3;\n"
+      "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n"
+      "mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n"
+      "mbarrier.test_wait.parity.shared::cta.b64 q2, [%5], %6;\n"
+      "mbarrier.test_wait.parity.shared::cta.b64 q3, [%7], %8;\n"
+      "and.pred q0, q0, q1;\nand.pred q2, q2, q3;\nand.pred q0, q0, q2;\n"
+      "selp.u32 %0, 1, 0, q0;\n}\n"
+      : "=r"(done)
+      : "r"(a0), "r"(p0), "r"(a1), "r"(p1), "r"(a2), "r"(p2), "r"(a3), "r"(p3)
+      : "memory");
+  return done != 0;
+}
+
 // Wait for the phase with the given parity. Gives up when `*abort` is set or
 // after `limit_ns` of wall time (then sets `*abort`), returning false.
 __device__ __forceinline__ bool mbar_wait_abort(uint64_t* mbar, uint32_t parity, volatile int* abort,
