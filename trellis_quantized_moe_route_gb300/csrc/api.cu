@@ -481,7 +481,6 @@ tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids
   a1.out_scale = at<uint8_t>(ws, L, Layout::ZS);
   a1.route_w = w;
   a1.atomic = d.deterministic ? 0 : 1;
-  d1.nseg = dp.nseg1;
   d1.units_m = dp.units1;
   d1.bi = dp.bi;
   d1.partial = at<float>(ws, L, Layout::DEC_PARTIAL);
@@ -506,7 +505,16 @@ tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids
   a1.wcols = d.H / 32;
   const bool mx = d.fc1_wscale != nullptr;  // (TrellisMX-style weights expand by the hash)
   d1.lut = (layer->use_lut && !mx) ? layer->d_lut + (w4a8 ? 65536 : 0) : nullptr;
-  if ((e = tmoe::dec_fc_warps(1, w4a8, layer->uniform_k, d1.lut != nullptr, mx, &d1.fc_warps)) != cudaSuccess)
+  // Items of two kDecSeg-column pieces for K=4 layers once there are enough
+  // routes (measured on one GB300: T=8 step 53.5 -> 52.2 us; at T=1 and 2,
+  // where most warps hold at most one item, always-wide items took 22.4 ->
+  // 28.5 and 27.4 -> 29.7 us, hence the route threshold). The hash and table
+  // expansions take the same items, so that they sum in the same order. The
+  // partial-sum region is sized for one-piece items, the larger count.
+  d1.segs = (layer->uniform_k == 4 && !mx && T * d.topk >= tmoe::kDecWideRoutes) ? 2 : 1;
+  const int seg = tmoe::kDecSeg * d1.segs;
+  d1.nseg = (d.H + seg - 1) / seg;
+  if ((e = tmoe::dec_fc_warps(1, w4a8, layer->uniform_k, d1.lut != nullptr, mx, d1.segs, &d1.fc_warps)) != cudaSuccess)
     return cuda_fail(e, "FC1 (decode rows) setup");
   if ((e = tmoe::launch_dec_fc(d1, 1, w4a8, layer->uniform_k, st)) != cudaSuccess)
     return cuda_fail(e, "FC1 (decode rows)");
@@ -534,11 +542,11 @@ tm_status run_decode_path(tm_layer* layer, const uint16_t* x, const int32_t* ids
   a2.wscale = d.fc2_wscale;
   a2.wrows = d.H;
   a2.wcols = d.I / 32;
-  d2.nseg = dp.nseg2;
+  d2.nseg = (d.I + seg - 1) / seg;
   d2.act_scaled = d1.out_act_scaled;
   d2.units_m = dp.units2;
   d2.blk_off = pa.blk_off2;
-  if ((e = tmoe::dec_fc_warps(2, w4a8, layer->uniform_k, d2.lut != nullptr, mx, &d2.fc_warps)) != cudaSuccess)
+  if ((e = tmoe::dec_fc_warps(2, w4a8, layer->uniform_k, d2.lut != nullptr, mx, d2.segs, &d2.fc_warps)) != cudaSuccess)
     return cuda_fail(e, "FC2 (decode rows) setup");
   if ((e = tmoe::launch_dec_fc(d2, 2, w4a8, layer->uniform_k, st)) != cudaSuccess)
     return cuda_fail(e, "FC2 (decode rows)");

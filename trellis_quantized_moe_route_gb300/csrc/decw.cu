@@ -40,8 +40,8 @@ namespace tmoe {
 
 constexpr int kDwThreads = 128;          // four independent warps
 constexpr int kDwWarps = kDwThreads / 32;
-constexpr int kDwSteps = kDecSeg / 32;   // k-steps (two tiles each) per item
-constexpr int kDwTiles = kDecSeg / 16;   // payload tiles per item
+constexpr int kDwSteps = kDecSeg / 32;   // k-steps (two tiles each) per kDecSeg columns
+constexpr int kDwTiles = kDecSeg / 16;   // payload tiles per kDecSeg columns
 constexpr int kDwRing = 2;
 
 __device__ __forceinline__ void dw_griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
@@ -83,7 +83,7 @@ __device__ __forceinline__ DwMetaW dw_meta_final(const DwRaw& r, int rb, int lan
   return m;
 }
 
-__host__ __device__ inline int dw_slot_bytes(int kmax) { return kDwTiles * 32 * kmax; }
+__host__ __device__ inline int dw_slot_bytes(int kmax, int segs) { return segs * kDwTiles * 32 * kmax; }
 
 // Codebook lookup table: the fp16 weight of each of the 65,536 trellis states
 // (W4A8: of its E4M3 rounding), 128 KB. The lookup variant runs one CTA per
@@ -91,9 +91,13 @@ __host__ __device__ inline int dw_slot_bytes(int kmax) { return kDwTiles * 32 * 
 // runs several four-warp CTAs per SM.
 constexpr int kDwLutEntries = 65536;
 constexpr int kDwLutBytes = kDwLutEntries * 2;
-__host__ __device__ constexpr int dw_cta_warps(int kb, bool lut) { return lut ? (kb > 0 ? 24 : 16) : kDwWarps; }
-__host__ __device__ inline int dw_smem_bytes(int kmax, bool lut, int warps) {
-  return (lut ? kDwLutBytes : 0) + warps * kDwRing * dw_slot_bytes(kmax);
+// (lookup variant with two-piece items: half the warps, so that the table and
+// their rings still fit in one CTA's shared memory)
+__host__ __device__ constexpr int dw_cta_warps(int kb, bool lut, int segs = 1) {
+  return lut ? (kb > 0 ? 24 : 16) / segs : kDwWarps;
+}
+__host__ __device__ inline int dw_smem_bytes(int kmax, bool lut, int warps, int segs) {
+  return (lut ? kDwLutBytes : 0) + warps * kDwRing * dw_slot_bytes(kmax, segs);
 }
 
 // Window of a run for any K, read from shared memory: the 64 stream bits
@@ -145,14 +149,14 @@ struct DwItem {
   int ncols;  // columns of this segment (a multiple of 32)
 };
 
-__device__ __forceinline__ DwItem dw_item(const DecArgs& d, uint32_t id, uint32_t nstrips, int kdim) {
+__device__ __forceinline__ DwItem dw_item(const DecArgs& d, uint32_t id, uint32_t nstrips, int kdim, int seg) {
   DwItem it;
   const uint32_t t = id / nstrips;
   it.strip = (int)(id - t * nstrips);
   const uint32_t rb = t / (uint32_t)d.nseg;
   it.sg = (int)(t - rb * (uint32_t)d.nseg);
   it.rb = (int)rb;
-  it.ncols = min(kDecSeg, kdim - it.sg * kDecSeg);
+  it.ncols = min(seg, kdim - it.sg * seg);
   return it;
 }
 
@@ -175,10 +179,11 @@ __device__ __forceinline__ DwAct dw_act(const DecArgs& d, const DwItem& it) {
   return {reinterpret_cast<const uint16_t*>(d.f.act), d.act_scaled, d.f.act_scale};
 }
 
-__device__ __forceinline__ const unsigned char* dw_src(const DecArgs& d, const DwMetaW& m, const DwItem& it, int kdim) {
+__device__ __forceinline__ const unsigned char* dw_src(const DecArgs& d, const DwMetaW& m, const DwItem& it, int kdim,
+                                                     int seg) {
   const int tiles_k = kdim >> 4;
   return reinterpret_cast<const unsigned char*>(d.f.payload) + m.off +
-         ((size_t)it.strip * tiles_k + (size_t)it.sg * kDwTiles) * 32 * it.k;
+         ((size_t)it.strip * tiles_k + (size_t)it.sg * (seg >> 4)) * 32 * it.k;
 }
 
 // One 8-weight run of a tile (tile row r, half h; K = 4: the 32-bit words at
@@ -236,14 +241,14 @@ constexpr int kDwLutRuns = 2;
 // MX (TrellisMX-style weights): the weights are E4M3-rounded in both modes
 // and every 32-column block of a weight row carries a UE8M0 scale, applied
 // to that k-step's MMA result per row (exact powers of two in fp32).
-template <bool W4A8, bool PRE, int K, bool LUT, bool MX>
+template <bool W4A8, bool PRE, int K, bool LUT, bool MX, int SEGS>
 __device__ __forceinline__ void dw_compute(const DecArgs& d, const DwItem& it, int row,
                                            const unsigned char* wt, const uint16_t* lut, int kdim, float (&acc)[4]) {
   const FcArgs& a = d.f;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3, h = q & 1, tsel = q >> 1;
   const int steps = it.ncols >> 5;
-  const int col0 = it.sg * kDecSeg;
+  const int col0 = it.sg * (SEGS * kDecSeg);
   // activation fragment source: slot g's row, columns 32 ks + 16 tsel + 8 h
   const int arow = __shfl_sync(0xFFFFFFFFu, row, g);
   const DwAct src = dw_act(d, it);
@@ -263,7 +268,7 @@ __device__ __forceinline__ void dw_compute(const DecArgs& d, const DwItem& it, i
   const int oc0 = (4 * (2 * g + h)) ^ swz, op0 = (4 * ((2 * g + h + 31) & 31)) ^ swz;
   const int oc1 = (4 * (2 * g + 16 + h)) ^ swz, op1 = (4 * (2 * g + 15 + h)) ^ swz;
 #pragma unroll
-  for (int ks = 0; ks < kDwSteps; ++ks) {
+  for (int ks = 0; ks < SEGS * kDwSteps; ++ks) {
     if (ks < steps) {
       const uint4 bv = (arow >= 0) ? __ldg(reinterpret_cast<const uint4*>(ap + 32 * ks)) : make_uint4(0u, 0u, 0u, 0u);
       const unsigned char* tile = wt + (2 * ks + tsel) * 32 * K;
@@ -308,51 +313,57 @@ __device__ __forceinline__ void dw_compute(const DecArgs& d, const DwItem& it, i
   }
 }
 
-template <bool W4A8, bool PRE, int KB, bool LUT, bool MX>
+template <bool W4A8, bool PRE, int KB, bool LUT, bool MX, int SEGS>
 __device__ __forceinline__ void dw_compute_k(const DecArgs& d, const DwItem& it, int row, const unsigned char* wt,
                                              const uint16_t* lut, int kdim, float (&acc)[4]) {
   if (KB > 0) {
-    dw_compute<W4A8, PRE, (KB > 0 ? KB : 4), LUT, MX>(d, it, row, wt, lut, kdim, acc);
+    dw_compute<W4A8, PRE, (KB > 0 ? KB : 4), LUT, MX, SEGS>(d, it, row, wt, lut, kdim, acc);
     return;
   }
   switch (it.k) {
-    case 2: dw_compute<W4A8, PRE, 2, LUT, MX>(d, it, row, wt, lut, kdim, acc); break;
-    case 3: dw_compute<W4A8, PRE, 3, LUT, MX>(d, it, row, wt, lut, kdim, acc); break;
-    case 4: dw_compute<W4A8, PRE, 4, LUT, MX>(d, it, row, wt, lut, kdim, acc); break;
-    case 5: dw_compute<W4A8, PRE, 5, LUT, MX>(d, it, row, wt, lut, kdim, acc); break;
-    default: dw_compute<W4A8, PRE, 6, LUT, MX>(d, it, row, wt, lut, kdim, acc); break;
+    case 2: dw_compute<W4A8, PRE, 2, LUT, MX, SEGS>(d, it, row, wt, lut, kdim, acc); break;
+    case 3: dw_compute<W4A8, PRE, 3, LUT, MX, SEGS>(d, it, row, wt, lut, kdim, acc); break;
+    case 4: dw_compute<W4A8, PRE, 4, LUT, MX, SEGS>(d, it, row, wt, lut, kdim, acc); break;
+    case 5: dw_compute<W4A8, PRE, 5, LUT, MX, SEGS>(d, it, row, wt, lut, kdim, acc); break;
+    default: dw_compute<W4A8, PRE, 6, LUT, MX, SEGS>(d, it, row, wt, lut, kdim, acc); break;
   }
 }
 
-template <bool W4A8, int KB, bool LUT, bool MX>
+template <bool W4A8, int KB, bool LUT, bool MX, int SEGS>
 __device__ __forceinline__ void dw_compute_any(const DecArgs& d, const DwItem& it, bool pre, int row,
                                                const unsigned char* wt, const uint16_t* lut, int kdim,
                                                float (&acc)[4]) {
   if (W4A8 && pre)
-    dw_compute_k<W4A8, true, KB, LUT, MX>(d, it, row, wt, lut, kdim, acc);
+    dw_compute_k<W4A8, true, KB, LUT, MX, SEGS>(d, it, row, wt, lut, kdim, acc);
   else
-    dw_compute_k<W4A8, false, KB, LUT, MX>(d, it, row, wt, lut, kdim, acc);
+    dw_compute_k<W4A8, false, KB, LUT, MX, SEGS>(d, it, row, wt, lut, kdim, acc);
 }
 
 // W4A8: the E8M0 exponents an item reads (its valid slots x its 32-column
-// blocks), two per lane (lane l: slot l/4, blocks 2(l%4) and 2(l%4)+1),
-// loaded one item ahead; dw_pre_final says whether all lie in [-15, 7].
+// blocks), 2 * SEGS per lane (lane l: slot l/4, blocks 2 SEGS (l%4) on, one
+// byte each of the result), loaded one item ahead; dw_pre_final says whether
+// all lie in [-15, 7] (absent blocks count as 0 = 127 - 127).
+template <int SEGS>
 __device__ __forceinline__ uint32_t dw_pre_issue(const DecArgs& d, const DwItem& it, int row, int kdim, int lane) {
-  const int n = lane >> 2, b0 = 2 * (lane & 3);
+  const int n = lane >> 2, b0 = 2 * SEGS * (lane & 3);
   const int r = __shfl_sync(0xFFFFFFFFu, row, n);
   const int nb = it.ncols >> 5;
-  uint32_t lo = 127u, hi = 127u;
+  uint32_t v = 0x7F7F7F7Fu;
   if (r >= 0) {
-    const uint8_t* sp = dw_act(d, it).scale + (size_t)r * (kdim >> 5) + it.sg * kDwSteps + b0;
-    if (b0 < nb) lo = __ldg(sp);
-    if (b0 + 1 < nb) hi = __ldg(sp + 1);
+    const uint8_t* sp = dw_act(d, it).scale + (size_t)r * (kdim >> 5) + it.sg * (SEGS * kDwSteps) + b0;
+#pragma unroll
+    for (int j = 0; j < 2 * SEGS; ++j)
+      if (b0 + j < nb) v = (v & ~(0xFFu << (8 * j))) | ((uint32_t)__ldg(sp + j) << (8 * j));
   }
-  return lo | (hi << 8);
+  return v;
 }
 __device__ __forceinline__ bool dw_pre_final(uint32_t v) {
-  const uint32_t lo = v & 0xFFu, hi = v >> 8;
-  const bool ok = lo >= (uint32_t)kE8m0PreLo && lo <= (uint32_t)kE8m0PreHi && hi >= (uint32_t)kE8m0PreLo &&
-                  hi <= (uint32_t)kE8m0PreHi;
+  bool ok = true;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t b = (v >> (8 * j)) & 0xFFu;
+    ok = ok && b >= (uint32_t)kE8m0PreLo && b <= (uint32_t)kE8m0PreHi;
+  }
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
@@ -649,14 +660,15 @@ __device__ __forceinline__ void dw_epilogue_fc2_512(const DecArgs& d, int t, int
 // constant weights before it waits for its predecessor, so its first payload
 // copy overlaps the FC1 epilogue. Partial sums: per item, [slot][16 rows] fp32.
 // ---------------------------------------------------------------------------
-template <bool W4A8, int PROJ, int KB, bool LUT, bool MX>
-__global__ void __launch_bounds__(dw_cta_warps(KB, LUT) * 32, LUT ? 1 : (KB > 0 ? 6 : 4)) k_dec_warp(const DecArgs d) {
+template <bool W4A8, int PROJ, int KB, bool LUT, bool MX, int SEGS>
+__global__ void __launch_bounds__(dw_cta_warps(KB, LUT, SEGS) * 32, LUT ? 1 : (KB > 0 ? 6 : 4)) k_dec_warp(const DecArgs d) {
   extern __shared__ __align__(128) unsigned char dw_smem[];
-  constexpr int NW = dw_cta_warps(KB, LUT);
+  constexpr int NW = dw_cta_warps(KB, LUT, SEGS);
   const FcArgs& a = d.f;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int KMAX = KB > 0 ? KB : 6;
-  const int slot_bytes = dw_slot_bytes(KMAX);
+  const int slot_bytes = dw_slot_bytes(KMAX, SEGS);
+  constexpr int SEG = SEGS * kDecSeg;  // contraction columns per item
   unsigned char* ring = dw_smem + (LUT ? kDwLutBytes : 0) + warp * kDwRing * slot_bytes;
   const uint16_t* lut = reinterpret_cast<const uint16_t*>(dw_smem);
   const int kdim = PROJ == 1 ? a.H : a.I;
@@ -693,21 +705,21 @@ __global__ void __launch_bounds__(dw_cta_warps(KB, LUT) * 32, LUT ? 1 : (KB > 0 
       h += nwarps;
       raw1 = dw_meta_issue(d, (int)(pn / per_block), lane);
     }
-    it = dw_item(d, pc, nstrips, kdim);
+    it = dw_item(d, pc, nstrips, kdim, SEG);
     m = dw_meta_final<PROJ>(raw0, it.rb, lane, a.topk, d.split);
     dw_item_meta(it, m);
-    dw_copy_any(KB > 0 ? KB : it.k, ring, dw_src(d, m, it, kdim), it.ncols >> 4, lane);
+    dw_copy_any(KB > 0 ? KB : it.k, ring, dw_src(d, m, it, kdim, SEG), it.ncols >> 4, lane);
   }
   cp_async_commit();
   if (PROJ == 2) dw_griddep_wait();  // z~, its exponents and the partial buffer belong to the predecessors until now
   dw_griddep_launch();
   if (!any) return;
-  if (W4A8) pre_cur = dw_pre_issue(d, it, m.row, kdim, lane);
+  if (W4A8) pre_cur = dw_pre_issue<SEGS>(d, it, m.row, kdim, lane);
   if (has1) {
-    nit = dw_item(d, pn, nstrips, kdim);
+    nit = dw_item(d, pn, nstrips, kdim, SEG);
     nm = dw_meta_final<PROJ>(raw1, nit.rb, lane, a.topk, d.split);
     dw_item_meta(nit, nm);
-    if (W4A8) pre_next = dw_pre_issue(d, nit, nm.row, kdim, lane);
+    if (W4A8) pre_next = dw_pre_issue<SEGS>(d, nit, nm.row, kdim, lane);
     has2 = h < h1;
     if (has2) {
       pn2 = h;
@@ -717,14 +729,14 @@ __global__ void __launch_bounds__(dw_cta_warps(KB, LUT) * 32, LUT ? 1 : (KB > 0 
   }
   for (int n = 0;; ++n) {
     if (has1)
-      dw_copy_any(KB > 0 ? KB : nit.k, ring + ((n + 1) & 1) * slot_bytes, dw_src(d, nm, nit, kdim), nit.ncols >> 4, lane);
+      dw_copy_any(KB > 0 ? KB : nit.k, ring + ((n + 1) & 1) * slot_bytes, dw_src(d, nm, nit, kdim, SEG), nit.ncols >> 4, lane);
     cp_async_commit();
     cp_async_wait<1>();
     __syncwarp();
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     const bool pre = W4A8 && dw_pre_final(pre_cur);
-    dw_compute_any<W4A8, KB, LUT, MX>(d, it, pre, m.row, ring + (n & 1) * slot_bytes, lut, kdim, acc);
+    dw_compute_any<W4A8, KB, LUT, MX, SEGS>(d, it, pre, m.row, ring + (n & 1) * slot_bytes, lut, kdim, acc);
 
     // partial sums of the valid slots, [slot][16 rows]
     const int g = lane >> 2, c = 2 * (lane & 3);
@@ -746,10 +758,10 @@ __global__ void __launch_bounds__(dw_cta_warps(KB, LUT) * 32, LUT ? 1 : (KB > 0 
     has1 = has2;
     if (has1) {
       pn = pn2;
-      nit = dw_item(d, pn, nstrips, kdim);
+      nit = dw_item(d, pn, nstrips, kdim, SEG);
       nm = dw_meta_final<PROJ>(raw2, nit.rb, lane, a.topk, d.split);
       dw_item_meta(nit, nm);
-      if (W4A8) pre_next = dw_pre_issue(d, nit, nm.row, kdim, lane);
+      if (W4A8) pre_next = dw_pre_issue<SEGS>(d, nit, nm.row, kdim, lane);
       has2 = h < h1;
       if (has2) {
         pn2 = h;
@@ -794,14 +806,14 @@ __global__ void __launch_bounds__(256) k_dec_epi(const DecArgs d) {
   }
 }
 
-template <bool W4A8, int PROJ, int KB, bool LUT, bool MX = false>
+template <bool W4A8, int PROJ, int KB, bool LUT, bool MX = false, int SEGS = 1>
 static cudaError_t dw_warps_t(int* warps) {
   // attributes and the resident-CTA count are fixed on the first call (before any capture)
-  constexpr int NW = dw_cta_warps(KB, LUT);
+  constexpr int NW = dw_cta_warps(KB, LUT, SEGS);
   static int resident = 0;
   if (resident == 0) {
-    auto kern = k_dec_warp<W4A8, PROJ, KB, LUT, MX>;
-    const int smem = dw_smem_bytes(KB > 0 ? KB : 6, LUT, NW);
+    auto kern = k_dec_warp<W4A8, PROJ, KB, LUT, MX, SEGS>;
+    const int smem = dw_smem_bytes(KB > 0 ? KB : 6, LUT, NW, SEGS);
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     int per_sm = 0;
@@ -816,22 +828,22 @@ static cudaError_t dw_warps_t(int* warps) {
   return cudaSuccess;
 }
 
-template <bool W4A8, int PROJ, int KB, bool LUT, bool MX = false>
+template <bool W4A8, int PROJ, int KB, bool LUT, bool MX = false, int SEGS = 1>
 static cudaError_t launch_dw_t(const DecArgs& d, cudaStream_t st) {
-  constexpr int NW = dw_cta_warps(KB, LUT);
-  if (d.fc_warps <= 0 || d.fc_warps % NW) return cudaErrorInvalidValue;
+  constexpr int NW = dw_cta_warps(KB, LUT, SEGS);
+  if (d.fc_warps <= 0 || d.fc_warps % NW || d.segs != SEGS) return cudaErrorInvalidValue;
   if (LUT && (!d.lut || ((uintptr_t)d.lut) % 16)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(d.fc_warps / NW);
   cfg.blockDim = dim3(NW * 32);
-  cfg.dynamicSmemBytes = dw_smem_bytes(KB > 0 ? KB : 6, LUT, NW);
+  cfg.dynamicSmemBytes = dw_smem_bytes(KB > 0 ? KB : 6, LUT, NW, SEGS);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_dec_warp<W4A8, PROJ, KB, LUT, MX>, d);
+  return cudaLaunchKernelEx(&cfg, k_dec_warp<W4A8, PROJ, KB, LUT, MX, SEGS>, d);
 }
 
 // FC2 epilogue for 512-point output rotation blocks: one CTA per (token,
@@ -891,8 +903,12 @@ static cudaError_t dec_fc_warps_mx(int proj, bool w4a8, int* warps) {
 }
 
 template <bool LUT>
-static cudaError_t dec_fc_warps_t(int proj, bool w4a8, int uniform_k, int* warps) {
+static cudaError_t dec_fc_warps_t(int proj, bool w4a8, int uniform_k, int segs, int* warps) {
   const bool k4 = uniform_k == 4;
+  if (k4 && segs == 2) {
+    if (proj == 1) return w4a8 ? dw_warps_t<true, 1, 4, LUT, false, 2>(warps) : dw_warps_t<false, 1, 4, LUT, false, 2>(warps);
+    return w4a8 ? dw_warps_t<true, 2, 4, LUT, false, 2>(warps) : dw_warps_t<false, 2, 4, LUT, false, 2>(warps);
+  }
   if (proj == 1) {
     if (w4a8) return k4 ? dw_warps_t<true, 1, 4, LUT>(warps) : dw_warps_t<true, 1, 0, LUT>(warps);
     return k4 ? dw_warps_t<false, 1, 4, LUT>(warps) : dw_warps_t<false, 1, 0, LUT>(warps);
@@ -901,9 +917,10 @@ static cudaError_t dec_fc_warps_t(int proj, bool w4a8, int uniform_k, int* warps
   return k4 ? dw_warps_t<false, 2, 4, LUT>(warps) : dw_warps_t<false, 2, 0, LUT>(warps);
 }
 
-cudaError_t dec_fc_warps(int proj, bool w4a8, int uniform_k, bool lut, bool mx, int* warps) {
+cudaError_t dec_fc_warps(int proj, bool w4a8, int uniform_k, bool lut, bool mx, int segs, int* warps) {
   if (mx) return dec_fc_warps_mx(proj, w4a8, warps);
-  return lut ? dec_fc_warps_t<true>(proj, w4a8, uniform_k, warps) : dec_fc_warps_t<false>(proj, w4a8, uniform_k, warps);
+  return lut ? dec_fc_warps_t<true>(proj, w4a8, uniform_k, segs, warps)
+             : dec_fc_warps_t<false>(proj, w4a8, uniform_k, segs, warps);
 }
 
 cudaError_t launch_dec_epilogue(const DecArgs& d, int proj, bool w4a8, cudaStream_t st) {
@@ -915,6 +932,10 @@ cudaError_t launch_dec_epilogue(const DecArgs& d, int proj, bool w4a8, cudaStrea
 template <bool LUT>
 static cudaError_t launch_dec_fc_t(const DecArgs& d, int proj, bool w4a8, int uniform_k, cudaStream_t st) {
   const bool k4 = uniform_k == 4;
+  if (k4 && d.segs == 2) {
+    if (proj == 1) return w4a8 ? launch_dw_t<true, 1, 4, LUT, false, 2>(d, st) : launch_dw_t<false, 1, 4, LUT, false, 2>(d, st);
+    return w4a8 ? launch_dw_t<true, 2, 4, LUT, false, 2>(d, st) : launch_dw_t<false, 2, 4, LUT, false, 2>(d, st);
+  }
   if (proj == 1) {
     if (w4a8) return k4 ? launch_dw_t<true, 1, 4, LUT>(d, st) : launch_dw_t<true, 1, 0, LUT>(d, st);
     return k4 ? launch_dw_t<false, 1, 4, LUT>(d, st) : launch_dw_t<false, 1, 0, LUT>(d, st);

@@ -110,6 +110,10 @@ struct DecPrologueArgs {
 
 constexpr int kDecSeg = 256;  // contraction columns of one decode-rows item
 constexpr int kDecBlock = 8;  // slots per route block
+// Routes from which the K=4 decode kernels take items of 2 * kDecSeg columns:
+// fewer, longer items halve the per-item bookkeeping once each warp holds
+// several of them, and cost time when most warps hold at most one.
+constexpr int kDecWideRoutes = 48;
 
 struct DecArgs {
   FcArgs f;                 // act: fp16 rows (W4A8: E4M3 codes as fp16, E8M0 scales in act_scale)
@@ -117,7 +121,8 @@ struct DecArgs {
   uint16_t* out_act_scaled;    // FC1 W4A8: z~ as code * 2^e
   const int32_t* blk_meta;  // per route block: expert | bits << 16 | valid slots << 24
   const long long* blk_off; // per route block: byte offset of the expert's payload (this projection)
-  int nseg;                 // contraction segments of kDecSeg columns
+  int nseg;                 // contraction segments of kDecSeg * segs columns (one item each)
+  int segs;                 // kDecSeg-column pieces per item: 1, or 2 (K=4 layers, >= kDecWideRoutes routes)
   int units_m;              // epilogue units per route block (FC1: I/BI, FC2: H/128)
   int bi;                   // FC1 half-row block (64 or 128)
   int max_blocks;           // route blocks the route map can produce
@@ -141,7 +146,7 @@ struct DecArgs {
 cudaError_t launch_dec_prologue(const DecPrologueArgs& a, cudaStream_t st);
 // Warps of the decode-rows FC kernel's grid (all resident: CTAs per SM x SMs);
 // fixed on the first call, which also sets the kernel's attributes.
-cudaError_t dec_fc_warps(int proj, bool w4a8, int uniform_k, bool lut, bool mx, int* warps);
+cudaError_t dec_fc_warps(int proj, bool w4a8, int uniform_k, bool lut, bool mx, int segs, int* warps);
 // Codebook tables for the lookup variant: decode_lut_bytes() bytes, built on `st`.
 size_t decode_lut_bytes();
 cudaError_t build_decode_lut(uint16_t* lut, cudaStream_t st);
