@@ -352,7 +352,7 @@ def workload_string(name, cfg, K, mode, T):
 # program (profiles/); workloads without a capture of the current kernel get
 # None
 NCU_TRAFFIC = {
-    ("decode", 8, "w4a8"): (28.386e6, "profiles/k_dec_warp_fc1_decode_w4a8_T8.md"),
+    ("decode", 8, "w4a8"): (28.400e6, "profiles/k_dec_warp_fc1_decode_w4a8_T8.md"),
     ("prefill", 2048, "w4a16"): (128.64e6, "profiles/k_tc_fc_fc1_prefill_w4a16_T2048.md"),
 }
 
