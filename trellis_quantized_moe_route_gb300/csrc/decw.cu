@@ -4,9 +4,11 @@
 // "feat(moe): serve canonical Fruit QSRT atoms", Hot path: W4A8 only for
 // bounded decode rows; the payload is expanded straight into MMA operands).
 //
-// Work item = (route block rb of 8 slots, 16-row strip, 256-column segment).
-// Warp w of the grid takes items w, w + W, w + 2W, ... (W warps in all; items
-// cost the same, so no claiming is needed). It copies each item's 16 payload
+// Work item = (route block rb of 8 slots, 16-row strip, segment of 256
+// contraction columns, or of 512 for K=4 layers from kDecWideRoutes routes
+// on, where fewer and longer items halve the per-item bookkeeping). Warp w of
+// the grid takes items w, w + W, w + 2W, ... (W warps in all; items cost the
+// same, so no claiming is needed). It copies each item's 16 (32) payload
 // tiles (one K-bit trellis tile holds 16x16 weights) into a private two-slot
 // shared ring with cp.async -- the copy of the next item overlaps the
 // expansion of this one -- expands the tiles in registers into fp16 mma.sync
