@@ -388,6 +388,7 @@ DECODE_SHAPES = [
     dict(T=2, E=16, topk=3, rot_block_h=1, rot_block_i=1),                   # identity rotations
     dict(T=1, E=8, topk=8, H=1024, I=512),                                   # every expert, one token
     dict(T=120, E=256, topk=8, H=256, I=128),                                # 960 routes: the regime's largest block table
+    dict(T=16, E=32, topk=4, H=768, I=320, rot_block_i=64),                  # 512-column items, ragged last ones (768, 320)
 ]
 
 
