@@ -185,7 +185,9 @@ Layout make_layout(const tm_layer_desc& d, int T) {
   L.bytes[Layout::ZS] = std::max(slots, dec_z_rows / 2) * (d.I / 32);
   L.bytes[Layout::ROWS] = slots * d.H * 4;
   L.bytes[Layout::SLOT_OF_ROUTE] = R * 4;
-  L.bytes[Layout::ERR] = 16;  // error word, then the tcgen05 kernels' unit counters
+  // error word, the tcgen05 kernels' unit counters, then one z~ completion
+  // counter per route block of the fused FC1 + FC2 launch
+  L.bytes[Layout::ERR] = 16 + (R / 128 + (size_t)d.E + 2) * 4;
   L.bytes[Layout::IDS] = R * 4;
   L.bytes[Layout::W] = R * 4;
   L.bytes[Layout::RANK] = R * 4;
@@ -260,7 +262,7 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
   const DecPlan dp = dec_plan(d, T, w4a8);
   // (the decode prologue clears the error word itself)
   if (dp.use) return run_decode_path(layer, x, ids, w, logits, T, w4a8, out, ws, L, dp, st);
-  if ((e = cudaMemsetAsync(err, 0, 16, st)) != cudaSuccess) return cuda_fail(e, "clear error word");
+  if ((e = cudaMemsetAsync(err, 0, L.bytes[Layout::ERR], st)) != cudaSuccess) return cuda_fail(e, "clear error word");
   if (logits) {
     e = tmoe::launch_route_topk(logits, T, d.E, d.topk, const_cast<int32_t*>(ids), const_cast<float*>(w), st);
     if (e != cudaSuccess) return cuda_fail(e, "router");
@@ -338,8 +340,6 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
   t1.stall_issuer = layer->stall_issuer;
   t1.route_block = bn;
   t1.act2 = split ? at<void>(ws, L, Layout::XQ2) : nullptr;
-  if ((e = tmoe::launch_tc_fc(t1, 1, layer->uniform_k, max_blocks, st)) != cudaSuccess) return cuda_fail(e, "FC1");
-  if ((e = stage_mark(layer, 4, st)) != cudaSuccess) return cuda_fail(e, "stage event");
 
   tmoe::FcArgs a2 = a1;
   a2.rot_b = d.rot_block_h;
@@ -365,17 +365,23 @@ tm_status run_layer(tm_layer* layer, const uint16_t* x, const int32_t* ids, cons
   } else {
     a2.out_f32 = at<float>(ws, L, Layout::ROWS);
   }
-  tmoe::TcArgs t2{};
-  t2.f = a2;
-  t2.bi = layer->bi;
-  t2.err = err;
-  t2.sched = err + 2;
-  t2.act_rows = (int)(R + (size_t)d.E * (kBlockMax - 1));  // slots
-  t2.wait_ns = layer->wait_ns;
-  t2.stall_issuer = layer->stall_issuer;
-  t2.route_block = bn;
-  t2.act2 = nullptr;
-  if ((e = tmoe::launch_tc_fc(t2, 2, layer->uniform_k, max_blocks, st)) != cudaSuccess) return cuda_fail(e, "FC2");
+  // FC1 and FC2 in one launch where both take 256-row units: the FC2 units
+  // fill the last wave of FC1 units instead of waiting for all of them
+  if (tmoe::tc_fused_supported(d.H, layer->bi, split)) {
+    t1.f2 = a2;
+    t1.dep = err + 4;
+    if ((e = tmoe::launch_tc_fc(t1, 3, layer->uniform_k, max_blocks, st)) != cudaSuccess)
+      return cuda_fail(e, "FC1+FC2");
+    if ((e = stage_mark(layer, 4, st)) != cudaSuccess) return cuda_fail(e, "stage event");
+  } else {
+    if ((e = tmoe::launch_tc_fc(t1, 1, layer->uniform_k, max_blocks, st)) != cudaSuccess) return cuda_fail(e, "FC1");
+    if ((e = stage_mark(layer, 4, st)) != cudaSuccess) return cuda_fail(e, "stage event");
+    tmoe::TcArgs t2 = t1;
+    t2.f = a2;
+    t2.sched = err + 2;
+    t2.act2 = nullptr;
+    if ((e = tmoe::launch_tc_fc(t2, 2, layer->uniform_k, max_blocks, st)) != cudaSuccess) return cuda_fail(e, "FC2");
+  }
   if ((e = stage_mark(layer, 5, st)) != cudaSuccess) return cuda_fail(e, "stage event");
   if (a2.raw_rows) {
     tmoe::CombineUnrotArgs c{a2.out_f32, rm.slot_of_route, rm.block_expert, bn, w, d.out_svh,
@@ -905,7 +911,7 @@ tm_status trellis_moe_route_map(tm_layer* layer, const int32_t* topk_ids, int32_
   cudaStream_t st = (cudaStream_t)stream;
   uint32_t* err = at<uint32_t>(workspace, L, Layout::ERR);
   cudaError_t e;
-  if ((e = cudaMemsetAsync(err, 0, 16, st)) != cudaSuccess) return cuda_fail(e, "clear error word");
+  if ((e = cudaMemsetAsync(err, 0, L.bytes[Layout::ERR], st)) != cudaSuccess) return cuda_fail(e, "clear error word");
   tmoe::RouteMapArgs rm;
   rm.ids = topk_ids;
   rm.R = R;

@@ -165,10 +165,21 @@ struct TcArgs {
   int stall_issuer;  // test of the bounded waits: the MMA issuer first waits on a barrier nothing arrives on
   int route_block;   // slots per route block: 256, or 128 with split activations
   const void* act2;  // FC1 with separate gate / up input signs: the up rows' operand (f.act: the gate rows'), else NULL
+  // FC1 and FC2 in one launch (proj 3): f holds FC1's arguments, f2 FC2's;
+  // dep[rb] counts the FC1 epilogue warps that have stored their z~ rows of
+  // route block rb (zero before the launch, one entry per route block)
+  FcArgs f2;
+  uint32_t* dep;
   CUtensorMap amap2; // filled by launch_tc_fc from act2
   CUtensorMap amap;  // filled by launch_tc_fc: the activations as [act_rows][K] fp16, box 64 x 128, 128-byte swizzle
+  CUtensorMap amapz; // proj 3: filled by launch_tc_fc from f2.act (z~ [act_rows][I])
 };
+// proj 1 (FC1), 2 (FC2) or 3 (both in one launch: every FC1 unit is queued
+// before every FC2 unit, and an FC2 unit waits until its route block's z~
+// rows are complete); 3 needs N = 256 for both (bi = 128, H % 256 == 0) and
+// no split operands (tc_fused_supported).
 cudaError_t launch_tc_fc(const TcArgs& args, int proj, int uniform_k, int max_blocks, cudaStream_t st);
+bool tc_fused_supported(int H, int bi, bool split);
 int tc_route_block();
 // Geometry the tcgen05 kernels handle (H, I, FC1 half-row block, rotation blocks).
 bool tc_supported(int H, int I, int bi, int rot_h, int rot_i);

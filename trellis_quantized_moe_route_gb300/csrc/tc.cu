@@ -572,146 +572,237 @@ struct TcAccPlan {
   __device__ __forceinline__ void advance(int macc) { nb = (macc == 2) ? 0 : (nb ^ 1); }
 };
 
-template <int PROJ, int KB, int NR, bool MX>
-__device__ __forceinline__ void tc_expanders(const TcArgs& args, const TcGeom<PROJ, NR>& G, volatile int* uring, TcBars& B,
-                                             const unsigned char* wring, unsigned char* bring, volatile int* abort) {
-  const FcArgs& a = args.f;
+// Fused launch (proj 3): the FC1 units of every route block come first in
+// the unit order, then the FC2 units. An FC2 unit's activations are the z~
+// rows of its route block, complete once every epilogue warp of each of the
+// block's FC1 units has counted itself in dep[rb] (after a device-scope fence
+// over its stores). Only FC2 units wait, and only on FC1 units claimed before
+// them, whose pipelines wait on nothing outside their CTA: no cycle.
+template <int PROJ>
+struct TcProj {
+  static constexpr int first = PROJ == 3 ? 1 : PROJ;  // projection of the launch's first units
+  static constexpr bool fused = PROJ == 3;
+};
+
+// Waits (bounded) until *cnt >= target, then orders the acquired z~ rows
+// before this thread's later bulk-tensor (async proxy) reads.
+__device__ __forceinline__ bool tc_dep_wait(const uint32_t* cnt, uint32_t target, volatile int* abort) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(cnt) : "memory");
+  if (v < target) {
+    const uint64_t t0 = global_ns();
+    for (;;) {
+      __nanosleep(128);
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(cnt) : "memory");
+      if (v >= target) break;
+      if (*abort) return false;
+      if (global_ns() - t0 > tc_wait_limit) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+  asm volatile("fence.proxy.async.global;\n" ::: "memory");
+  return true;
+}
+
+// One unit's stages on the expander warps; false when a wait gave up.
+template <int P, int KB, int NR, bool MX>
+__device__ __forceinline__ bool tc_expand_unit(const FcArgs& a, const TcGeom<P, NR>& G, int u, TcBars& B,
+                                               const unsigned char* wring, unsigned char* bring, int& g, int& ready,
+                                               volatile int* abort) {
   const int tid = threadIdx.x, lane = tid & 31;
   const uint32_t k16 = 0x10000u + (uint32_t)((unsigned)G.nst >> 30), nk16 = 0u - k16;
   const int wsz = tc_wslot_bytes(KB > 0 ? KB : 6);
   constexpr int SB = tc_sb(KB);
-  int g = 0, iu = 0, ready = -1;  // stages up to `ready` have their inputs
-  bool ok = true;
-  for (int u; (u = pop_unit_warp(B, uring, iu, abort, &ok)) >= 0;) {
-    const int rb = u / G.mblocks;
-    const int K = (KB > 0) ? KB : a.bits[a.block_expert[rb]];
-    // MX: the UE8M0 bytes of this thread's weight row (tc_expand_stage: row tid % NR)
-    const uint8_t* wsr = nullptr;
-    if (MX) {
-      const int mb = u - rb * G.mblocks, n = tid % NR;
-      const int row = G.tile_row0(a, mb, n >> 4) + (n & 15);
-      wsr = a.wscale + ((size_t)a.block_expert[rb] * a.wrows + row) * a.wcols;
-    }
-    for (int s = 0; s < G.nst; ++s, ++g) {
-      const int ws = g % kSW, bs = g % SB;
-      if (g > ready) {
-        // the stage's payload slot full and decoded buffer free, tested
-        // together; with three decoded buffers also the next stage's (its
-        // buffer was released by the MMAs of the stage before this one)
-        const bool two = SB >= 3 && s + 1 < G.nst;
-        const int g1 = two ? g + 1 : g;
-        const uint32_t fw0 = smem_u32(&B.fullW[ws]), fw1 = smem_u32(&B.fullW[g1 % kSW]);
-        const uint32_t eb0 = (g >= SB) ? smem_u32(&B.empty[bs]) : fw0;
-        const uint32_t eb1 = (g1 >= SB) ? smem_u32(&B.empty[g1 % SB]) : fw1;
-        const uint32_t pw0 = (g / kSW) & 1, pw1 = (g1 / kSW) & 1;
-        const uint32_t pb0 = (g >= SB) ? ((g / SB) - 1) & 1 : pw0, pb1 = (g1 >= SB) ? ((g1 / SB) - 1) & 1 : pw1;
-        if (mbar_test4(fw0, pw0, eb0, pb0, fw1, pw1, eb1, pb1)) {
-          ready = g1;
-        } else {
-          bool okw = mbar_wait_abort_lim(&B.fullW[ws], pw0, abort, &tc_wait_limit);
-          if (okw && g >= SB) okw = mbar_wait_abort_lim(&B.empty[bs], pb0, abort, &tc_wait_limit);
-          if (!__all_sync(0xFFFFFFFFu, okw)) return;
-          ready = g;
-        }
-      }
-      const unsigned char* wsl = wring + ws * wsz;
-      unsigned char* bsl = bring + bs * kBBytes;
-      const uint8_t* wss = MX ? wsr + 2 * s : nullptr;
-      if (KB > 0) {
-        tc_expand_stage<NR, (KB > 0 ? KB : 4), MX>(wsl, bsl, tid, k16, nk16, wss);
+  const int rb = u / G.mblocks;
+  const int K = (KB > 0) ? KB : a.bits[a.block_expert[rb]];
+  // MX: the UE8M0 bytes of this thread's weight row (tc_expand_stage: row tid % NR)
+  const uint8_t* wsr = nullptr;
+  if (MX) {
+    const int mb = u - rb * G.mblocks, n = tid % NR;
+    const int row = G.tile_row0(a, mb, n >> 4) + (n & 15);
+    wsr = a.wscale + ((size_t)a.block_expert[rb] * a.wrows + row) * a.wcols;
+  }
+  for (int s = 0; s < G.nst; ++s, ++g) {
+    const int ws = g % kSW, bs = g % SB;
+    if (g > ready) {
+      // the stage's payload slot full and decoded buffer free, tested
+      // together; with three decoded buffers also the next stage's (its
+      // buffer was released by the MMAs of the stage before this one)
+      const bool two = SB >= 3 && s + 1 < G.nst;
+      const int g1 = two ? g + 1 : g;
+      const uint32_t fw0 = smem_u32(&B.fullW[ws]), fw1 = smem_u32(&B.fullW[g1 % kSW]);
+      const uint32_t eb0 = (g >= SB) ? smem_u32(&B.empty[bs]) : fw0;
+      const uint32_t eb1 = (g1 >= SB) ? smem_u32(&B.empty[g1 % SB]) : fw1;
+      const uint32_t pw0 = (g / kSW) & 1, pw1 = (g1 / kSW) & 1;
+      const uint32_t pb0 = (g >= SB) ? ((g / SB) - 1) & 1 : pw0, pb1 = (g1 >= SB) ? ((g1 / SB) - 1) & 1 : pw1;
+      if (mbar_test4(fw0, pw0, eb0, pb0, fw1, pw1, eb1, pb1)) {
+        ready = g1;
       } else {
-        switch (K) {
-          case 2: tc_expand_stage<NR, 2, MX>(wsl, bsl, tid, k16, nk16, wss); break;
-          case 3: tc_expand_stage<NR, 3, MX>(wsl, bsl, tid, k16, nk16, wss); break;
-          case 4: tc_expand_stage<NR, 4, MX>(wsl, bsl, tid, k16, nk16, wss); break;
-          case 5: tc_expand_stage<NR, 5, MX>(wsl, bsl, tid, k16, nk16, wss); break;
-          default: tc_expand_stage<NR, 6, MX>(wsl, bsl, tid, k16, nk16, wss); break;
-        }
+        bool okw = mbar_wait_abort_lim(&B.fullW[ws], pw0, abort, &tc_wait_limit);
+        if (okw && g >= SB) okw = mbar_wait_abort_lim(&B.empty[bs], pb0, abort, &tc_wait_limit);
+        if (!__all_sync(0xFFFFFFFFu, okw)) return false;
+        ready = g;
       }
-      fence_proxy_async();  // generic-proxy stores -> visible to the tensor core
-      __syncwarp();
-      if (lane == 0) {      // one arrival per warp
-        mbar_arrive(&B.full[bs]);
-        mbar_arrive(&B.emptyW[ws]);
+    }
+    const unsigned char* wsl = wring + ws * wsz;
+    unsigned char* bsl = bring + bs * kBBytes;
+    const uint8_t* wss = MX ? wsr + 2 * s : nullptr;
+    if (KB > 0) {
+      tc_expand_stage<NR, (KB > 0 ? KB : 4), MX>(wsl, bsl, tid, k16, nk16, wss);
+    } else {
+      switch (K) {
+        case 2: tc_expand_stage<NR, 2, MX>(wsl, bsl, tid, k16, nk16, wss); break;
+        case 3: tc_expand_stage<NR, 3, MX>(wsl, bsl, tid, k16, nk16, wss); break;
+        case 4: tc_expand_stage<NR, 4, MX>(wsl, bsl, tid, k16, nk16, wss); break;
+        case 5: tc_expand_stage<NR, 5, MX>(wsl, bsl, tid, k16, nk16, wss); break;
+        default: tc_expand_stage<NR, 6, MX>(wsl, bsl, tid, k16, nk16, wss); break;
       }
+    }
+    fence_proxy_async();  // generic-proxy stores -> visible to the tensor core
+    __syncwarp();
+    if (lane == 0) {      // one arrival per warp
+      mbar_arrive(&B.full[bs]);
+      mbar_arrive(&B.emptyW[ws]);
     }
   }
+  return true;
 }
 
-template <int PROJ, int KB, int NR>
-__device__ __forceinline__ void tc_epilogue(const TcArgs& args, const TcGeom<PROJ, NR>& G, volatile int* uring, TcBars& B,
-                                            float* ev, uint32_t* stg, uint32_t tmem, volatile int* abort) {
-  const FcArgs& a = args.f;
+template <int PROJ, int KB, int NR, bool MX>
+__device__ __forceinline__ void tc_expanders(const TcArgs& args, const TcGeom<TcProj<PROJ>::first, NR>& G,
+                                             const TcGeom<2, NR>& G2, int U1, volatile int* uring, TcBars& B,
+                                             const unsigned char* wring, unsigned char* bring, volatile int* abort) {
+  int g = 0, iu = 0, ready = -1;  // stages up to `ready` have their inputs
+  bool ok = true;
+  // a CTA's units ascend: (fused) its FC1 units, then its FC2 units
+  int u = pop_unit_warp(B, uring, iu, abort, &ok);
+  for (; u >= 0 && (!TcProj<PROJ>::fused || u < U1); u = pop_unit_warp(B, uring, iu, abort, &ok))
+    if (!tc_expand_unit<TcProj<PROJ>::first, KB, NR, MX>(args.f, G, u, B, wring, bring, g, ready, abort)) return;
+  if constexpr (TcProj<PROJ>::fused)
+    for (; u >= 0; u = pop_unit_warp(B, uring, iu, abort, &ok))
+      if (!tc_expand_unit<2, KB, NR, MX>(args.f2, G2, u - U1, B, wring, bring, g, ready, abort)) return;
+}
+
+// One unit on an epilogue warp: its vectors, then each accumulator once the
+// MMAs have filled it; false when a wait gave up.
+template <int P, int KB, int NR>
+__device__ __forceinline__ bool tc_epi_unit(const TcArgs& args, const FcArgs& a, const TcGeom<P, NR>& G, int u,
+                                            TcBars& B, float* ev, uint32_t* stg, uint32_t tmem, PairSync& ps,
+                                            TcAccPlan& plan, volatile int* abort) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;           // TMEM lane quarter
   const int h = (warp - 8) >> 2;    // column half
-  PairSync ps{&B.pair[q], 0};
-  TcAccPlan plan;
-  int iu = 0;
-  bool ok = true;
-  for (int u; (u = pop_unit_warp(B, uring, iu, abort, &ok)) >= 0;) {
-    const int rb = u / G.mblocks, mb = u - rb * G.mblocks;
-    const int e = a.block_expert[rb];
-    const int slot0 = rb * args.route_block;
-    const int macc = tc_macc(args, slot0);
-    // this warp's half of the unit's vectors, converted to fp32 and folded
-    // (its reads of the last unit are done)
-    __syncwarp();
-    {
-      const float hs = hadamard_scale(a.rot_b);
-      if (PROJ == 1) {
-        const int bi = NR / 2, hf = bi / 2, c0 = mb * bi + h * hf;
-        const uint16_t* s1 = a.scale + (size_t)e * 2 * a.I + c0;
-        const uint16_t* rt = a.rot_tab + (size_t)e * 3 * a.I + c0;
-        for (int c = lane; c < hf; c += 32) {
-          ev[c] = __half2float(__ushort_as_half(s1[c]));
-          ev[hf + c] = hs * __half2float(__ushort_as_half(rt[c]));
-          ev[2 * hf + c] = __half2float(__ushort_as_half(s1[a.I + c]));
-          ev[3 * hf + c] = hs * __half2float(__ushort_as_half(rt[a.I + c])) * __half2float(__ushort_as_half(rt[2 * a.I + c]));
-        }
-      } else {
-        const uint16_t* s2 = a.scale + (size_t)e * a.H + mb * NR;
-        const uint16_t* sv = a.rot_tab + (size_t)e * a.H + mb * NR;
-        for (int i = lane; i < NR / 2; i += 32) {
-          const int blk = i >> 6, c = blk * 128 + h * 64 + (i & 63);
-          ev[blk * 128 + (i & 63)] = __half2float(__ushort_as_half(s2[c]));
-          ev[blk * 128 + 64 + (i & 63)] = hs * __half2float(__ushort_as_half(sv[c]));
-        }
+  const int rb = u / G.mblocks, mb = u - rb * G.mblocks;
+  const int e = a.block_expert[rb];
+  const int slot0 = rb * args.route_block;
+  const int macc = tc_macc(args, slot0);
+  // this warp's half of the unit's vectors, converted to fp32 and folded
+  // (its reads of the last unit are done)
+  __syncwarp();
+  {
+    const float hs = hadamard_scale(a.rot_b);
+    if (P == 1) {
+      const int bi = NR / 2, hf = bi / 2, c0 = mb * bi + h * hf;
+      const uint16_t* s1 = a.scale + (size_t)e * 2 * a.I + c0;
+      const uint16_t* rt = a.rot_tab + (size_t)e * 3 * a.I + c0;
+      for (int c = lane; c < hf; c += 32) {
+        ev[c] = __half2float(__ushort_as_half(s1[c]));
+        ev[hf + c] = hs * __half2float(__ushort_as_half(rt[c]));
+        ev[2 * hf + c] = __half2float(__ushort_as_half(s1[a.I + c]));
+        ev[3 * hf + c] = hs * __half2float(__ushort_as_half(rt[a.I + c])) * __half2float(__ushort_as_half(rt[2 * a.I + c]));
+      }
+    } else {
+      const uint16_t* s2 = a.scale + (size_t)e * a.H + mb * NR;
+      const uint16_t* sv = a.rot_tab + (size_t)e * a.H + mb * NR;
+      for (int i = lane; i < NR / 2; i += 32) {
+        const int blk = i >> 6, c = blk * 128 + h * 64 + (i & 63);
+        ev[blk * 128 + (i & 63)] = __half2float(__ushort_as_half(s2[c]));
+        ev[blk * 128 + 64 + (i & 63)] = hs * __half2float(__ushort_as_half(sv[c]));
       }
     }
-    __syncwarp();
-    for (int acc = 0; acc < macc; ++acc) {
-      const int b = plan.buf(macc, acc);
-      const bool ok = mbar_wait_abort_lim(&B.accFull[b], plan.uses[b] & 1, abort, &tc_wait_limit);
-      if (!__all_sync(0xFFFFFFFFu, ok)) return;
-      tc_fence_after();
-      const int n = acc * 128 + 32 * q + lane;
-      const int route = a.route_of_slot[slot0 + n];
-      const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 256);
-      // a lane quarter without valid routes has nothing to store (both warps
-      // of the pair see the same lanes, so they skip together)
-      if (__any_sync(0xFFFFFFFFu, route >= 0)) {
-        const bool done = (PROJ == 1)
-                              ? tc_epi_fc1<NR / 2>(a, ev, stg, mb, slot0 + n, route >= 0, taddr, h, ps, abort)
-                              : tc_epi_fc2<NR>(a, ev, stg, mb, slot0 + n, route, route >= 0, taddr, h, ps, abort);
-        if (!done) return;
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&B.accEmpty[b]);
-      plan.uses[b]++;
-    }
-    plan.advance(macc);
   }
+  __syncwarp();
+  for (int acc = 0; acc < macc; ++acc) {
+    const int b = plan.buf(macc, acc);
+    const bool ok = mbar_wait_abort_lim(&B.accFull[b], plan.uses[b] & 1, abort, &tc_wait_limit);
+    if (!__all_sync(0xFFFFFFFFu, ok)) return false;
+    tc_fence_after();
+    const int n = acc * 128 + 32 * q + lane;
+    const int route = a.route_of_slot[slot0 + n];
+    const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 256);
+    // a lane quarter without valid routes has nothing to store (both warps
+    // of the pair see the same lanes, so they skip together)
+    if (__any_sync(0xFFFFFFFFu, route >= 0)) {
+      const bool done = (P == 1) ? tc_epi_fc1<NR / 2>(a, ev, stg, mb, slot0 + n, route >= 0, taddr, h, ps, abort)
+                                 : tc_epi_fc2<NR>(a, ev, stg, mb, slot0 + n, route, route >= 0, taddr, h, ps, abort);
+      if (!done) return false;
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&B.accEmpty[b]);
+    plan.uses[b]++;
+  }
+  plan.advance(macc);
+  return true;
 }
 
 template <int PROJ, int KB, int NR>
-__device__ __forceinline__ void tc_payload_loader(const TcArgs& args, const TcGeom<PROJ, NR>& G, int units,
-                                                  volatile int* uring, TcBars& B, unsigned char* wring,
-                                                  volatile int* abort) {
-  const FcArgs& a = args.f;
+__device__ __forceinline__ void tc_epilogue(const TcArgs& args, const TcGeom<TcProj<PROJ>::first, NR>& G,
+                                            const TcGeom<2, NR>& G2, int U1, volatile int* uring, TcBars& B, float* ev,
+                                            uint32_t* stg, uint32_t tmem, volatile int* abort) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  PairSync ps{&B.pair[warp & 3], 0};
+  TcAccPlan plan;
+  int iu = 0;
+  bool ok = true;
+  // a CTA's units ascend: (fused) its FC1 units, then its FC2 units
+  int u = pop_unit_warp(B, uring, iu, abort, &ok);
+  for (; u >= 0 && (!TcProj<PROJ>::fused || u < U1); u = pop_unit_warp(B, uring, iu, abort, &ok)) {
+    if (!tc_epi_unit<TcProj<PROJ>::first, KB, NR>(args, args.f, G, u, B, ev, stg, tmem, ps, plan, abort)) return;
+    if constexpr (TcProj<PROJ>::fused) {
+      // this warp's z~ rows of the unit are stored: count it for the route block
+      __threadfence();
+      asm volatile("fence.proxy.async.global;\n" ::: "memory");
+      __syncwarp();
+      if (lane == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;\n" ::"l"(args.dep + u / G.mblocks) : "memory");
+    }
+  }
+  if constexpr (TcProj<PROJ>::fused)
+    for (; u >= 0; u = pop_unit_warp(B, uring, iu, abort, &ok))
+      if (!tc_epi_unit<2, KB, NR>(args, args.f2, G2, u - U1, B, ev, stg, tmem, ps, plan, abort)) return;
+}
+
+// One unit's payload stages (payload warp); false when a wait gave up.
+template <int P, int KB, int NR>
+__device__ __forceinline__ bool tc_payload_unit(const FcArgs& a, const TcGeom<P, NR>& G, int u, TcBars& B,
+                                                unsigned char* wring, int& g, int& gw, volatile int* abort) {
   const int lane = threadIdx.x & 31;
   const int wsz = tc_wslot_bytes(KB > 0 ? KB : 6);
+  const int rb = u / G.mblocks, mb = u - rb * G.mblocks;
+  const int e = a.block_expert[rb];
+  const int K = (KB > 0) ? KB : a.bits[e];
+  const uint32_t wbytes = 4 * 32 * K;  // one tile row of a stage
+  const uint16_t* wsrc = reinterpret_cast<const uint16_t*>(a.payload);
+  if (lane < NR / 16) wsrc += a.word_off[e] + (size_t)(G.tile_row0(a, mb, lane) >> 4) * G.tiles_k * 16 * K;
+  for (int s = 0; s < G.nst; ++s, ++g) {
+    const int ws = g % kSW;
+    const bool okw = (g < kSW) || mbar_wait_abort_lim(&B.emptyW[ws], ((g / kSW) - 1) & 1, abort, &tc_wait_limit);
+    if (!__all_sync(0xFFFFFFFFu, okw)) return false;
+    if (lane == 0) mbar_arrive_expect_tx(&B.fullW[ws], (NR / 16) * wbytes);
+    __syncwarp();
+    if (lane < NR / 16) bulk_g2s(wring + ws * wsz + lane * wbytes, wsrc + (size_t)s * 4 * 16 * K, wbytes, &B.fullW[ws]);
+    gw = g + 1;
+  }
+  return true;
+}
+
+template <int PROJ, int KB, int NR>
+__device__ __forceinline__ void tc_payload_loader(const TcArgs& args, const TcGeom<TcProj<PROJ>::first, NR>& G,
+                                                  const TcGeom<2, NR>& G2, int U1, int units, volatile int* uring,
+                                                  TcBars& B, unsigned char* wring, volatile int* abort) {
+  const int lane = threadIdx.x & 31;
   int g = 0, gw = 0;
   bool ok = true;
   uint32_t next = (lane == 0) ? atomicAdd(args.sched, 1u) : 0u;
@@ -732,24 +823,14 @@ __device__ __forceinline__ void tc_payload_loader(const TcArgs& args, const TcGe
       if (u >= 0) next = atomicAdd(args.sched, 1u);
     }
     if (u < 0) break;
-    const int rb = u / G.mblocks, mb = u - rb * G.mblocks;
-    const int e = a.block_expert[rb];
-    const int K = (KB > 0) ? KB : a.bits[e];
-    const uint32_t wbytes = 4 * 32 * K;  // one tile row of a stage
-    const uint16_t* wsrc = reinterpret_cast<const uint16_t*>(a.payload);
-    if (lane < NR / 16) wsrc += a.word_off[e] + (size_t)(G.tile_row0(a, mb, lane) >> 4) * G.tiles_k * 16 * K;
-    for (int s = 0; s < G.nst; ++s, ++g) {
-      const int ws = g % kSW;
-      const bool okw = (g < kSW) || mbar_wait_abort_lim(&B.emptyW[ws], ((g / kSW) - 1) & 1, abort, &tc_wait_limit);
-      if (!__all_sync(0xFFFFFFFFu, okw)) {
-        ok = false;
-        break;
+    if constexpr (TcProj<PROJ>::fused) {
+      if (u >= U1) {
+        ok = tc_payload_unit<2, KB, NR>(args.f2, G2, u - U1, B, wring, g, gw, abort);
+        if (!ok) break;
+        continue;
       }
-      if (lane == 0) mbar_arrive_expect_tx(&B.fullW[ws], (NR / 16) * wbytes);
-      __syncwarp();
-      if (lane < NR / 16) bulk_g2s(wring + ws * wsz + lane * wbytes, wsrc + (size_t)s * 4 * 16 * K, wbytes, &B.fullW[ws]);
-      gw = g + 1;
     }
+    ok = tc_payload_unit<TcProj<PROJ>::first, KB, NR>(args.f, G, u, B, wring, g, gw, abort);
     if (!ok) break;
   }
   if (!ok && lane == 0)  // copies in flight land before the CTA exits
@@ -765,37 +846,55 @@ __device__ __forceinline__ void tma_tile2d(void* dst, const CUtensorMap* map, in
       : "memory");
 }
 
-// Lane 0 loads each stage's activation operand: one box per 128 routes. Rows
-// of padding routes hold whatever the slot holds; they only reach accumulator
-// rows that no epilogue stores.
-template <int PROJ, int KB, int NR, bool SPLIT>
-__device__ __forceinline__ void tc_act_loader(const TcArgs& args, const TcGeom<PROJ, NR>& G, volatile int* uring,
-                                              TcBars& B, unsigned char* aring, volatile int* abort) {
-  const CUtensorMap* map = &args.amap;
+// One unit's activation stages (lane 0 of the activation warp): one box per
+// 128 routes. Rows of padding routes hold whatever the slot holds; they only
+// reach accumulator rows that no epilogue stores. False when a wait gave up.
+template <int P, int KB, int NR, bool SPLIT>
+__device__ __forceinline__ bool tc_act_unit(const TcArgs& args, const CUtensorMap* map, const TcGeom<P, NR>& G, int u,
+                                            TcBars& B, unsigned char* aring, int& g, int& ga, volatile int* abort) {
   constexpr int SB = tc_sb(KB);
   static_assert(kSA <= SB, "the activation ring must not be deeper than the decoded ring");
+  const int slot0 = (u / G.mblocks) * args.route_block;
+  const int macc = tc_macc(args, slot0);
+  constexpr bool split = SPLIT;  // separate gate / up operands (route blocks of 128: one accumulator)
+  for (int s = 0; s < G.nst; ++s, ++g) {
+    const int as = g % kSA;
+    uint64_t* fb = &B.full[g % SB];
+    // the slot's previous stage, g - kSA, has completed its MMAs
+    if (g >= kSA && !mbar_wait_abort_lim(&B.empty[(g - kSA) % SB], ((g - kSA) / SB) & 1, abort, &tc_wait_limit))
+      return false;
+    mbar_arrive_expect_tx(fb, (uint32_t)(split ? 2 : macc) * 128 * 128);
+    unsigned char* dst = aring + as * kABytes;
+    tma_tile2d(dst, map, s * kTcKS, slot0, fb);
+    if constexpr (split)  // the up rows' operand in the second half
+      tma_tile2d(dst + 128 * 128, &args.amap2, s * kTcKS, slot0, fb);
+    else if (macc == 2)
+      tma_tile2d(dst + 128 * 128, map, s * kTcKS, slot0 + 128, fb);
+    ga = g + 1;
+  }
+  return true;
+}
+
+template <int PROJ, int KB, int NR, bool SPLIT>
+__device__ __forceinline__ void tc_act_loader(const TcArgs& args, const TcGeom<TcProj<PROJ>::first, NR>& G,
+                                              const TcGeom<2, NR>& G2, int U1, volatile int* uring, TcBars& B,
+                                              unsigned char* aring, volatile int* abort) {
+  constexpr int SB = tc_sb(KB);
   int g = 0, ga = 0, iu = 0;
   bool ok = true;
-  for (int u; ok && (u = pop_unit_thread(B, uring, iu, abort, &ok)) >= 0;) {
-    const int slot0 = (u / G.mblocks) * args.route_block;
-    const int macc = tc_macc(args, slot0);
-    constexpr bool split = SPLIT;  // separate gate / up operands (route blocks of 128: one accumulator)
-    for (int s = 0; s < G.nst; ++s, ++g) {
-      const int as = g % kSA;
-      uint64_t* fb = &B.full[g % SB];
-      // the slot's previous stage, g - kSA, has completed its MMAs
-      if (g >= kSA && !mbar_wait_abort_lim(&B.empty[(g - kSA) % SB], ((g - kSA) / SB) & 1, abort, &tc_wait_limit)) {
-        ok = false;
-        break;
-      }
-      mbar_arrive_expect_tx(fb, (uint32_t)(split ? 2 : macc) * 128 * 128);
-      unsigned char* dst = aring + as * kABytes;
-      tma_tile2d(dst, map, s * kTcKS, slot0, fb);
-      if constexpr (split)  // the up rows' operand in the second half
-        tma_tile2d(dst + 128 * 128, &args.amap2, s * kTcKS, slot0, fb);
-      else if (macc == 2)
-        tma_tile2d(dst + 128 * 128, map, s * kTcKS, slot0 + 128, fb);
-      ga = g + 1;
+  // a CTA's units ascend: (fused) its FC1 units, then its FC2 units
+  int u = pop_unit_thread(B, uring, iu, abort, &ok);
+  while (ok && u >= 0 && (!TcProj<PROJ>::fused || u < U1)) {
+    ok = tc_act_unit<TcProj<PROJ>::first, KB, NR, SPLIT>(args, &args.amap, G, u, B, aring, g, ga, abort);
+    if (ok) u = pop_unit_thread(B, uring, iu, abort, &ok);
+  }
+  if constexpr (TcProj<PROJ>::fused) {
+    while (ok && u >= 0) {
+      const int v = u - U1;
+      // the route block's z~ rows: every epilogue warp of its FC1 units
+      ok = tc_dep_wait(args.dep + v / G2.mblocks, (uint32_t)(G.mblocks * kTcEpiWarps), abort) &&
+           tc_act_unit<2, KB, NR, false>(args, &args.amapz, G2, v, B, aring, g, ga, abort);
+      if (ok) u = pop_unit_thread(B, uring, iu, abort, &ok);
     }
   }
   // copies in flight land before the CTA exits (their stage barrier also
@@ -806,10 +905,10 @@ __device__ __forceinline__ void tc_act_loader(const TcArgs& args, const TcGeom<P
 }
 
 template <int PROJ, int KB, int NR, bool SPLIT>
-__device__ __forceinline__ void tc_issuer(const TcArgs& args, const TcGeom<PROJ, NR>& G, volatile int* uring, TcBars& B,
+__device__ __forceinline__ void tc_issuer(const TcArgs& args, const TcGeom<TcProj<PROJ>::first, NR>& G,
+                                          const TcGeom<2, NR>& G2, int U1, volatile int* uring, TcBars& B,
                                           const unsigned char* aring, const unsigned char* bring, uint32_t tmem,
                                           volatile int* abort) {
-  const FcArgs& a = args.f;
   const uint32_t idesc = idesc_f16(128, NR);
   const uint32_t idesc_half = idesc_f16(128, NR / 2);
   constexpr bool split = SPLIT;
@@ -822,7 +921,12 @@ __device__ __forceinline__ void tc_issuer(const TcArgs& args, const TcGeom<PROJ,
   // issued, so that the CTA aborts with only completed copies behind it
   if (args.stall_issuer && !mbar_wait_abort_lim(&B.never, 0, abort, &tc_wait_limit)) return;
   for (int u; ok && (u = pop_unit_thread(B, uring, iu, abort, &ok)) >= 0;) {
-    const int macc = tc_macc(args, (u / G.mblocks) * args.route_block);
+    int rb = u / G.mblocks, nst = G.nst;
+    if (TcProj<PROJ>::fused && u >= U1) {
+      rb = (u - U1) / G2.mblocks;
+      nst = G2.nst;
+    }
+    const int macc = tc_macc(args, rb * args.route_block);
     for (int acc = 0; acc < macc && ok; ++acc) {  // the unit's buffers drained by the epilogue
       const int b = plan.buf(macc, acc);
       if (plan.uses[b] > 0) ok = mbar_wait_abort_lim(&B.accEmpty[b], (plan.uses[b] - 1) & 1, abort, &tc_wait_limit);
@@ -830,7 +934,7 @@ __device__ __forceinline__ void tc_issuer(const TcArgs& args, const TcGeom<PROJ,
     if (!ok) break;
     tc_fence_after();
     const uint32_t d0 = tmem + (uint32_t)(plan.buf(macc, 0) * 256);
-    for (int s = 0; s < G.nst; ++s, ++g) {
+    for (int s = 0; s < nst; ++s, ++g) {
       const int as = g % kSA, bs = g % tc_sb(KB);
       if (!mbar_wait_abort_lim(&B.full[bs], (g / tc_sb(KB)) & 1, abort, &tc_wait_limit)) {
         ok = false;
@@ -893,7 +997,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__
   unsigned char* wring = bring + tc_sb(KB) * kBBytes;
   unsigned char* evec = wring + kSW * tc_wslot_bytes(kmax);
   const int tid = threadIdx.x, warp = tid >> 5;
-  const TcGeom<PROJ, NR> G(args);
+  const TcGeom<TcProj<PROJ>::first, NR> G(args);
+  const TcGeom<2, NR> G2(args);  // (fused launch: the FC2 units)
   if (tid == 0) {
     for (int i = 0; i < tc_sb(KB); ++i) {
       mbar_init(&bars.full[i], kTcExp / 32 + 1);  // expander warps + the activation loader's expect_tx
@@ -921,26 +1026,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_fc(const __grid_constant__
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const int units = *args.f.nblocks * G.mblocks;
+  const int U1 = *args.f.nblocks * G.mblocks;  // (fused launch: the FC1 units, then the FC2 units)
+  const int units = TcProj<PROJ>::fused ? U1 + *args.f.nblocks * G2.mblocks : U1;
   const uint32_t tmem = tmem_slot;
   volatile int* abort = &s_abort;
   volatile int* uring = s_uring;
   if (warp < 8) {
     if (TcRegs<KB>::exp < kRegLaunch) regs_dec<TcRegs<KB>::exp>();
-    tc_expanders<PROJ, KB, NR, MX>(args, G, uring, bars, wring, bring, abort);
+    tc_expanders<PROJ, KB, NR, MX>(args, G, G2, U1, uring, bars, wring, bring, abort);
   } else if (warp < 16) {
     regs_inc<TcRegs<KB>::epi>();
-    tc_epilogue<PROJ, KB, NR>(args, G, uring, bars, reinterpret_cast<float*>(evec + (warp - 8) * kEvecBytes),
-                                    reinterpret_cast<uint32_t*>(evec + kTcEpiWarps * kEvecBytes + (warp - 8) * kStageBytes),
-                                    tmem, abort);
+    tc_epilogue<PROJ, KB, NR>(args, G, G2, U1, uring, bars, reinterpret_cast<float*>(evec + (warp - 8) * kEvecBytes),
+                              reinterpret_cast<uint32_t*>(evec + kTcEpiWarps * kEvecBytes + (warp - 8) * kStageBytes),
+                              tmem, abort);
   } else {
     regs_dec<kRegAux>();
     if (warp == 16)
-      tc_payload_loader<PROJ, KB, NR>(args, G, units, uring, bars, wring, abort);
+      tc_payload_loader<PROJ, KB, NR>(args, G, G2, U1, units, uring, bars, wring, abort);
     else if (warp == 17 && (tid & 31) == 0)
-      tc_act_loader<PROJ, KB, NR, SPLIT>(args, G, uring, bars, aring, abort);
+      tc_act_loader<PROJ, KB, NR, SPLIT>(args, G, G2, U1, uring, bars, aring, abort);
     else if (warp == 18 && (tid & 31) == 0)
-      tc_issuer<PROJ, KB, NR, SPLIT>(args, G, uring, bars, aring, bring, tmem, abort);
+      tc_issuer<PROJ, KB, NR, SPLIT>(args, G, G2, U1, uring, bars, aring, bring, tmem, abort);
   }
   tc_fence_before();
   __syncthreads();
@@ -968,7 +1074,7 @@ static cudaError_t launch_tc_t(const TcArgs& args, int max_blocks, cudaStream_t 
   cudaError_t err = cudaGetDevice(&dev);
   if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (err != cudaSuccess) return err;
-  const int mblocks = (PROJ == 1) ? args.f.I / args.bi : args.f.H / NR;
+  const int mblocks = (PROJ == 1) ? args.f.I / args.bi : (PROJ == 2) ? args.f.H / NR : args.f.I / args.bi + args.f.H / NR;
   const long units = (long)max_blocks * mblocks;
   const int grid = (int)std::max<long>(1, std::min<long>(units, sms));
   kern<<<grid, kTcThreads, tc_smem_total(kmax, tc_sb(KB)), st>>>(args);
@@ -976,6 +1082,8 @@ static cudaError_t launch_tc_t(const TcArgs& args, int max_blocks, cudaStream_t 
 }
 
 int tc_route_block() { return kTcBN; }
+
+bool tc_fused_supported(int H, int bi, bool split) { return bi == 128 && H % 256 == 0 && !split; }
 
 bool tc_supported(int H, int I, int bi, int rot_h, int rot_i) {
   // (512-point output rotations: the FC2 epilogue takes the levels inside
@@ -1002,7 +1110,7 @@ cudaError_t launch_tc_fc(const TcArgs& args_in, int proj, int uniform_k, int max
   {
     // the activation operand [act_rows][K] fp16 in boxes of 64 columns (128
     // bytes, the swizzle span) x 128 rows
-    const int kdim = (proj == 1) ? args.f.H : args.f.I;
+    const int kdim = (proj == 2) ? args.f.I : args.f.H;
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     cuuint64_t dims[2] = {(cuuint64_t)kdim, (cuuint64_t)args.act_rows};
@@ -1013,6 +1121,17 @@ cudaError_t launch_tc_fc(const TcArgs& args_in, int proj, int uniform_k, int max
                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (proj == 3) {
+      // FC2's operand: z~ [act_rows][I]
+      if (!tc_fused_supported(args.f.H, args.bi, args.act2 != nullptr) || args.dep == nullptr)
+        return cudaErrorInvalidValue;
+      cuuint64_t dz[2] = {(cuuint64_t)args.f.I, (cuuint64_t)args.act_rows};
+      cuuint64_t sz[1] = {(cuuint64_t)args.f.I * 2};
+      const CUresult rz = enc(&args.amapz, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(args.f2.act), dz, sz,
+                              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (rz != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
     if (args.act2 != nullptr) {
       // separate gate / up operands: FC1 only, one 128-route accumulator per unit
       if (proj != 1 || args.route_block != 128) return cudaErrorInvalidValue;
@@ -1032,6 +1151,7 @@ cudaError_t launch_tc_fc(const TcArgs& args_in, int proj, int uniform_k, int max
   return args.f.wscale ? launch_tc_t<P, 0, N, true, SP>(args, max_blocks, st)                 \
                        : (k4 ? launch_tc_t<P, 4, N, false, SP>(args, max_blocks, st)          \
                              : launch_tc_t<P, 0, N, false, SP>(args, max_blocks, st))
+  if (proj == 3) TC_PICK(3, 256, false);
   if (proj == 1) {
     if (args.bi == 128) {
       if (split) TC_PICK(1, 256, true);
