@@ -32,6 +32,12 @@
 //                           into the fused W4A16 API", review of kernel.py;
 //                           FC2: scale, H, down_svh).
 //
+// Where FC1 and FC2 both take 256-row units the two run as one launch: the
+// unit order holds every FC1 unit, then every FC2 unit; an FC2 unit's
+// activation loader waits (bounded) until the epilogue warps of its route
+// block's FC1 units have counted their z~ rows in a per-block counter, so the
+// FC2 units fill the SMs that the last wave of FC1 units leaves idle.
+//
 // Tensor memory holds two 256-column accumulator buffers: a unit of up to 128
 // routes takes one (alternating), a unit of up to 256 routes takes both, so
 // the epilogue of one unit overlaps the contraction of the next. Every
