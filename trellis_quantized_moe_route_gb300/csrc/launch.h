@@ -180,6 +180,11 @@ struct TcArgs {
 // no split operands (tc_fused_supported).
 cudaError_t launch_tc_fc(const TcArgs& args, int proj, int uniform_k, int max_blocks, cudaStream_t st);
 bool tc_fused_supported(int H, int bi, bool split);
+// The variants of each projection (tc_fc1.cu, tc_fc2.cu, tc_fused.cu), called
+// by launch_tc_fc once the tensor maps are in args.
+cudaError_t launch_tc_fc1(const TcArgs& args, int uniform_k, int max_blocks, cudaStream_t st);
+cudaError_t launch_tc_fc2(const TcArgs& args, int uniform_k, int max_blocks, cudaStream_t st);
+cudaError_t launch_tc_fused(const TcArgs& args, int uniform_k, int max_blocks, cudaStream_t st);
 int tc_route_block();
 // Geometry the tcgen05 kernels handle (H, I, FC1 half-row block, rotation blocks).
 bool tc_supported(int H, int I, int bi, int rot_h, int rot_i);
