@@ -173,6 +173,47 @@ def sampler_started(dev):
     return smp
 
 
+def roofline_record(cfg, T, mode, stages_us, fc1_bytes, pk, ncu):
+    """The roofline object of one layer workload, from its stage times (us),
+    the FC1 launch's algorithmic bytes and the peaks. Returns (roofline,
+    decode_path, fused): the decode rows are bound by HBM bytes, the tensor-core
+    path by FLOPs. Where FC1 and FC2 both take 256-row units the library runs
+    them as one tensor-core launch (FC2 units fill FC1's last wave); the stage
+    after its event is then empty and that launch's work is both GEMMs."""
+    K = max(cfg.bits)
+    R = T * cfg.topk
+    decode_path = R <= 1024 and (mode == "w4a8" or R < 4 * cfg.E)   # the library's decode-rows regime
+    fused = not decode_path and stages_us["fc2"] < 0.1 * stages_us["fc1"]
+    if decode_path:
+        achieved = fc1_bytes / (stages_us["fc1"] * 1e-6) / 1e9
+        roof = {"bound": "hbm", "kernel": "k_dec_warp<%s,FC1,K=%d> (decode rows, persistent warp items)" % (
+                    mode.upper(), K),
+                "achieved": round(achieved, 1),
+                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                "traffic": ncu[0] if ncu else None, "traffic_source": ncu[1] if ncu else None,
+                "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst)",
+                "bytes_per_launch": int(fc1_bytes)}
+    else:
+        flops = 2 * R * 2 * cfg.I * cfg.H + (2 * R * cfg.H * cfg.I if fused else 0)
+        achieved = flops / (stages_us["fc1"] * 1e-6) / 1e12
+        kern = "k_tc_fc<FC1+FC2,K=%d> (tcgen05, W4A16, one launch)" if fused else "k_tc_fc<FC1,K=%d> (tcgen05, W4A16)"
+        roof = {"bound": "tensor", "kernel": kern % K, "achieved": round(achieved, 2),
+                "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4),
+                "traffic": ncu[0] if ncu else None, "traffic_source": ncu[1] if ncu else None,
+                "peak_source": pk["source"] + " (bf16 dense burst; fp16 runs at the bf16 rate)",
+                "flops_per_launch": flops}
+    return roof, decode_path, fused
+
+
+def launches_per_layer_step(R, decode_path, fused):
+    """Our kernels per layer step: decode rows: prologue, FC1, FC1 epilogue,
+    FC2, FC2 epilogue; otherwise router, route map (1 kernel, 3 above 1024
+    routes), rotate, FC1 and FC2 (one launch when fused), combine."""
+    if decode_path:
+        return 5
+    return 6 + (2 if R > 1024 else 0) - (1 if fused else 0)
+
+
 def measure_layer(name, T, mode, steps, warmup, rank, world, dev, e2e_steps):
     """One workload of the layer: graphs per (layer copy, token batch), K timed
     steps between CUDA events on the launching stream, stage durations from
@@ -278,30 +319,8 @@ def measure_layer(name, T, mode, steps, warmup, rank, world, dev, e2e_steps):
         fc1_bytes.append(nb)
         distinct.append(d)
     pk = peaks()
-    decode_path = R <= 1024 and (mode == "w4a8" or R < 4 * cfg.E)   # the library's decode-rows regime
-    fused = not decode_path and stages_us["fc2"] < 0.1 * stages_us["fc1"]
-    ncu = NCU_TRAFFIC.get((name, T, mode))
-    if decode_path:
-        achieved = statistics.mean(fc1_bytes) / (stages_us["fc1"] * 1e-6) / 1e9
-        roof = {"bound": "hbm", "kernel": "k_dec_warp<%s,FC1,K=%d> (decode rows, persistent warp items)" % (
-                    mode.upper(), K),
-                "achieved": round(achieved, 1),
-                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
-                "traffic": ncu[0] if ncu else None, "traffic_source": ncu[1] if ncu else None,
-                "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst)",
-                "bytes_per_launch": int(statistics.mean(fc1_bytes))}
-    else:
-        # where FC1 and FC2 both take 256-row units the library runs them as
-        # one tensor-core launch (FC2 units fill FC1's last wave); the stage
-        # after its event is then empty and the launch's work is both GEMMs
-        flops = 2 * R * 2 * cfg.I * cfg.H + (2 * R * cfg.H * cfg.I if fused else 0)
-        achieved = flops / (stages_us["fc1"] * 1e-6) / 1e12
-        kern = "k_tc_fc<FC1+FC2,K=%d> (tcgen05, W4A16, one launch)" if fused else "k_tc_fc<FC1,K=%d> (tcgen05, W4A16)"
-        roof = {"bound": "tensor", "kernel": kern % K, "achieved": round(achieved, 2),
-                "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4),
-                "traffic": ncu[0] if ncu else None, "traffic_source": ncu[1] if ncu else None,
-                "peak_source": pk["source"] + " (bf16 dense burst; fp16 runs at the bf16 rate)",
-                "flops_per_launch": flops}
+    roof, decode_path, fused = roofline_record(cfg, T, mode, stages_us, statistics.mean(fc1_bytes), pk,
+                                               NCU_TRAFFIC.get((name, T, mode)))
 
     # end to end through the host-buffer C-ABI call
     xh = [torch.from_numpy(np.ascontiguousarray(b[3].view(np.int16))).pin_memory() for b in batches]
@@ -330,10 +349,7 @@ def measure_layer(name, T, mode, steps, warmup, rank, world, dev, e2e_steps):
                        "logits and write the fp32 result over NVLink-C2C each call (no staging copies); the call "
                        "replays a graph cached for the buffer set and synchronises the stream"}
 
-    # decode rows: prologue, FC1, FC1 epilogue, FC2, FC2 epilogue; otherwise
-    # router, route map (1 or 3 kernels), rotate, FC1 and FC2 (one launch
-    # when fused), combine
-    launches_per_step = 5 if decode_path else 6 + (2 if R > 1024 else 0) - (1 if fused else 0)
+    launches_per_step = launches_per_layer_step(R, decode_path, fused)
     for m in moes:
         m.close()
     return {
