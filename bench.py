@@ -559,7 +559,7 @@ def run_linear(args, rank, world):
                      "achieved": round(achieved, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(achieved / pk["bf16_tflops"], 4),
                      # DRAM bytes of the projection launch from one ncu capture of this workload
-                     "traffic": 25.66e6 if (N, K, T) == (4096, 4096, 2048) else None,
+                     "traffic": 26.36e6 if (N, K, T) == (4096, 4096, 2048) else None,
                      "traffic_source": "profiles/k_tc_fc_fc2_linear_w4a16_N4096_T2048.md (k_tc_fc<FC2> launch)",
                      "peak_source": pk["source"] + " (bf16 dense burst; fp16 runs at the bf16 rate)",
                      "flops_per_launch": flops},
